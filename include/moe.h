@@ -1,0 +1,189 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) fused mixture-of-experts layer
+ * forward: router -> top-k gate -> dispatch -> expert FFN -> combine.
+ *
+ * The operation is the five-step MoE forward of the page "用Ascend C写一个
+ * MoE融合算子" (Writing a fused MoE operator in Ascend C), section
+ * "MoE的计算流程":
+ *   1. Routing   scores  = TopK(x × W_router)
+ *   2. Gating    weights = Softmax(scores)            (over the k selected)
+ *   3. Dispatch  x_e     = x[tokens assigned to e]
+ *   4. Expert    y_e     = GELU(x_e × W1_e) × W2_e    (section "2. Dispatch +
+ *                          Expert + Combine 流水线", listing "Expert计算")
+ *   5. Combine   y       = Σ_j weights_j × y_{e_j}     (listing "Scatter + 加权")
+ * with an optional capacity factor (article "CANN ops-transformer MoE",
+ * section 4.3, capacity_factor = 1.2) that drops an overloaded expert's
+ * assignments in ascending token order (page "CANN ops-transformer：MoE
+ * 路由算子的负载均衡策略", section "负载不均衡的根源", token dropping).
+ *
+ * Readings fixed by this library where the pages are silent:
+ *   - TopK: descending logit; equal logits -> lower expert index first.
+ *     Column j of ids/weights is the j-th best expert.
+ *   - Router logits and the gate softmax are fp32 (bf16 inputs, fp32
+ *     accumulation); an optional fp32 bias b[E] is added to the logits.
+ *   - GELU is the exact form 0.5 z (1 + erf(z / sqrt 2)).
+ *   - capacity C = ceil(capacity_factor * T * k / E - 1e-9) when
+ *     capacity_factor > 0, else unlimited.  The first C assignments of each
+ *     expert in ascending (token, slot) order are kept; dropped ones are not
+ *     re-routed and the survivors keep their softmax weight; a token whose
+ *     slots are all dropped gets y = 0.
+ *   - The expert hidden activation h and the expert output are rounded to
+ *     bf16 in the workspace; y is bf16 (round to nearest even) from an fp32
+ *     combine summed in slot order j = 0..k-1.
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers owned by the caller, row-major and
+ *     contiguous, 16-byte aligned.  bf16 tensors are passed as uint16_t bit
+ *     patterns.  The library never allocates, frees or retains memory.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous on that stream: they only enqueue work and never
+ *     synchronise the host, except moe_get_device_status.
+ *   - `ws` is a caller-owned device workspace of `ws_bytes` bytes, at least
+ *     moe_workspace_size() for moe_forward / moe_expert_ffn_combine and at
+ *     least MOE_WS_MIN_BYTES for moe_route / moe_dispatch; its first bytes
+ *     hold the device status word of the most recent call.  Concurrent calls
+ *     must not share a workspace.
+ *   - Return value: MOE_OK or an MOE_ERR_* code.  Arguments are validated on
+ *     the host before anything is enqueued; on an error nothing is launched
+ *     and moe_last_error_string() describes the problem.
+ *   - Faults found on the device (a bounded wait that ran out, an expert id
+ *     out of range) do not trap: kernels set bits in the status word, which
+ *     moe_get_device_status() reads back.
+ *
+ * Limits (MOE_ERR_UNSUPPORTED beyond them): 1 <= E <= 256, E % 8 == 0,
+ * 1 <= k <= min(8, E), H % 8 == 0, F % 8 == 0, H >= 8, F >= 8,
+ * T * k <= 2^24.  T == 0 is accepted and only clears counts/offsets.
+ */
+#ifndef MOE_GB300_MOE_H
+#define MOE_GB300_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG 1 /* null/misaligned pointer, bad size, small workspace */
+#define MOE_ERR_UNSUPPORTED 2 /* shape outside the limits above */
+#define MOE_ERR_CUDA 3        /* a CUDA runtime/driver call failed */
+#define MOE_ERR_TIMEOUT 4     /* moe_get_device_status: a device wait ran out */
+#define MOE_ERR_DEVICE 5      /* moe_get_device_status: another device fault bit */
+
+/* Device status bits (the word moe_get_device_status returns). */
+#define MOE_DEV_TIMEOUT 0x1 /* a kernel's bounded wait gave up */
+#define MOE_DEV_BAD_ID 0x2  /* an expert id outside [0, E) reached dispatch */
+
+/* Smallest workspace accepted by moe_route and moe_dispatch. */
+#define MOE_WS_MIN_BYTES 256
+
+typedef struct moe_shape {
+  int32_t T; /* tokens */
+  int32_t H; /* hidden size */
+  int32_t F; /* expert FFN width (ignored by moe_route / moe_dispatch) */
+  int32_t E; /* experts */
+  int32_t k; /* experts per token */
+  double capacity_factor; /* <= 0 or NaN: no capacity limit */
+} moe_shape;
+
+/* Library version, (major << 16) | minor. */
+MOE_API int moe_version(void);
+
+/* Message describing the last error returned on this host thread. */
+MOE_API const char* moe_last_error_string(void);
+
+/* Expert capacity C for the shape (see above), or -1 for no limit. */
+MOE_API int64_t moe_expert_capacity(const moe_shape* s);
+
+/* Workspace bytes needed by moe_forward and moe_expert_ffn_combine:
+ * the status word, h [T*k, F] bf16 and the expert outputs [T*k, H] bf16.
+ * Returns 0 for an invalid shape. */
+MOE_API size_t moe_workspace_size(const moe_shape* s);
+
+/*
+ * Steps 1-3 (the router kernel "MoERouterKernel::Process": x × W_router on
+ * the tensor cores, per-token TopK, Softmax over the k scores; then the
+ * dispatch of GatherTokensByExpert) for all T tokens.
+ *   x        [T, H]  bf16        w_router [H, E] bf16 (E contiguous)
+ *   b_router [E]     fp32 or NULL (added to the logits)
+ * Outputs (device, caller-owned):
+ *   ids      [T, k]  int32   selected experts, best first
+ *   weights  [T, k]  fp32    softmax over the k selected logits
+ *   counts   [E]     int32   kept assignments per expert (after capacity)
+ *   offsets  [E+1]   int32   exclusive prefix sum of counts
+ *   perm     [T*k]   int32   perm[offsets[e] + r] = t*k + j of the r-th kept
+ *                            assignment of expert e, tokens ascending;
+ *                            entries >= offsets[E] are -1
+ *   slot     [T, k]  int32   row of assignment (t, j) in perm, -1 if dropped
+ * The router logits never leave the chip.
+ */
+MOE_API int moe_route(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
+              const float* b_router, int32_t* ids, float* weights, int32_t* counts,
+              int32_t* offsets, int32_t* perm, int32_t* slot, void* ws, size_t ws_bytes,
+              void* stream);
+
+/*
+ * Step 3 alone (GatherTokensByExpert as a stable counting sort plus the
+ * capacity clip): ids [T, k] -> counts, offsets, perm, slot as in moe_route.
+ * Ids outside [0, E) are treated as dropped and set MOE_DEV_BAD_ID.
+ */
+MOE_API int moe_dispatch(const moe_shape* s, const int32_t* ids, int32_t* counts, int32_t* offsets,
+                 int32_t* perm, int32_t* slot, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Steps 4-5 (the expert kernel "MoEExpertKernel::Process" and its
+ * ScatterWithWeights, written as a gather): for every kept assignment,
+ * h = GELU(x[t] × W1[e]) and y_e = h × W2[e]; then
+ * y[t] = Σ_{j: slot[t,j] >= 0} weights[t,j] × y_e(t,j).
+ *   x [T, H] bf16, W1 [E, H, F] bf16 (F contiguous), W2 [E, F, H] bf16
+ *   (H contiguous); weights, offsets, perm, slot as produced by moe_route.
+ *   y [T, H] bf16 (output).
+ * perm/offsets must describe a valid dispatch (0 <= perm < T*k, offsets
+ * non-decreasing, offsets[E] <= T*k); the library does not re-validate them.
+ */
+MOE_API int moe_expert_ffn_combine(const moe_shape* s, const uint16_t* x, const uint16_t* w1,
+                           const uint16_t* w2, const float* weights, const int32_t* offsets,
+                           const int32_t* perm, const int32_t* slot, uint16_t* y, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/*
+ * The whole layer (the op "MoEFusion::Compute(x, w_router, expert_weights,
+ * y)" of section "3. 完整调用流程"): moe_route followed by
+ * moe_expert_ffn_combine, five kernels on `stream` and no host
+ * synchronisation.  The routing outputs are written as in moe_route.
+ */
+MOE_API int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
+                const float* b_router, const uint16_t* w1, const uint16_t* w2, uint16_t* y,
+                int32_t* ids, float* weights, int32_t* counts, int32_t* offsets, int32_t* perm,
+                int32_t* slot, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, reads the device status word of the workspace into
+ * *status and clears it.  Returns MOE_OK when the word is 0,
+ * MOE_ERR_TIMEOUT when MOE_DEV_TIMEOUT is set, MOE_ERR_DEVICE for other
+ * bits, MOE_ERR_CUDA if the copy fails.
+ */
+MOE_API int moe_get_device_status(void* ws, void* stream, int32_t* status);
+
+/*
+ * Self-test of the bounded-wait machinery, no counterpart on the pages:
+ * launches one CTA that waits on an mbarrier nobody arrives on, with a
+ * limit of `limit_ns` nanoseconds (1e3 .. 1e10), then records
+ * MOE_DEV_TIMEOUT in the workspace status word and returns.  Used by the
+ * failure-detection test; nothing traps or hangs.
+ */
+MOE_API int moe_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_MOE_H */

@@ -1,0 +1,260 @@
+"""GB300-native fused MoE layer forward: Python binding of libmoe.so.
+
+The entry points mirror the C ABI of ``include/moe.h`` name for name and
+only marshal arguments: torch tensors (device memory owned by the caller)
+become raw pointers, the stream defaults to torch's current stream, and a
+non-zero return code raises :class:`MoEError` with the library's message.
+Every step of the layer runs in the library's CUDA kernels; there is no
+other code path, and a missing library raises instead of falling back.
+
+The method is the five-step MoE forward of the page "用Ascend C写一个MoE
+融合算子", section "MoE的计算流程" (Routing, Gating, Dispatch, Expert,
+Combine); ``include/moe.h`` gives each entry point's definition.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_CUDA = 3
+MOE_ERR_TIMEOUT = 4
+MOE_ERR_DEVICE = 5
+MOE_DEV_TIMEOUT = 0x1
+MOE_DEV_BAD_ID = 0x2
+MOE_WS_MIN_BYTES = 256
+
+# Every symbol include/moe.h declares.
+EXPORTS = ("moe_version", "moe_last_error_string", "moe_expert_capacity", "moe_workspace_size",
+           "moe_route", "moe_dispatch", "moe_expert_ffn_combine", "moe_forward",
+           "moe_get_device_status", "moe_selftest_wait_timeout")
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"[moe error {code}] {message}")
+        self.code = code
+
+
+class moe_shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("F", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("capacity_factor", ctypes.c_double)]
+
+
+def make_shape(T: int, H: int, F: int, E: int, k: int, capacity_factor=None) -> moe_shape:
+    cf = -1.0 if capacity_factor is None else float(capacity_factor)
+    return moe_shape(int(T), int(H), int(F), int(E), int(k), cf)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Loads libmoe.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise ImportError(f"libmoe.so not found at {p}; run mixture_experts_layer_12_gb300/build.py "
+                              "(or __graft_entry__.build()) first")
+        lib = ctypes.CDLL(p)
+        P, S = ctypes.c_void_p, ctypes.POINTER(moe_shape)
+        sig = {
+            "moe_version": ([], ctypes.c_int),
+            "moe_last_error_string": ([], ctypes.c_char_p),
+            "moe_expert_capacity": ([S], ctypes.c_int64),
+            "moe_workspace_size": ([S], ctypes.c_size_t),
+            "moe_route": ([S, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
+            "moe_dispatch": ([S, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
+            "moe_expert_ffn_combine": ([S, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
+            "moe_forward": ([S, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
+            "moe_get_device_status": ([P, P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+            "moe_selftest_wait_timeout": ([P, ctypes.c_size_t, ctypes.c_uint64, P], ctypes.c_int),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(rc: int):
+    if rc != MOE_OK:
+        msg = load_library().moe_last_error_string().decode(errors="replace")
+        raise MoEError(rc, msg)
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device.type != "cuda" and t.numel() > 0:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+# ------------------------------------------------------------ C ABI names --
+
+def moe_version() -> int:
+    return load_library().moe_version()
+
+
+def moe_expert_capacity(shape: moe_shape) -> int:
+    return int(load_library().moe_expert_capacity(ctypes.byref(shape)))
+
+
+def moe_workspace_size(shape: moe_shape) -> int:
+    n = int(load_library().moe_workspace_size(ctypes.byref(shape)))
+    if n == 0:
+        _check(MOE_ERR_UNSUPPORTED)
+    return n
+
+
+def moe_route(shape, x, w_router, b_router, ids, weights, counts, offsets, perm, slot, ws,
+              stream=None):
+    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+    _check(load_library().moe_route(
+        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(w_router, bf, "w_router"),
+        _ptr(b_router, f32, "b_router"), _ptr(ids, i32, "ids"), _ptr(weights, f32, "weights"),
+        _ptr(counts, i32, "counts"), _ptr(offsets, i32, "offsets"), _ptr(perm, i32, "perm"),
+        _ptr(slot, i32, "slot"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+        _stream(stream)))
+
+
+def moe_dispatch(shape, ids, counts, offsets, perm, slot, ws, stream=None):
+    i32 = torch.int32
+    _check(load_library().moe_dispatch(
+        ctypes.byref(shape), _ptr(ids, i32, "ids"), _ptr(counts, i32, "counts"),
+        _ptr(offsets, i32, "offsets"), _ptr(perm, i32, "perm"), _ptr(slot, i32, "slot"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_expert_ffn_combine(shape, x, w1, w2, weights, offsets, perm, slot, y, ws, stream=None):
+    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+    _check(load_library().moe_expert_ffn_combine(
+        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(w1, bf, "w1"), _ptr(w2, bf, "w2"),
+        _ptr(weights, f32, "weights"), _ptr(offsets, i32, "offsets"), _ptr(perm, i32, "perm"),
+        _ptr(slot, i32, "slot"), _ptr(y, bf, "y"), _ptr(ws, None, "ws"),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_forward(shape, x, w_router, b_router, w1, w2, y, ids, weights, counts, offsets, perm,
+                slot, ws, stream=None):
+    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+    _check(load_library().moe_forward(
+        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(w_router, bf, "w_router"),
+        _ptr(b_router, f32, "b_router"), _ptr(w1, bf, "w1"), _ptr(w2, bf, "w2"),
+        _ptr(y, bf, "y"), _ptr(ids, i32, "ids"), _ptr(weights, f32, "weights"),
+        _ptr(counts, i32, "counts"), _ptr(offsets, i32, "offsets"), _ptr(perm, i32, "perm"),
+        _ptr(slot, i32, "slot"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+        _stream(stream)))
+
+
+def moe_get_device_status(ws, stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status word.
+    Raises MoEError if a status bit is set."""
+    v = ctypes.c_int32(0)
+    rc = load_library().moe_get_device_status(_ptr(ws, None, "ws"), _stream(stream), ctypes.byref(v))
+    if rc not in (MOE_OK,):
+        raise MoEError(rc, load_library().moe_last_error_string().decode(errors="replace"))
+    return v.value
+
+
+def moe_selftest_wait_timeout(ws, limit_ns: int, stream=None):
+    _check(load_library().moe_selftest_wait_timeout(
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), int(limit_ns), _stream(stream)))
+
+
+# --------------------------------------------------------------- helpers --
+
+@dataclass
+class RoutingBuffers:
+    ids: torch.Tensor
+    weights: torch.Tensor
+    counts: torch.Tensor
+    offsets: torch.Tensor
+    perm: torch.Tensor
+    slot: torch.Tensor
+
+
+def alloc_routing(T: int, E: int, k: int, device) -> RoutingBuffers:
+    i32 = dict(dtype=torch.int32, device=device)
+    return RoutingBuffers(ids=torch.empty(T, k, **i32),
+                          weights=torch.empty(T, k, dtype=torch.float32, device=device),
+                          counts=torch.empty(E, **i32), offsets=torch.empty(E + 1, **i32),
+                          perm=torch.empty(max(T * k, 1), **i32), slot=torch.empty(T, k, **i32))
+
+
+def alloc_workspace(shape: moe_shape, device) -> torch.Tensor:
+    n = max(moe_workspace_size(shape), MOE_WS_MIN_BYTES)
+    return torch.empty((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
+
+
+class MoELayer:
+    """Holds a layer's weights (device tensors) and reusable buffers; calling
+    it runs moe_forward on the current stream."""
+
+    def __init__(self, w_router, w1, w2, k: int, bias=None, capacity_factor=None):
+        self.w_router, self.w1, self.w2, self.bias = w_router, w1, w2, bias
+        self.E, self.H, self.F = w1.shape[0], w1.shape[1], w1.shape[2]
+        self.k = int(k)
+        self.capacity_factor = capacity_factor
+        self._T = None
+
+    def _ensure(self, T: int, device):
+        if self._T == T:
+            return
+        self.shape = make_shape(T, self.H, self.F, self.E, self.k, self.capacity_factor)
+        self.ws = alloc_workspace(self.shape, device)
+        self.routing = alloc_routing(T, self.E, self.k, device)
+        self.y = torch.empty(T, self.H, dtype=torch.bfloat16, device=device)
+        self._T = T
+
+    def __call__(self, x: torch.Tensor, stream=None) -> torch.Tensor:
+        self._ensure(x.shape[0], x.device)
+        r = self.routing
+        moe_forward(self.shape, x, self.w_router, self.bias, self.w1, self.w2, self.y, r.ids,
+                    r.weights, r.counts, r.offsets, r.perm, r.slot, self.ws, stream)
+        return self.y
+
+
+def capacity(T: int, E: int, k: int, capacity_factor) -> int:
+    """The library's expert capacity (-1 = unlimited), computed by the library."""
+    return moe_expert_capacity(make_shape(T, 8, 8, E, k, capacity_factor))
+
+
+def roofline_flops(N_rows: int, H: int, F: int) -> float:
+    """Algorithmic FLOPs of the two expert GEMMs for N_rows kept rows."""
+    return 4.0 * N_rows * H * F
+
+
+__all__ = [n for n in EXPORTS] + ["MoEError", "moe_shape", "make_shape", "load_library",
+                                   "alloc_routing", "alloc_workspace", "MoELayer", "RoutingBuffers",
+                                   "capacity", "roofline_flops"]

@@ -1,0 +1,425 @@
+// api.cu -- the C ABI declared in include/moe.h: argument validation,
+// workspace layout, TMA descriptor encoding and the launch sequence of the
+// fused MoE forward on the caller's stream.  No host synchronisation and no
+// allocation happen here (except moe_get_device_status, which syncs).
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "moe_internal.h"
+
+namespace moe {
+cudaError_t grouped_gemm_set_attributes();
+cudaError_t router_set_attributes();
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(MOE_ERR_CUDA, "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+}
+
+// ---------------------------------------------------------------- device --
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool ready;
+  int sms;
+};
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_setup(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_UNSUPPORTED, "device %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_dev[dev].ready) {
+    int major = 0, minor = 0, n = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3)
+      return fail(MOE_ERR_UNSUPPORTED, "built for sm_103a; device %d is sm_%d%d", dev, major, minor);
+    if ((e = router_set_attributes()) != cudaSuccess) return cuda_fail(e, "router attributes");
+    if ((e = grouped_gemm_set_attributes()) != cudaSuccess) return cuda_fail(e, "gemm attributes");
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    g_dev[dev].sms = n;
+    g_dev[dev].ready = true;
+  }
+  *sms = g_dev[dev].sms;
+  return MOE_OK;
+}
+
+// bf16 tensor map, 128-byte swizzle, zero fill out of bounds.
+int encode_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+               const uint64_t* strides_bytes, const uint32_t* box, const char* what) {
+  uint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
+                        dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(MOE_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
+  return MOE_OK;
+}
+
+int map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+           uint32_t box_outer, const char* what) {
+  const uint64_t dims[2] = {inner, outer};
+  const uint64_t strides[1] = {inner * 2};
+  const uint32_t box[2] = {box_inner, box_outer};
+  return encode_map(m, base, 2, dims, strides, box, what);
+}
+
+int map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+           uint32_t box0, uint32_t box1, const char* what) {
+  const uint64_t dims[3] = {d0, d1, d2};
+  const uint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const uint32_t box[3] = {box0, box1, 1};
+  return encode_map(m, base, 3, dims, strides, box, what);
+}
+
+// ------------------------------------------------------------ validation --
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(const moe_shape* s, bool need_ffn) {
+  if (!s) return fail(MOE_ERR_INVALID_ARG, "shape is null");
+  if (s->T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d < 0", s->T);
+  if (s->E < 1 || s->E > kMaxExperts || s->E % 8 != 0)
+    return fail(MOE_ERR_UNSUPPORTED, "E = %d: need 8 <= E <= %d and E %% 8 == 0", s->E, kMaxExperts);
+  if (s->k < 1 || s->k > kMaxTopK || s->k > s->E)
+    return fail(MOE_ERR_UNSUPPORTED, "k = %d: need 1 <= k <= min(8, E)", s->k);
+  if (s->H < 8 || s->H % 8 != 0) return fail(MOE_ERR_UNSUPPORTED, "H = %d: need H >= 8, H %% 8 == 0", s->H);
+  if (need_ffn && (s->F < 8 || s->F % 8 != 0))
+    return fail(MOE_ERR_UNSUPPORTED, "F = %d: need F >= 8, F %% 8 == 0", s->F);
+  if ((int64_t)s->T * s->k > (int64_t)1 << 24)
+    return fail(MOE_ERR_UNSUPPORTED, "T * k = %lld exceeds 2^24", (long long)s->T * s->k);
+  return MOE_OK;
+}
+
+#define REQUIRE_PTR(p)                                                               \
+  do {                                                                               \
+    if (!(p)) return fail(MOE_ERR_INVALID_ARG, "%s is null", #p);                    \
+    if (!aligned16(p)) return fail(MOE_ERR_INVALID_ARG, "%s is not 16-byte aligned", #p); \
+  } while (0)
+
+int64_t capacity_of(const moe_shape* s) {
+  const double cf = s->capacity_factor;
+  if (!(cf > 0.0)) return -1;
+  const double tk = (double)s->T * (double)s->k;
+  double c = ceil(cf * tk / (double)s->E - 1e-9);
+  if (c < 0.0) c = 0.0;
+  if (c > tk) c = tk;
+  return (int64_t)c;
+}
+
+// --------------------------------------------------------------- workspace --
+
+constexpr size_t kStatusBytes = 1024;  // status word + padding (keeps h 1024-aligned)
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+size_t h_bytes(const moe_shape* s) { return align_up((size_t)s->T * s->k * s->F * 2, 1024); }
+size_t y_bytes(const moe_shape* s) { return align_up((size_t)s->T * s->k * s->H * 2, 1024); }
+size_t ws_bytes_for(const moe_shape* s) { return kStatusBytes + h_bytes(s) + y_bytes(s); }
+
+int* status_ptr(void* ws) { return reinterpret_cast<int*>(ws); }
+uint16_t* h_ptr(void* ws) { return reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + kStatusBytes); }
+uint16_t* y_ptr(void* ws, const moe_shape* s) {
+  return reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + kStatusBytes + h_bytes(s));
+}
+
+// ------------------------------------------------------------------ steps --
+
+int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t* w_router,
+                  const float* b_router, int32_t* ids, float* weights, int32_t* counts,
+                  int32_t* offsets, int32_t* perm, int32_t* slot, void* ws, cudaStream_t st) {
+  int rc;
+  CUtensorMap tm_x, tm_w;
+  if ((rc = map_2d(&tm_x, x, (uint64_t)s->H, (uint64_t)s->T, 64, 128, "x (router)")) != MOE_OK) return rc;
+  if ((rc = map_2d(&tm_w, w_router, (uint64_t)s->E, (uint64_t)s->H, 64, 64, "w_router")) != MOE_OK) return rc;
+  RouterArgs ra;
+  ra.T = s->T;
+  ra.H = s->H;
+  ra.E = s->E;
+  ra.k = s->k;
+  ra.npad = (s->E + 15) / 16 * 16;
+  ra.tmem_cols = 32;
+  while (ra.tmem_cols < ra.npad) ra.tmem_cols *= 2;
+  const int mtiles = (s->T + 127) / 128;
+  const int kblocks = (s->H + 63) / 64;
+  ra.splits = 1;
+  while (ra.splits < 8 && mtiles * ra.splits * 2 <= sms && ra.splits * 2 <= kblocks) ra.splits *= 2;
+  ra.bias = b_router;
+  ra.ids = ids;
+  ra.weights = weights;
+  ra.status = status_ptr(ws);
+  ra.wait_limit_ns = kWaitLimitNs;
+  cudaError_t e = launch_router(tm_x, tm_w, ra, st);
+  if (e != cudaSuccess) return cuda_fail(e, "router launch");
+
+  DispatchArgs da;
+  da.ids = ids;
+  da.T = s->T;
+  da.k = s->k;
+  da.E = s->E;
+  da.capacity = (int)capacity_of(s);
+  da.counts = counts;
+  da.offsets = offsets;
+  da.perm = perm;
+  da.slot = slot;
+  da.status = status_ptr(ws);
+  e = launch_dispatch(da, st);
+  if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
+  return MOE_OK;
+}
+
+int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const uint16_t* w1,
+                        const uint16_t* w2, const float* weights, const int32_t* offsets,
+                        const int32_t* perm, const int32_t* slot, uint16_t* y, void* ws,
+                        cudaStream_t st) {
+  int rc;
+  const uint64_t rows = (uint64_t)s->T * s->k;
+  uint16_t* h = h_ptr(ws);
+  uint16_t* Y = y_ptr(ws, s);
+  CUtensorMap tm_xg, tm_w1, tm_h, tm_w2;
+  if ((rc = map_2d(&tm_xg, x, (uint64_t)s->H, (uint64_t)s->T, 64, 1, "x (gather)")) != MOE_OK) return rc;
+  if ((rc = map_3d(&tm_w1, w1, (uint64_t)s->F, (uint64_t)s->H, (uint64_t)s->E, 64, 64, "W1")) != MOE_OK) return rc;
+  if ((rc = map_2d(&tm_h, h, (uint64_t)s->F, rows, 64, 128, "h")) != MOE_OK) return rc;
+  if ((rc = map_3d(&tm_w2, w2, (uint64_t)s->H, (uint64_t)s->F, (uint64_t)s->E, 64, 64, "W2")) != MOE_OK) return rc;
+
+  const int64_t row_blocks_ub = ((int64_t)rows + kGemmBM - 1) / kGemmBM + s->E;
+  GemmArgs g;
+  g.offsets = offsets;
+  g.perm = perm;
+  g.k = s->k;
+  g.E = s->E;
+  g.T = s->T;
+  g.status = status_ptr(ws);
+  g.wait_limit_ns = kWaitLimitNs;
+
+  g.N = s->F;
+  g.K = s->H;
+  g.out = h;
+  int64_t ub = row_blocks_ub * ((s->F + kGemmBN - 1) / kGemmBN);
+  cudaError_t e = launch_grouped_gemm(true, tm_xg, tm_w1, g, (int)(ub < sms ? ub : sms), st);
+  if (e != cudaSuccess) return cuda_fail(e, "expert GEMM1 launch");
+
+  g.N = s->H;
+  g.K = s->F;
+  g.out = Y;
+  ub = row_blocks_ub * ((s->H + kGemmBN - 1) / kGemmBN);
+  e = launch_grouped_gemm(false, tm_h, tm_w2, g, (int)(ub < sms ? ub : sms), st);
+  if (e != cudaSuccess) return cuda_fail(e, "expert GEMM2 launch");
+
+  CombineArgs ca;
+  ca.Y = Y;
+  ca.w = weights;
+  ca.slot = slot;
+  ca.T = s->T;
+  ca.H = s->H;
+  ca.k = s->k;
+  ca.y = y;
+  e = launch_combine(ca, st);
+  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  return MOE_OK;
+}
+
+int clear_status(void* ws, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int), st);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "cudaMemsetAsync(status)");
+}
+
+int empty_routing(const moe_shape* s, int32_t* counts, int32_t* offsets, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)s->E, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (size_t)(s->E + 1), st);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "cudaMemsetAsync(counts/offsets)");
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+
+extern "C" {
+
+int moe_version(void) { return (1 << 16) | 0; }
+
+const char* moe_last_error_string(void) { return g_err; }
+
+int64_t moe_expert_capacity(const moe_shape* s) {
+  if (check_shape(s, false) != MOE_OK) return -1;
+  return capacity_of(s);
+}
+
+size_t moe_workspace_size(const moe_shape* s) {
+  if (check_shape(s, true) != MOE_OK) return 0;
+  return ws_bytes_for(s);
+}
+
+int moe_route(const moe_shape* s, const uint16_t* x, const uint16_t* w_router, const float* b_router,
+              int32_t* ids, float* weights, int32_t* counts, int32_t* offsets, int32_t* perm,
+              int32_t* slot, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_shape(s, false);
+  if (rc != MOE_OK) return rc;
+  REQUIRE_PTR(ws);
+  if (ws_bytes < MOE_WS_MIN_BYTES) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
+  REQUIRE_PTR(counts);
+  REQUIRE_PTR(offsets);
+  if (b_router && !aligned16(b_router)) return fail(MOE_ERR_INVALID_ARG, "b_router is not 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int sms = 0;
+  if ((rc = device_setup(&sms)) != MOE_OK) return rc;
+  if ((rc = clear_status(ws, st)) != MOE_OK) return rc;
+  if (s->T == 0) return empty_routing(s, counts, offsets, st);
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(w_router);
+  REQUIRE_PTR(ids);
+  REQUIRE_PTR(weights);
+  REQUIRE_PTR(perm);
+  REQUIRE_PTR(slot);
+  return enqueue_route(s, sms, x, w_router, b_router, ids, weights, counts, offsets, perm, slot, ws, st);
+}
+
+int moe_dispatch(const moe_shape* s, const int32_t* ids, int32_t* counts, int32_t* offsets,
+                 int32_t* perm, int32_t* slot, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_shape(s, false);
+  if (rc != MOE_OK) return rc;
+  REQUIRE_PTR(ws);
+  if (ws_bytes < MOE_WS_MIN_BYTES) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
+  REQUIRE_PTR(counts);
+  REQUIRE_PTR(offsets);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int sms = 0;
+  if ((rc = device_setup(&sms)) != MOE_OK) return rc;
+  if ((rc = clear_status(ws, st)) != MOE_OK) return rc;
+  if (s->T == 0) return empty_routing(s, counts, offsets, st);
+  REQUIRE_PTR(ids);
+  REQUIRE_PTR(perm);
+  REQUIRE_PTR(slot);
+  DispatchArgs da;
+  da.ids = ids;
+  da.T = s->T;
+  da.k = s->k;
+  da.E = s->E;
+  da.capacity = (int)capacity_of(s);
+  da.counts = counts;
+  da.offsets = offsets;
+  da.perm = perm;
+  da.slot = slot;
+  da.status = status_ptr(ws);
+  cudaError_t e = launch_dispatch(da, st);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "dispatch launch");
+}
+
+int moe_expert_ffn_combine(const moe_shape* s, const uint16_t* x, const uint16_t* w1,
+                           const uint16_t* w2, const float* weights, const int32_t* offsets,
+                           const int32_t* perm, const int32_t* slot, uint16_t* y, void* ws,
+                           size_t ws_bytes, void* stream) {
+  int rc = check_shape(s, true);
+  if (rc != MOE_OK) return rc;
+  REQUIRE_PTR(ws);
+  if (ws_bytes < ws_bytes_for(s))
+    return fail(MOE_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed", ws_bytes, ws_bytes_for(s));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int sms = 0;
+  if ((rc = device_setup(&sms)) != MOE_OK) return rc;
+  if ((rc = clear_status(ws, st)) != MOE_OK) return rc;
+  if (s->T == 0) return MOE_OK;
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(w1);
+  REQUIRE_PTR(w2);
+  REQUIRE_PTR(weights);
+  REQUIRE_PTR(offsets);
+  REQUIRE_PTR(perm);
+  REQUIRE_PTR(slot);
+  REQUIRE_PTR(y);
+  return enqueue_ffn_combine(s, sms, x, w1, w2, weights, offsets, perm, slot, y, ws, st);
+}
+
+int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
+                const float* b_router, const uint16_t* w1, const uint16_t* w2, uint16_t* y,
+                int32_t* ids, float* weights, int32_t* counts, int32_t* offsets, int32_t* perm,
+                int32_t* slot, void* ws, size_t ws_bytes, void* stream) {
+  int rc = check_shape(s, true);
+  if (rc != MOE_OK) return rc;
+  REQUIRE_PTR(ws);
+  if (ws_bytes < ws_bytes_for(s))
+    return fail(MOE_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed", ws_bytes, ws_bytes_for(s));
+  REQUIRE_PTR(counts);
+  REQUIRE_PTR(offsets);
+  if (b_router && !aligned16(b_router)) return fail(MOE_ERR_INVALID_ARG, "b_router is not 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int sms = 0;
+  if ((rc = device_setup(&sms)) != MOE_OK) return rc;
+  if ((rc = clear_status(ws, st)) != MOE_OK) return rc;
+  if (s->T == 0) return empty_routing(s, counts, offsets, st);
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(w_router);
+  REQUIRE_PTR(w1);
+  REQUIRE_PTR(w2);
+  REQUIRE_PTR(y);
+  REQUIRE_PTR(ids);
+  REQUIRE_PTR(weights);
+  REQUIRE_PTR(perm);
+  REQUIRE_PTR(slot);
+  rc = enqueue_route(s, sms, x, w_router, b_router, ids, weights, counts, offsets, perm, slot, ws, st);
+  if (rc != MOE_OK) return rc;
+  return enqueue_ffn_combine(s, sms, x, w1, w2, weights, offsets, perm, slot, y, ws, st);
+}
+
+int moe_get_device_status(void* ws, void* stream, int32_t* status) {
+  if (!ws || !status) return fail(MOE_ERR_INVALID_ARG, "ws/status is null");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(int32_t), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device status");
+  *status = v;
+  if (v == 0) return MOE_OK;
+  if (v & MOE_DEV_TIMEOUT) return fail(MOE_ERR_TIMEOUT, "a device wait timed out (status 0x%x)", v);
+  return fail(MOE_ERR_DEVICE, "device status 0x%x", v);
+}
+
+int moe_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns, void* stream) {
+  if (!ws || !aligned16(ws) || ws_bytes < MOE_WS_MIN_BYTES)
+    return fail(MOE_ERR_INVALID_ARG, "workspace null, misaligned or too small");
+  if (limit_ns < 1000ull || limit_ns > 10000000000ull)
+    return fail(MOE_ERR_INVALID_ARG, "limit_ns %llu outside [1e3, 1e10]", (unsigned long long)limit_ns);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int sms = 0;
+  int rc = device_setup(&sms);
+  if (rc != MOE_OK) return rc;
+  if ((rc = clear_status(ws, st)) != MOE_OK) return rc;
+  cudaError_t e = launch_wait_selftest(status_ptr(ws), limit_ns, st);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "self-test launch");
+}
+
+}  // extern "C"

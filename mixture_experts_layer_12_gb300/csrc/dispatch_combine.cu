@@ -1,0 +1,213 @@
+// dispatch_combine.cu -- token dispatch (stable counting sort by expert with
+// a capacity clip) and the gate-weighted combine.
+//
+// Dispatch restates GatherTokensByExpert of "用Ascend C写一个MoE融合算子"
+// (section "2. Dispatch + Expert + Combine 流水线", listing "Gather操作"):
+// expert e's rows are its assignments in ascending (token, slot) order, each
+// recorded with its original position (token_indices) and its top-k slot
+// (token_weight_indices) -- here packed as perm[r] = t*k + j, with the
+// inverse map slot[t][j].  Instead of one O(T*k) scan per expert, one pass
+// ranks every assignment among the earlier assignments of its expert
+// (warp match + per-warp counts + a scan across warps), which yields the
+// same order.  Assignments ranked at or beyond the capacity are dropped
+// (token dropping, "CANN ops-transformer：MoE 路由算子的负载均衡策略",
+// section "负载不均衡的根源"; capacity_factor of the article's section 4.3).
+//
+// Combine restates ScatterWithWeights (listing "Scatter + 加权":
+// output(orig_pos, d) += weight * expert_out(i, d), accumulated over the
+// token's k experts) as a gather: each token reads its kept rows, so no two
+// threads write the same output and no atomics are needed; the sum is fp32
+// in slot order j = 0..k-1.
+#include "tc_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int DTHREADS = 1024;
+constexpr int DWARPS = DTHREADS / 32;
+
+__global__ void __launch_bounds__(DTHREADS, 1) dispatch_kernel(const DispatchArgs a) {
+  __shared__ int s_cnt[kMaxExperts];
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_run[kMaxExperts];
+  __shared__ int s_wc[DWARPS * kMaxExperts];  // [warp][expert]
+  __shared__ int s_bad;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int E = a.E;
+  const int Tk = a.T * a.k;
+  const int cap = a.capacity;  // -1: unlimited
+
+  for (int e = tid; e < E; e += DTHREADS) {
+    s_cnt[e] = 0;
+    s_run[e] = 0;
+  }
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+
+  // 1. histogram of assignments per expert
+  for (int i = tid; i < Tk; i += DTHREADS) {
+    const int e = __ldg(a.ids + i);
+    if (e >= 0 && e < E)
+      atomicAdd(&s_cnt[e], 1);
+    else
+      s_bad = 1;
+  }
+  __syncthreads();
+
+  // 2. kept counts (capacity clip) and their exclusive scan (warp 0)
+  if (warp == 0) {
+    int loc[8];
+    int sum = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = lane * 8 + u;
+      int n = 0;
+      if (e < E) {
+        n = s_cnt[e];
+        if (cap >= 0) n = min(n, cap);
+      }
+      loc[u] = n;
+      sum += n;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = lane * 8 + u;
+      if (e < E) {
+        s_off[e] = run;
+        a.offsets[e] = run;
+        a.counts[e] = loc[u];
+      }
+      run += loc[u];
+    }
+    if (lane == 31) {
+      s_off[E] = incl;
+      a.offsets[E] = incl;
+    }
+  }
+  __syncthreads();
+
+  // 3. stable rank of every assignment within its expert, 1024 at a time
+  for (int base = 0; base < Tk; base += DTHREADS) {
+    for (int idx = tid; idx < DWARPS * E; idx += DTHREADS) s_wc[idx] = 0;
+    __syncthreads();
+    const int i = base + tid;
+    int e = -1;
+    if (i < Tk) {
+      e = __ldg(a.ids + i);
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank_w = __popc(peers & ((1u << lane) - 1u));
+    if (e >= 0 && rank_w == 0) s_wc[warp * E + e] = __popc(peers);
+    __syncthreads();
+    // exclusive scan across warps per expert, continuing the running count
+    for (int ee = tid; ee < E; ee += DTHREADS) {
+      int run = s_run[ee];
+      for (int w = 0; w < DWARPS; ++w) {
+        const int c = s_wc[w * E + ee];
+        s_wc[w * E + ee] = run;
+        run += c;
+      }
+      s_run[ee] = run;
+    }
+    __syncthreads();
+    if (i < Tk) {
+      int sl = -1;
+      if (e >= 0) {
+        const int r = s_wc[warp * E + e] + rank_w;
+        if (cap < 0 || r < cap) {
+          sl = s_off[e] + r;
+          a.perm[sl] = i;
+        }
+      }
+      a.slot[i] = sl;
+    }
+    __syncthreads();
+  }
+
+  // 4. unused tail of perm
+  for (int i = s_off[E] + tid; i < Tk; i += DTHREADS) a.perm[i] = -1;
+  if (tid == 0 && s_bad) record_status(a.status, MOE_DEV_BAD_ID);
+}
+
+constexpr int CTHREADS = 128;
+
+// y[t, c..c+7] = sum_j w[t,j] * Y[slot[t,j], c..c+7]; one thread per
+// 8 columns (16-byte loads and stores), grid (T, H / 1024 columns).
+__global__ void __launch_bounds__(CTHREADS) combine_kernel(const CombineArgs a) {
+  const int t = blockIdx.x;
+  const int col = (blockIdx.y * CTHREADS + threadIdx.x) * 8;
+  if (col >= a.H) return;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int j = 0; j < a.k; ++j) {
+    const int r = __ldg(a.slot + (size_t)t * a.k + j);
+    if (r < 0) continue;
+    const float wt = __ldg(a.w + (size_t)t * a.k + j);
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.Y + (size_t)r * a.H + col));
+    acc[0] = fmaf(wt, bf16_lo(v.x), acc[0]);
+    acc[1] = fmaf(wt, bf16_hi(v.x), acc[1]);
+    acc[2] = fmaf(wt, bf16_lo(v.y), acc[2]);
+    acc[3] = fmaf(wt, bf16_hi(v.y), acc[3]);
+    acc[4] = fmaf(wt, bf16_lo(v.z), acc[4]);
+    acc[5] = fmaf(wt, bf16_hi(v.z), acc[5]);
+    acc[6] = fmaf(wt, bf16_lo(v.w), acc[6]);
+    acc[7] = fmaf(wt, bf16_hi(v.w), acc[7]);
+  }
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  *reinterpret_cast<uint4*>(a.y + (size_t)t * a.H + col) = o;
+}
+
+// One thread waits on an mbarrier that nothing arrives on; the bounded wait
+// gives up after limit_ns, records MOE_DEV_TIMEOUT and the kernel returns.
+__global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const WaitCtl wc{&abort_flag, status, limit_ns};
+    (void)mbar_wait(&bar, 0, wc);
+  }
+  __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st) {
+  dispatch_kernel<<<1, DTHREADS, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
+  const int cols_per_block = CTHREADS * 8;
+  dim3 grid((unsigned)a.T, (unsigned)((a.H + cols_per_block - 1) / cols_per_block), 1);
+  combine_kernel<<<grid, CTHREADS, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,386 @@
+// ffn_gemm.cu -- grouped expert GEMM on the 5th-generation tensor cores.
+//
+// Computes, for every expert e and every dispatch row r of e
+// (offsets[e] <= r < offsets[e+1]):
+//   GEMM1 (gather + GELU):  h[r, :] = GELU(x[perm[r] / k, :] · W1[e])
+//   GEMM2 (plain):          Y[r, :] = h[r, :] · W2[e]
+// which are the two Mmad calls of the expert kernel in "用Ascend C写一个
+// MoE融合算子", section "2. Dispatch + Expert + Combine 流水线" (listing
+// "Expert计算": M = tokens of the expert, N = ffn_hidden_dim, K = hidden_dim,
+// then N = hidden_dim, K = ffn_hidden_dim, with GELU in between).
+//
+// Design (sm_103a):
+//   * persistent CTAs, one per SM; tiles of 128 rows x 256 columns; the
+//     tile list is ragged per expert (ceil(n_e/128) row blocks) and is built
+//     on the device from `offsets`, so no host synchronisation is needed.
+//     Tiles are ordered expert-major, row-block fastest, so CTAs working at
+//     the same time share the expert's weight columns through L2 (the
+//     pages' expert-block / token-block tiling, made ragged).
+//   * warp 0: TMA producer.  The A tile of GEMM1 is gathered straight from
+//     x with tile::gather4 (4 token rows per lane, 32 lanes = 128 rows), so
+//     no permuted copy of x exists; GEMM2 reads contiguous rows of h.  The
+//     weight tile is four 64-column boxes of W[e] (N contiguous, MN-major).
+//   * warp 1: allocates 512 TMEM columns (two 128x256 fp32 accumulators)
+//     and one thread issues tcgen05.mma (M=128, N=256, K=16) from a 4-stage
+//     shared-memory ring (load / compute / store overlap of the article's
+//     section 2.2 pipeline).
+//   * warps 2-9: epilogue; tcgen05.ld of the accumulator, GELU(erf) for
+//     GEMM1, bf16 rounding and 16-byte stores; double-buffered against the
+//     next tile's MMAs.
+// Every mbarrier wait is bounded (MOE_DEV_TIMEOUT on expiry).
+#include "tc_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = kGemmBM;
+constexpr int BN = kGemmBN;
+constexpr int BK = kGemmBK;
+constexpr int STAGES = 4;
+constexpr int ACC = 2;
+constexpr int A_BYTES = BM * BK * 2;   // 16 KB: 128 rows x 128 B
+constexpr int B_CHUNK = BK * 64 * 2;   // 8 KB: one 64-column box, 64 K rows
+constexpr int B_BYTES = (BN / 64) * B_CHUNK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 32 * (2 + EPI_WARPS);
+constexpr int TMEM_COLS = ACC * BN;  // 512
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, /*a_mn=*/false, /*b_mn=*/true);
+
+static_assert(BK == 64, "one 128-byte swizzle atom of K per stage");
+static_assert(BN % 64 == 0 && BN <= 256, "UMMA N");
+static_assert(TMEM_COLS <= 512, "TMEM capacity");
+
+struct Ctrl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[ACC];
+  uint64_t tempty[ACC];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int n_tiles;
+  int tile_start[kMaxExperts + 1];
+  int mblocks[kMaxExperts];
+  int row_off[kMaxExperts];
+  int rows[kMaxExperts];
+};
+
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctrl);
+
+struct Tile {
+  int e, nb, row0, rows_valid;
+};
+
+// Tiles of one CTA increase monotonically, so the expert cursor only moves
+// forward; experts without rows own no tiles and are skipped.
+__device__ __forceinline__ Tile decode_tile(const Ctrl& c, int tile, int& e) {
+  while (tile >= c.tile_start[e + 1]) ++e;
+  const int local = tile - c.tile_start[e];
+  const int mbs = c.mblocks[e];
+  const int mb = local % mbs;
+  Tile t;
+  t.e = e;
+  t.nb = local / mbs;
+  t.row0 = c.row_off[e] + mb * BM;
+  t.rows_valid = min(BM, c.rows[e] - mb * BM);
+  return t;
+}
+
+// Wait that ignores the abort flag (used to drain in-flight copies and
+// MMAs before the CTA releases its shared memory and TMEM); still bounded.
+__device__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns, int* status) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) {
+      record_status(status, MOE_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ float gelu_erf(float z) {
+  return 0.5f * z * (1.0f + erff(z * 0.70710678118654752440f));
+}
+
+template <bool GATHER_GELU>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                        const __grid_constant__ CUtensorMap tm_b, const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  Ctrl& c = *reinterpret_cast<Ctrl*>(smem + STAGES * STAGE_BYTES);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int NB = (p.N + BN - 1) / BN;
+  const int KB = (p.K + BK - 1) / BK;
+
+  // ---- tile schedule from the dispatch offsets (warp 0), barriers (warp 1)
+  if (warp == 0) {
+    int cnt[8];
+    int sum = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = lane * 8 + u;
+      cnt[u] = 0;
+      if (e < p.E) {
+        const int o0 = __ldg(p.offsets + e);
+        const int n = max(__ldg(p.offsets + e + 1) - o0, 0);
+        const int mbs = (n + BM - 1) / BM;
+        c.row_off[e] = o0;
+        c.rows[e] = n;
+        c.mblocks[e] = mbs;
+        cnt[u] = mbs * NB;
+      }
+      sum += cnt[u];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = lane * 8 + u;
+      if (e < p.E) c.tile_start[e] = run;
+      run += cnt[u];
+    }
+    if (lane == 31) {
+      c.tile_start[p.E] = incl;
+      c.n_tiles = incl;
+    }
+  } else if (threadIdx.x == 32) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&c.full[i], 1);
+      mbar_init(&c.empty[i], 1);
+    }
+    for (int i = 0; i < ACC; ++i) {
+      mbar_init(&c.tfull[i], 1);
+      mbar_init(&c.tempty[i], EPI_WARPS);
+    }
+    mbar_init(&c.drain, 1);
+    c.abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int n_tiles = c.n_tiles;
+  if ((int)blockIdx.x >= n_tiles) return;  // uniform: nothing allocated yet
+
+  if (warp == 1) {
+    tmem_alloc(&c.tmem_base, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = c.tmem_base;
+  const WaitCtl wc{&c.abort_flag, p.status, p.wait_limit_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer warp
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_a);
+      tma_prefetch_desc(&tm_b);
+    }
+    int stage = 0;
+    uint32_t phase = 0;
+    int armed = 0;
+    int e = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile(c, tile, e);
+      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+      if constexpr (GATHER_GELU) {
+        // rows 4*lane .. 4*lane+3 of the tile; rows past the expert's end
+        // repeat its last row (computed, never stored)
+        int rr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = t.row0 + min(4 * lane + i, t.rows_valid - 1);
+          const int tok = __ldg(p.perm + row) / p.k;
+          rr[i] = min(max(tok, 0), p.T - 1);
+        }
+        r0 = rr[0];
+        r1 = rr[1];
+        r2 = rr[2];
+        r3 = rr[3];
+      }
+      bool ok = true;
+      for (int kb = 0; kb < KB; ++kb) {
+        int got = 1;
+        if (lane == 0) {
+          got = mbar_wait(&c.empty[stage], phase ^ 1u, wc);
+          if (got) mbar_arrive_expect_tx(&c.full[stage], STAGE_BYTES);
+        }
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        uint8_t* a = sA + stage * A_BYTES;
+        uint8_t* b = sB + stage * B_BYTES;
+        if constexpr (GATHER_GELU) {
+          tma_gather4(a + lane * 4 * 128, &tm_a, &c.full[stage], kb * BK, r0, r1, r2, r3);
+        } else {
+          if (lane == 0) tma_load_2d(a, &tm_a, &c.full[stage], kb * BK, t.row0);
+        }
+        if (lane < BN / 64)
+          tma_load_3d(b + lane * B_CHUNK, &tm_b, &c.full[stage], t.nb * BN + lane * 64, kb * BK,
+                      t.e);
+        ++armed;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+    }
+    // Drain: every armed stage's bytes must have landed before this CTA's
+    // shared memory can be released (a no-op on the normal path).
+    if (lane == 0) {
+      for (int m = max(0, armed - STAGES); m < armed; ++m)
+        mbar_wait_drain(&c.full[m % STAGES], (uint32_t)((m / STAGES) & 1), p.wait_limit_ns,
+                        p.status);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&c.tempty[acc], acc_phase ^ 1u, wc)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&c.full[stage], phase, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int j = 0; j < BK / 16; ++j) {
+            // A: K-major, advance 16 elements = 32 bytes inside the swizzle row.
+            // B: MN-major, advance 16 K rows = two 1024-byte atoms.
+            const uint64_t ad = sdesc_sw128(a0 + j * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b0 + j * 2048, B_CHUNK, 1024);
+            umma_bf16(d, ad, bd, IDESC, (kb | j) != 0 ? 1u : 0u);
+          }
+          umma_commit(&c.empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&c.tfull[acc]);
+        if (++acc == ACC) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // all MMAs issued by this thread have completed once `drain` fires
+      umma_commit(&c.drain);
+      mbar_wait_drain(&c.drain, 0, p.wait_limit_ns, p.status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ epilogue warps
+    const int q = warp & 3;            // TMEM lane quadrant this warp may read
+    const int half = (warp - 2) >> 2;  // column half of the 256-wide tile
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int e = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile(c, tile, e);
+      int got = 1;
+      if (lane == 0) got = mbar_wait(&c.tfull[acc], acc_phase, wc);
+      got = __shfl_sync(0xffffffffu, got, 0);
+      if (!got) break;
+      tc_fence_after();
+      const int row = q * 32 + lane;
+      const bool row_ok = row < t.rows_valid;
+      uint16_t* orow = p.out + (size_t)(t.row0 + (row_ok ? row : 0)) * (size_t)p.N;
+      const uint32_t tbase = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        const int col = half * 128 + ch * 32;
+        uint32_t v[32];
+        tmem_ld_x32(tbase + (uint32_t)col, v);
+        tmem_ld_wait();
+        const int gcol = t.nb * BN + col;
+        if (row_ok) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            if (gcol + g * 8 + 8 <= p.N) {
+              float f[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                f[i] = __uint_as_float(v[g * 8 + i]);
+                if constexpr (GATHER_GELU) f[i] = gelu_erf(f[i]);
+              }
+              uint4 pk;
+              pk.x = pack_bf16x2(f[0], f[1]);
+              pk.y = pack_bf16x2(f[2], f[3]);
+              pk.z = pack_bf16x2(f[4], f[5]);
+              pk.w = pack_bf16x2(f[6], f[7]);
+              *reinterpret_cast<uint4*>(orow + gcol + g * 8) = pk;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&c.tempty[acc]);
+      if (++acc == ACC) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+size_t grouped_gemm_smem_bytes() { return SMEM_BYTES; }
+
+cudaError_t launch_grouped_gemm(bool gather_gelu, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                const GemmArgs& a, int grid, cudaStream_t st) {
+  if (grid <= 0) return cudaSuccess;
+  if (gather_gelu) {
+    grouped_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, st>>>(tm_a, tm_b, a);
+  } else {
+    grouped_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(tm_a, tm_b, a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t grouped_gemm_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(grouped_gemm_kernel<false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+}
+
+}  // namespace moe

@@ -1,0 +1,86 @@
+// moe_internal.h -- launch interfaces between the C ABI (api.cu) and the
+// kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+
+// Default limit of every bounded device wait (one second).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// ---- router: logits (tcgen05, split-K over a thread-block cluster),
+//      TopK and the top-k softmax, fused; logits stay on chip.
+struct RouterArgs {
+  int T, H, E, k;
+  int npad;        // E rounded up to 16 (the MMA N)
+  int tmem_cols;   // power of two >= max(32, npad)
+  int splits;      // cluster size along K (1, 2, 4 or 8)
+  const float* bias;  // [E] or null
+  int32_t* ids;       // [T, k]
+  float* weights;     // [T, k]
+  int* status;
+  uint64_t wait_limit_ns;
+};
+// Launches ceil(T/128) x splits CTAs in clusters of `splits`.
+// tm_x: x [T, H] bf16, box {64, 128}, 128B swizzle.
+// tm_w: w_router [H, E] bf16, box {64, 64}, 128B swizzle.
+cudaError_t launch_router(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterArgs& a,
+                          cudaStream_t st);
+size_t router_smem_bytes(int E);
+
+// ---- dispatch: histogram, capacity clip, scan, stable counting sort.
+struct DispatchArgs {
+  const int32_t* ids;
+  int T, k, E;
+  int capacity;  // -1: unlimited
+  int32_t *counts, *offsets, *perm, *slot;
+  int* status;
+};
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st);
+
+// ---- grouped expert GEMM (tcgen05 + TMA, persistent ragged scheduler).
+struct GemmArgs {
+  const int32_t* offsets;  // [E+1] dispatch offsets (device)
+  const int32_t* perm;     // gather mode: token row of output row r is perm[r] / k
+  int k;
+  int E;
+  int N;                   // output columns
+  int K;                   // reduction length
+  int T;                   // rows of the gathered tensor (gather mode)
+  uint16_t* out;           // [rows, N] bf16, row r = dispatch row
+  int* status;
+  uint64_t wait_limit_ns;
+};
+// GEMM1: A rows gathered from x through perm, GELU epilogue.
+//   tm_a: x [T, H], box {64, 1} (gather4), tm_b: W1 [E, H, F] box {64, 64, 1}.
+// GEMM2: A rows contiguous (dispatch order), no activation.
+//   tm_a: h [T*k, F], box {64, 128}, tm_b: W2 [E, F, H] box {64, 64, 1}.
+cudaError_t launch_grouped_gemm(bool gather_gelu, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                const GemmArgs& a, int grid, cudaStream_t st);
+size_t grouped_gemm_smem_bytes();
+constexpr int kGemmBM = 128;
+constexpr int kGemmBN = 256;
+constexpr int kGemmBK = 64;
+
+// ---- combine: y[t] = sum_j w[t,j] * Y[slot[t,j]] (fp32), bf16 out.
+struct CombineArgs {
+  const uint16_t* Y;  // [rows, H]
+  const float* w;     // [T, k]
+  const int32_t* slot;
+  int T, H, k;
+  uint16_t* y;
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
+
+// ---- bounded-wait self test.
+cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st);
+
+}  // namespace moe

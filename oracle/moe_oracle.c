@@ -81,19 +81,33 @@ int oracle_router_logits(int T, int H, int E, const uint16_t *x,
 {
     if (T < 0 || H < 1 || E < 1 || !x || !w_router || !logits) return 1;
     set_threads(nthreads);
-#pragma omp parallel for schedule(static)
-    for (int t = 0; t < T; t++) {
-        for (int e = 0; e < E; e++) {
-            double acc = 0.0;
-            for (int h = 0; h < H; h++)
-                acc += bf16_value(x[(size_t)t * H + h]) *
-                       bf16_value(w_router[(size_t)h * E + e]);
-            float l = (float)acc;
-            if (bias) l = l + bias[e];
-            logits[(size_t)t * E + e] = l;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *acc = (double *)malloc(sizeof(double) * (size_t)E);
+        if (!acc) {
+#pragma omp atomic write
+            bad = 2;
         }
+#pragma omp for schedule(static)
+        for (int t = 0; t < T; t++) {
+            if (!acc) continue;
+            /* acc[e] accumulates over h in ascending order for every e */
+            for (int e = 0; e < E; e++) acc[e] = 0.0;
+            for (int h = 0; h < H; h++) {
+                double xv = bf16_value(x[(size_t)t * H + h]);
+                for (int e = 0; e < E; e++)
+                    acc[e] += xv * bf16_value(w_router[(size_t)h * E + e]);
+            }
+            for (int e = 0; e < E; e++) {
+                float l = (float)acc[e];
+                if (bias) l = l + bias[e];
+                logits[(size_t)t * E + e] = l;
+            }
+        }
+        free(acc);
     }
-    return 0;
+    return bad;
 }
 
 /*
@@ -217,17 +231,24 @@ static void expert_ffn_row(int H, int F, const uint16_t *xrow,
                            const uint16_t *w1e, const uint16_t *w2e,
                            double *g, double *out)
 {
+    /* u[f] = sum_h x[h] * W1[h][f], accumulated over h in ascending order
+     * (the loops run h-outer only so that W1 is read row by row) */
+    for (int f = 0; f < F; f++) g[f] = 0.0;
+    for (int h = 0; h < H; h++) {
+        double xv = bf16_value(xrow[h]);
+        const uint16_t *w1row = w1e + (size_t)h * F;
+        for (int f = 0; f < F; f++) g[f] += xv * bf16_value(w1row[f]);
+    }
     for (int f = 0; f < F; f++) {
-        double u = 0.0;
-        for (int h = 0; h < H; h++)
-            u += bf16_value(xrow[h]) * bf16_value(w1e[(size_t)h * F + f]);
+        double u = g[f];
         g[f] = 0.5 * u * (1.0 + erf(u / sqrt(2.0)));
     }
-    for (int h = 0; h < H; h++) {
-        double v = 0.0;
-        for (int f = 0; f < F; f++)
-            v += g[f] * bf16_value(w2e[(size_t)f * H + h]);
-        out[h] = v;
+    /* out[h] = sum_f g[f] * W2[f][h], accumulated over f in ascending order */
+    for (int h = 0; h < H; h++) out[h] = 0.0;
+    for (int f = 0; f < F; f++) {
+        double gv = g[f];
+        const uint16_t *w2row = w2e + (size_t)f * H;
+        for (int h = 0; h < H; h++) out[h] += gv * bf16_value(w2row[h]);
     }
 }
 

@@ -1,0 +1,109 @@
+"""The C ABI library: builds, loads, exports what include/moe.h declares, and
+validates arguments on the host (no GPU needed: every call below is rejected
+before the library touches CUDA)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_layer_12_gb300 as moe
+from mixture_experts_layer_12_gb300 import build as moe_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe_build.build()
+    return moe.load_library()
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        src = f.read()
+    return set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", src))
+
+
+def exported_symbols(path):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    return {line.split()[-1] for line in out.splitlines() if line.strip()}
+
+
+def test_exports_match_header(lib):
+    decl = declared_symbols()
+    assert len(decl) == 10
+    assert decl == set(moe.EXPORTS)
+    exported = {s for s in exported_symbols(moe.LIB_PATH) if s.startswith("moe_")}
+    assert exported == decl
+    for name in decl:
+        assert getattr(lib, name) is not None
+
+
+def test_version(lib):
+    assert moe.moe_version() >> 16 == 1
+
+
+def test_workspace_size_and_capacity_host_only(lib):
+    s = moe.make_shape(4096, 4096, 14336, 8, 2)
+    # status block + h [T*k, F] + Y [T*k, H], bf16
+    assert moe.moe_workspace_size(s) == 1024 + 8192 * 14336 * 2 + 8192 * 4096 * 2
+    assert moe.moe_expert_capacity(moe.make_shape(8192, 2048, 1408, 64, 4, 1.2)) == 615
+    assert moe.moe_expert_capacity(moe.make_shape(8192, 2048, 1408, 64, 4, None)) == -1
+    assert moe.moe_expert_capacity(moe.make_shape(64, 128, 256, 8, 2, 1.0)) == 16
+
+
+@pytest.mark.parametrize("T,k,E,cf", [(8192, 4, 64, 1.2), (64, 2, 8, 1.0), (10, 1, 8, 0.8),
+                                      (3, 2, 8, 1.0), (100, 8, 256, 0.37), (7, 3, 16, float("nan"))])
+def test_capacity_matches_oracle(lib, T, k, E, cf):
+    import oracle
+    assert moe.moe_expert_capacity(moe.make_shape(T, 8, 8, E, k, cf)) == oracle.capacity(T, k, E, cf)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(E=7), moe.MOE_ERR_UNSUPPORTED), (dict(E=264), moe.MOE_ERR_UNSUPPORTED),
+    (dict(k=9), moe.MOE_ERR_UNSUPPORTED), (dict(k=0), moe.MOE_ERR_UNSUPPORTED),
+    (dict(H=100), moe.MOE_ERR_UNSUPPORTED), (dict(F=12), moe.MOE_ERR_UNSUPPORTED),
+    (dict(T=-1), moe.MOE_ERR_INVALID_ARG), (dict(T=1 << 22, k=8), moe.MOE_ERR_UNSUPPORTED),
+])
+def test_bad_shapes_rejected_before_launch(lib, kw, code):
+    base = dict(T=64, H=128, F=256, E=8, k=2)
+    base.update(kw)
+    s = moe.make_shape(**base)
+    assert lib.moe_workspace_size(ctypes.byref(s)) == 0
+    rc = lib.moe_forward(ctypes.byref(s), *([None] * 13), 0, None)
+    assert rc == code
+    assert lib.moe_last_error_string()
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    s = moe.make_shape(64, 128, 256, 8, 2)
+    ws_need = lib.moe_workspace_size(ctypes.byref(s))
+    # null workspace
+    rc = lib.moe_forward(ctypes.byref(s), *([None] * 13), ws_need, None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    assert b"ws" in lib.moe_last_error_string()
+    # misaligned workspace pointer (never dereferenced: rejected on the host)
+    rc = lib.moe_forward(ctypes.byref(s), *([None] * 12), ctypes.c_void_p(0x1008), ws_need, None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    # workspace too small
+    rc = lib.moe_forward(ctypes.byref(s), *([None] * 12), ctypes.c_void_p(0x1000), ws_need - 16, None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    assert b"workspace" in lib.moe_last_error_string()
+    # route: null counts
+    rc = lib.moe_route(ctypes.byref(s), *([None] * 9), ctypes.c_void_p(0x1000), 4096, None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    # self-test limit outside its range
+    rc = lib.moe_selftest_wait_timeout(ctypes.c_void_p(0x1000), 4096, 10, None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+
+
+def test_python_binding_rejects_host_tensors(lib):
+    import torch
+    s = moe.make_shape(4, 8, 8, 8, 2)
+    with pytest.raises((ValueError, TypeError)):
+        moe.moe_dispatch(s, torch.zeros(4, 2, dtype=torch.int32), torch.zeros(8, dtype=torch.int32),
+                         torch.zeros(9, dtype=torch.int32), torch.zeros(8, dtype=torch.int32),
+                         torch.zeros(4, 2, dtype=torch.int32), torch.zeros(256, dtype=torch.uint8))

@@ -1,0 +1,281 @@
+"""CUDA path vs the oracle, element by element, through the C ABI.
+
+Small workloads compare every row; the full-size workloads compare routing
+and dispatch for every token and y on every 16th token (tokens are
+independent once routed and dispatched), in the same launch configuration
+bench.py times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_synth
+import oracle
+import mixture_experts_layer_12_gb300 as moe
+from parity import check_dispatch, check_routing, check_y, reference_y
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from mixture_experts_layer_12_gb300 import build
+    build.build()
+    oracle.build()
+    moe.load_library()
+
+
+def to_dev(inputs):
+    return {k: (None if v is None else v.to(DEV)) for k, v in inputs.items()}
+
+
+def gpu_route(cfg, dev_in):
+    s = moe.make_shape(cfg.T, cfg.H, max(cfg.F, 8), cfg.E, cfg.k, cfg.capacity_factor)
+    r = moe.alloc_routing(cfg.T, cfg.E, cfg.k, DEV)
+    ws = torch.empty(1024, dtype=torch.uint8, device=DEV)
+    moe.moe_route(s, dev_in["x"], dev_in["w_router"], dev_in["bias"], r.ids, r.weights, r.counts,
+                  r.offsets, r.perm, r.slot, ws)
+    assert moe.moe_get_device_status(ws) == 0
+    return r
+
+
+def gpu_forward(cfg, dev_in):
+    layer = moe.MoELayer(dev_in["w_router"], dev_in["w1"], dev_in["w2"], cfg.k, bias=dev_in["bias"],
+                         capacity_factor=cfg.capacity_factor)
+    y = layer(dev_in["x"])
+    assert moe.moe_get_device_status(layer.ws) == 0
+    return layer, y
+
+
+def np_(t):
+    return t.detach().cpu().numpy()
+
+
+def routing_parity(cfg, inputs, r, nthreads=0):
+    logits = oracle.router_logits(inputs["x"], inputs["w_router"], inputs["bias"], nthreads)
+    o_ids, o_vals = oracle.topk(logits, cfg.k)
+    o_w = oracle.gate_softmax(o_vals)
+    gids = np_(r.ids)
+    rep = check_routing(logits, o_ids, o_w, gids, np_(r.weights))
+    rep.update(check_dispatch(gids, cfg.E, cfg.capacity_factor, np_(r.counts), np_(r.offsets),
+                              np_(r.perm), np_(r.slot)))
+    return logits, rep
+
+
+def forward_parity(cfg, stride=1, nthreads=0):
+    inputs = moe_synth.make_inputs(cfg)
+    dev_in = to_dev(inputs)
+    layer, y = gpu_forward(cfg, dev_in)
+    logits, rep = routing_parity(cfg, inputs, layer.routing, nthreads)
+    rows = np.arange(0, cfg.T, stride, dtype=np.int32)
+    y_ref = reference_y(inputs, logits, np_(layer.routing.ids), np_(layer.routing.slot), rows, nthreads)
+    y_gpu = y.float().cpu().numpy()[rows]
+    rep.update(check_y(y_gpu, y_ref))
+    print(cfg.name, rep)
+    return rep
+
+
+# ------------------------------------------------------------- self test --
+
+def test_bounded_wait_times_out_and_reports():
+    ws = torch.empty(1024, dtype=torch.uint8, device=DEV)
+    moe.moe_selftest_wait_timeout(ws, 2_000_000)  # 2 ms
+    with pytest.raises(moe.MoEError) as e:
+        moe.moe_get_device_status(ws)
+    assert e.value.code == moe.MOE_ERR_TIMEOUT
+    # the context stays usable and the status word was cleared
+    assert moe.moe_get_device_status(ws) == 0
+    assert torch.ones(4, device=DEV).sum().item() == 4.0
+
+
+# --------------------------------------------------------------- dispatch --
+
+@pytest.mark.parametrize("T,E,k,cf,skew", [
+    (1, 8, 1, None, False), (7, 8, 2, None, False), (1000, 64, 4, 1.0, True),
+    (8192, 64, 4, 1.2, True), (3000, 256, 8, None, False), (2048, 128, 8, 0.5, False),
+    (4096, 8, 2, None, True), (513, 16, 3, 0.05, False),
+])
+def test_dispatch_fed_oracle_ids(T, E, k, cf, skew):
+    rng = np.random.default_rng(T + E + k)
+    if skew:
+        p = np.full(E, 1.0)
+        p[0] = 20.0 * E
+        p /= p.sum()
+    else:
+        p = None
+    ids = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
+    s = moe.make_shape(T, 8, 8, E, k, cf)
+    r = moe.alloc_routing(T, E, k, DEV)
+    ws = torch.empty(1024, dtype=torch.uint8, device=DEV)
+    moe.moe_dispatch(s, torch.from_numpy(ids).to(DEV), r.counts, r.offsets, r.perm, r.slot, ws)
+    assert moe.moe_get_device_status(ws) == 0
+    check_dispatch(ids, E, cf, np_(r.counts), np_(r.offsets), np_(r.perm), np_(r.slot))
+
+
+def test_dispatch_bad_ids_flagged():
+    ids = torch.tensor([[0, 9], [3, 1]], dtype=torch.int32, device=DEV)
+    s = moe.make_shape(2, 8, 8, 8, 2)
+    r = moe.alloc_routing(2, 8, 2, DEV)
+    ws = torch.empty(1024, dtype=torch.uint8, device=DEV)
+    moe.moe_dispatch(s, ids, r.counts, r.offsets, r.perm, r.slot, ws)
+    with pytest.raises(moe.MoEError) as e:
+        moe.moe_get_device_status(ws)
+    assert e.value.code == moe.MOE_ERR_DEVICE
+    assert np_(r.slot)[0, 1] == -1 and np_(r.counts).sum() == 3
+
+
+# ----------------------------------------------------------------- router --
+
+def test_router_tiny():
+    cfg = moe_synth.TINY
+    inputs = moe_synth.make_inputs(cfg, with_ffn=False)
+    r = gpu_route(cfg, to_dev(inputs))
+    _, rep = routing_parity(cfg, inputs, r)
+    print(rep)
+
+
+@pytest.mark.parametrize("k", [1, 2, 4, 8])
+def test_router_sweep_full_size(k):
+    cfg = moe_synth.ROUTER[k]
+    inputs = moe_synth.make_inputs(cfg, with_ffn=False)
+    r = gpu_route(cfg, to_dev(inputs))
+    _, rep = routing_parity(cfg, inputs, r)
+    print(cfg.name, rep)
+
+
+@pytest.mark.parametrize("T,H,E,k,bias", [(1, 64, 8, 1, None), (130, 200, 16, 3, 0.5),
+                                          (257, 520, 256, 8, None), (64, 4096, 40, 5, 2.0),
+                                          (300, 72, 192, 2, None)])
+def test_router_edge_shapes(T, H, E, k, bias):
+    cfg = moe_synth.MoEConfig("edge", T=T, H=H, F=0, E=E, k=k, seed=11, bias0=bias)
+    inputs = moe_synth.make_inputs(cfg, with_ffn=False)
+    r = gpu_route(cfg, to_dev(inputs))
+    routing_parity(cfg, inputs, r)
+
+
+def test_router_duplicate_columns_tie_to_lower_index():
+    cfg = moe_synth.MoEConfig("ties", T=200, H=256, F=0, E=16, k=4, seed=12)
+    inputs = moe_synth.make_inputs(cfg, with_ffn=False)
+    inputs["w_router"][:, 9] = inputs["w_router"][:, 4]  # experts 4 and 9 tie exactly
+    r = gpu_route(cfg, to_dev(inputs))
+    ids = np_(r.ids)
+    seen = 0
+    for t in range(cfg.T):
+        row = ids[t].tolist()
+        if 4 in row and 9 in row:
+            assert row.index(4) + 1 == row.index(9)
+            seen += 1
+        elif 9 in row:
+            raise AssertionError(f"token {t} picked 9 without 4: {row}")
+    assert seen > 0
+
+
+# ---------------------------------------------------------------- forward --
+
+def test_forward_tiny_all_rows():
+    forward_parity(moe_synth.TINY)
+
+
+def test_forward_decode_all_rows():
+    cfg = moe_synth.DECODE
+    rep = forward_parity(cfg)
+    # every expert is hit at least once on this seed
+    inputs = moe_synth.make_inputs(cfg, with_ffn=False)
+    _, ids, _, _ = oracle.route(inputs["x"], inputs["w_router"], cfg.k)
+    assert len(np.unique(ids)) == cfg.E
+    assert rep["near_tie_tokens"] >= 0
+
+
+def test_forward_prefill_sampled():
+    forward_parity(moe_synth.PREFILL, stride=16)
+
+
+@pytest.mark.parametrize("cfg", [moe_synth.SKEWED, moe_synth.SKEWED_CF], ids=lambda c: c.name)
+def test_forward_skewed_sampled(cfg):
+    rep = forward_parity(cfg, stride=16)
+    if cfg.capacity_factor is not None:
+        assert rep["dropped"] > 0
+
+
+@pytest.mark.parametrize("T,H,F,E,k,cf,bias", [
+    (1, 64, 64, 8, 1, None, None),          # one token
+    (7, 136, 200, 8, 2, None, None),        # ragged H, F (not multiples of 64 / 256)
+    (300, 128, 520, 16, 8, None, None),     # k = 8, many ragged row blocks
+    (200, 256, 264, 8, 2, 0.3, 3.0),        # heavy drops, skewed
+    (150, 64, 128, 8, 1, None, 50.0),       # all tokens to expert 0, others empty
+    (33, 512, 1408, 64, 4, 1.0, None),      # many experts with 0-3 rows
+    (129, 72, 8, 8, 3, None, None),         # F = 8
+])
+def test_forward_edge_shapes(T, H, F, E, k, cf, bias):
+    cfg = moe_synth.MoEConfig("edge", T=T, H=H, F=F, E=E, k=k, seed=21, capacity_factor=cf,
+                              bias0=bias)
+    forward_parity(cfg)
+
+
+def test_forward_all_dropped_rows_are_zero():
+    cfg = moe_synth.MoEConfig("drop", T=256, H=64, F=64, E=8, k=2, seed=22, capacity_factor=0.05,
+                              bias0=8.0)
+    inputs = moe_synth.make_inputs(cfg)
+    layer, y = gpu_forward(cfg, to_dev(inputs))
+    slot = np_(layer.routing.slot)
+    dead = np.all(slot < 0, axis=1)
+    assert dead.any()
+    assert torch.all(y[torch.from_numpy(dead).to(DEV)] == 0)
+    forward_parity(cfg)
+
+
+def test_forward_empty_batch():
+    cfg = moe_synth.TINY
+    inputs = to_dev(moe_synth.make_inputs(cfg))
+    s = moe.make_shape(0, cfg.H, cfg.F, cfg.E, cfg.k)
+    r = moe.alloc_routing(0, cfg.E, cfg.k, DEV)
+    r.counts.fill_(7)
+    r.offsets.fill_(7)
+    ws = torch.empty(1024, dtype=torch.uint8, device=DEV)
+    y = torch.empty(0, cfg.H, dtype=torch.bfloat16, device=DEV)
+    x0 = torch.empty(0, cfg.H, dtype=torch.bfloat16, device=DEV)
+    moe.moe_forward(s, x0, inputs["w_router"], None, inputs["w1"], inputs["w2"], y, r.ids, r.weights,
+                    r.counts, r.offsets, r.perm, r.slot, ws)
+    assert moe.moe_get_device_status(ws) == 0
+    assert np_(r.counts).tolist() == [0] * cfg.E and np_(r.offsets).tolist() == [0] * (cfg.E + 1)
+
+
+def test_forward_is_deterministic_and_graph_capturable():
+    cfg = moe_synth.MoEConfig("det", T=512, H=256, F=512, E=16, k=4, seed=23)
+    dev_in = to_dev(moe_synth.make_inputs(cfg))
+    layer, y = gpu_forward(cfg, dev_in)
+    y1 = y.clone()
+    ids1 = layer.routing.ids.clone()
+    y.zero_()
+    layer(dev_in["x"])
+    torch.cuda.synchronize()
+    assert torch.equal(y1, layer.y) and torch.equal(ids1, layer.routing.ids)
+    # the same call captured in a CUDA graph and replayed gives the same bits
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    layer.y.zero_()
+    with torch.cuda.graph(g, stream=stream):
+        layer(dev_in["x"])
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y1, layer.y)
+
+
+def test_split_entry_points_match_forward():
+    cfg = moe_synth.MoEConfig("split", T=300, H=192, F=320, E=16, k=2, seed=24, capacity_factor=0.9)
+    dev_in = to_dev(moe_synth.make_inputs(cfg))
+    layer, y = gpu_forward(cfg, dev_in)
+    s = moe.make_shape(cfg.T, cfg.H, cfg.F, cfg.E, cfg.k, cfg.capacity_factor)
+    r = moe.alloc_routing(cfg.T, cfg.E, cfg.k, DEV)
+    ws = moe.alloc_workspace(s, DEV)
+    moe.moe_route(s, dev_in["x"], dev_in["w_router"], None, r.ids, r.weights, r.counts, r.offsets,
+                  r.perm, r.slot, ws)
+    y2 = torch.empty_like(y)
+    moe.moe_expert_ffn_combine(s, dev_in["x"], dev_in["w1"], dev_in["w2"], r.weights, r.offsets,
+                               r.perm, r.slot, y2, ws)
+    assert moe.moe_get_device_status(ws) == 0
+    assert torch.equal(y, y2)
+    for a, b in [(r.ids, layer.routing.ids), (r.slot, layer.routing.slot), (r.perm, layer.routing.perm)]:
+        assert torch.equal(a, b)
