@@ -1,0 +1,419 @@
+#!/usr/bin/env python
+"""Benchmark of the fused MoE layer forward on GB300 (tokens/s + roofline).
+
+One step = one moe_forward over one batch: router (logits, TopK, softmax),
+dispatch, expert GEMM1 (+GELU), expert GEMM2, combine -- the whole path.
+Workload (default): prefill, T=4096 tokens, H=4096, F=14336, E=8, k=2,
+seeded synthetic bf16 inputs (x~N(0,1), W_router~N(0,1/H), W1~N(0,1/H),
+W2~N(0,1/F)), no capacity limit.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun: every rank runs its own batch of T tokens with the
+same weights (data-parallel replicas, no collective on the data path);
+value = all ranks' tokens / max over ranks of the timed region.
+--impl reference times the plain CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/sec at 1 GB300 + % of bf16 tensor/HBM roofline"
+UNIT = "tokens/s"
+WORKLOADS = ("prefill", "decode", "skewed", "skewed_cf1.2", "tiny")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# dominant kernel from one ncu capture, keyed by the sha256 of the kernel
+# source it was taken on; reported as null once the source changes.
+NCU_TRAFFIC = {}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=1000)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=WORKLOADS, default="prefill")
+    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample-tokens", type=int, default=512,
+                   help="tokens of the workload the oracle runs for cpu_baseline")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_cfg(name):
+    import moe_synth
+    return moe_synth.ALL[name]
+
+
+def workload_desc(cfg):
+    cf = "none" if cfg.capacity_factor is None else cfg.capacity_factor
+    return (f"{cfg.name}: T={cfg.T} H={cfg.H} F={cfg.F} E={cfg.E} k={cfg.k} capacity_factor={cf}"
+            + (f" bias0={cfg.bias0}" if cfg.bias0 is not None else ""))
+
+
+def src_sha(name):
+    with open(os.path.join(ROOT, "mixture_experts_layer_12_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for(device):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        idx = device.index or 0
+        return vis.split(",")[idx] if vis else str(idx)
+
+
+# --------------------------------------------------------- work per kernel --
+
+def kernel_work(cfg, n_rows, experts_hit):
+    """Algorithmic FLOPs and bytes of one launch of each kernel."""
+    T, H, F, E, k = cfg.T, cfg.H, cfg.F, cfg.E, cfg.k
+    return {
+        "router": dict(flops=2.0 * T * H * E, bytes=2.0 * T * H + 2.0 * H * E + 8.0 * T * k),
+        "dispatch": dict(flops=0.0, bytes=4.0 * T * k * 3 + 8.0 * E),
+        "expert_gemm1": dict(flops=2.0 * n_rows * H * F,
+                             bytes=2.0 * experts_hit * H * F + 2.0 * n_rows * H + 2.0 * n_rows * F),
+        "expert_gemm2": dict(flops=2.0 * n_rows * F * H,
+                             bytes=2.0 * experts_hit * F * H + 2.0 * n_rows * F + 2.0 * n_rows * H),
+        "combine": dict(flops=2.0 * n_rows * H, bytes=2.0 * n_rows * H + 2.0 * T * H + 8.0 * T * k),
+    }
+
+
+# ------------------------------------------------------------ cpu baseline --
+
+def oracle_sample_run(inputs, cfg, rows):
+    """The oracle as it stands on a token sample: routing, dispatch, expert
+    FFN and combine for the sampled tokens (no capacity limit, so a token's
+    result does not depend on the unsampled ones)."""
+    import oracle
+    xs = inputs["x"][rows]
+    t0 = time.perf_counter()
+    oracle.moe_forward(xs, inputs["w_router"], inputs["w1"], inputs["w2"], cfg.k,
+                       bias=inputs["bias"], capacity_factor=cfg.capacity_factor)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inputs, cfg, n_tokens):
+    import oracle
+    oracle.build()
+    stride = max(1, cfg.T // max(1, n_tokens))
+    rows = list(range(0, cfg.T, stride))[:n_tokens]
+    dt = oracle_sample_run(inputs, cfg, rows)
+    return {"value": len(rows) / dt, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} of {cfg.T} tokens (every {stride}th): routing, dispatch, "
+                      f"fp64 expert FFN and combine for those tokens; {dt:.1f} s"}
+
+
+# --------------------------------------------------------------- reference --
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    import moe_synth
+    oracle.build()
+    cfg = workload_cfg(args.workload)
+    inputs = moe_synth.make_inputs(cfg)
+    # size each step's token sample so that warm-up + steps take ~90 s
+    probe = list(range(0, cfg.T, max(1, cfg.T // 4)))[:4]
+    per_token = oracle_sample_run(inputs, cfg, probe) / len(probe)
+    n_steps = max(1, args.warmup + args.steps)
+    per_step = int(max(1, min(64, cfg.T, 90.0 / (n_steps * per_token))))
+    stride = max(1, cfg.T // per_step)
+    total, times = 0, []
+    for i in range(args.warmup + args.steps):
+        start = (i * 7) % stride
+        rows = list(range(start, cfg.T, stride))[:per_step]
+        dt = oracle_sample_run(inputs, cfg, rows)
+        if i >= args.warmup:
+            times.append(dt)
+            total += len(rows)
+    elapsed = sum(times)
+    value = total / elapsed
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * elapsed / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "tokens_per_step": per_step,
+                   "parallelism": "host cores (OpenMP over tokens)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": f"{per_step} of {cfg.T} tokens per step (strided), routing, "
+                                   "dispatch, fp64 expert FFN and combine"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# -------------------------------------------------------------------- ours --
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+
+    from mixture_experts_layer_12_gb300 import build as moe_build
+    moe_build.build()
+    import mixture_experts_layer_12_gb300 as moe
+    import moe_synth
+
+    cfg = workload_cfg(args.workload)
+    if world > 1:  # each replica routes its own tokens
+        cfg_rank = cfg.with_(seed=cfg.seed + 1000 * rank)
+        inputs = moe_synth.make_inputs(cfg)
+        inputs["x"] = moe_synth.make_x(cfg_rank)
+    else:
+        inputs = moe_synth.make_inputs(cfg)
+    dev = {k: (None if v is None else v.to(device)) for k, v in inputs.items()}
+    layer = moe.MoELayer(dev["w_router"], dev["w1"], dev["w2"], cfg.k, bias=dev["bias"],
+                         capacity_factor=cfg.capacity_factor)
+    x = dev["x"]
+    stream = torch.cuda.current_stream(device)
+
+    def step(events=None):
+        layer._ensure(cfg.T, device)
+        r = layer.routing
+        if events is None:
+            moe.moe_forward(layer.shape, x, layer.w_router, layer.bias, layer.w1, layer.w2, layer.y,
+                            r.ids, r.weights, r.counts, r.offsets, r.perm, r.slot, layer.ws, stream)
+        else:
+            moe.moe_forward_profiled(layer.shape, x, layer.w_router, layer.bias, layer.w1, layer.w2,
+                                     layer.y, r.ids, r.weights, r.counts, r.offsets, r.perm, r.slot,
+                                     layer.ws, events, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(device)
+    if moe.moe_get_device_status(layer.ws, stream) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    for row in evs:  # materialise the event handles outside the timed region
+        for e in row:
+            e.record(stream)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+
+    clocks = ClockSampler(gpu_id_for(device))
+    clocks.start()
+    time.sleep(0.3)  # let the sampler come up
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    t_start.record(stream)
+    for i in range(K):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(device)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if moe.moe_get_device_status(layer.ws, stream) != 0:
+        raise RuntimeError("device status set during the timed region")
+
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / K
+    value = world * cfg.T * K / (elapsed_ms / 1e3)
+
+    # per-kernel device time (averaged over the timed steps)
+    names = moe.KERNEL_NAMES
+    per_kernel = {n: statistics.fmean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
+                  for j, n in enumerate(names)}
+    counts = layer.routing.counts.cpu()
+    n_rows = int(counts.sum().item())
+    experts_hit = int((counts > 0).sum().item())
+    work = kernel_work(cfg, n_rows, experts_hit)
+
+    peaks, peak_src = load_peaks()
+    dominant = max(per_kernel, key=per_kernel.get)
+    kernels = {}
+    for n in names:
+        ms = per_kernel[n]
+        kernels[n] = {"ms": round(ms, 5), "share": round(ms / sum(per_kernel.values()), 4),
+                      "tflops": round(work[n]["flops"] / (ms * 1e-3) / 1e12, 2),
+                      "gbs": round(work[n]["bytes"] / (ms * 1e-3) / 1e9, 1)}
+    dk = work[dominant]
+    if dominant.startswith("expert_gemm"):
+        ach = dk["flops"] / (per_kernel[dominant] * 1e-3) / 1e12
+        peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4),
+                "peak_kind": f"bf16 dense, sustained ({peak_src})",
+                "frac_of_burst": round(ach / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]), 4),
+                "kernel": dominant, "flops_per_launch": dk["flops"]}
+    else:
+        ach = dk["bytes"] / (per_kernel[dominant] * 1e-3) / 1e9
+        peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(ach / peak, 4), "peak_kind": f"HBM copy ({peak_src})",
+                "kernel": dominant, "bytes_per_launch": dk["bytes"]}
+    tr = NCU_TRAFFIC.get(dominant)
+    roof["traffic"] = tr["bytes"] if tr and tr.get("src_sha") == src_sha(tr["src"]) else None
+
+    # end to end through the public API with host buffers: H2D of x, the
+    # forward, D2H of y, every step, inside the timed region
+    E2E = max(1, min(args.e2e_steps, K))
+    x_host = inputs["x"].pin_memory()
+    y_host = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    r = layer.routing
+    for i in range(3 + E2E):
+        if i == 3:
+            torch.cuda.synchronize(device)
+            e0.record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_forward(layer.shape, x_dev, layer.w_router, layer.bias, layer.w1, layer.w2, layer.y,
+                        r.ids, r.weights, r.counts, r.offsets, r.perm, r.slot, layer.ws, stream)
+        y_host.copy_(layer.y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": world * cfg.T * E2E / (e2e_ms / 1e3), "unit": UNIT,
+           "h2d_bytes_per_step": cfg.T * cfg.H * 2, "d2h_bytes_per_step": cfg.T * cfg.H * 2,
+           "steps": E2E}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inputs, cfg, args.cpu_sample_tokens)
+
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "tokens_per_gpu": cfg.T,
+                   "parallelism": f"replicas x{world} (token data-parallel, no collective)",
+                   "kept_rows": n_rows, "experts_hit": experts_hit,
+                   "l2": "inputs larger than L2: every step streams all expert weights "
+                         f"({2 * 2 * cfg.E * cfg.H * cfg.F / 1e9:.2f} GB)"},
+        "gpu_launches": len(names) * K,
+        "roofline": roof,
+        "kernels": kernels,
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -166,6 +166,19 @@ MOE_API int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w
                 int32_t* slot, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * moe_forward with timing hooks (no counterpart on the pages): `events`
+ * points to 6 cudaEvent_t handles (any may be NULL; `events` itself may be
+ * NULL), recorded on `stream` before the router kernel and after each of
+ * the five kernels: router, dispatch, expert GEMM1, expert GEMM2, combine.
+ * The events are caller-owned; the library only records them.
+ */
+MOE_API int moe_forward_profiled(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
+                                 const float* b_router, const uint16_t* w1, const uint16_t* w2,
+                                 uint16_t* y, int32_t* ids, float* weights, int32_t* counts,
+                                 int32_t* offsets, int32_t* perm, int32_t* slot, void* ws,
+                                 size_t ws_bytes, void* stream, void* const* events);
+
+/*
  * Synchronises `stream`, reads the device status word of the workspace into
  * *status and clears it.  Returns MOE_OK when the word is 0,
  * MOE_ERR_TIMEOUT when MOE_DEV_TIMEOUT is set, MOE_ERR_DEVICE for other

@@ -37,7 +37,7 @@ MOE_WS_MIN_BYTES = 256
 # Every symbol include/moe.h declares.
 EXPORTS = ("moe_version", "moe_last_error_string", "moe_expert_capacity", "moe_workspace_size",
            "moe_route", "moe_dispatch", "moe_expert_ffn_combine", "moe_forward",
-           "moe_get_device_status", "moe_selftest_wait_timeout")
+           "moe_get_device_status", "moe_selftest_wait_timeout", "moe_forward_profiled")
 
 
 class MoEError(RuntimeError):
@@ -83,6 +83,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "moe_forward": ([S, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "moe_get_device_status": ([P, P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
             "moe_selftest_wait_timeout": ([P, ctypes.c_size_t, ctypes.c_uint64, P], ctypes.c_int),
+            "moe_forward_profiled": ([S, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P],
+                                     ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -175,6 +177,29 @@ def moe_forward(shape, x, w_router, b_router, w1, w2, y, ids, weights, counts, o
         _ptr(counts, i32, "counts"), _ptr(offsets, i32, "offsets"), _ptr(perm, i32, "perm"),
         _ptr(slot, i32, "slot"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
         _stream(stream)))
+
+
+KERNEL_NAMES = ("router", "dispatch", "expert_gemm1", "expert_gemm2", "combine")
+
+
+def moe_forward_profiled(shape, x, w_router, b_router, w1, w2, y, ids, weights, counts, offsets,
+                         perm, slot, ws, events, stream=None):
+    """moe_forward recording ``events`` (6 torch.cuda.Event or None) at the
+    kernel boundaries: before the router, then after each of KERNEL_NAMES."""
+    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+    handles = (ctypes.c_void_p * 6)()
+    for i, ev in enumerate(events):
+        if ev is not None:
+            if not ev.cuda_event:
+                ev.record()  # materialise the underlying cudaEvent_t
+            handles[i] = ev.cuda_event
+    _check(load_library().moe_forward_profiled(
+        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(w_router, bf, "w_router"),
+        _ptr(b_router, f32, "b_router"), _ptr(w1, bf, "w1"), _ptr(w2, bf, "w2"),
+        _ptr(y, bf, "y"), _ptr(ids, i32, "ids"), _ptr(weights, f32, "weights"),
+        _ptr(counts, i32, "counts"), _ptr(offsets, i32, "offsets"), _ptr(perm, i32, "perm"),
+        _ptr(slot, i32, "slot"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+        _stream(stream), handles))
 
 
 def moe_get_device_status(ws, stream=None) -> int:

@@ -157,9 +157,19 @@ uint16_t* y_ptr(void* ws, const moe_shape* s) {
 
 // ------------------------------------------------------------------ steps --
 
+// Optional timing hooks: ev[i] (a cudaEvent_t, may be null) is recorded on
+// the stream at kernel boundary i (0 = before the router, 1..5 = after the
+// router, dispatch, GEMM1, GEMM2 and combine).
+int mark(void* const* ev, int i, cudaStream_t st) {
+  if (!ev || !ev[i]) return MOE_OK;
+  cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "cudaEventRecord");
+}
+
 int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t* w_router,
                   const float* b_router, int32_t* ids, float* weights, int32_t* counts,
-                  int32_t* offsets, int32_t* perm, int32_t* slot, void* ws, cudaStream_t st) {
+                  int32_t* offsets, int32_t* perm, int32_t* slot, void* ws, cudaStream_t st,
+                  void* const* ev = nullptr) {
   int rc;
   CUtensorMap tm_x, tm_w;
   if ((rc = map_2d(&tm_x, x, (uint64_t)s->H, (uint64_t)s->T, 64, 128, "x (router)")) != MOE_OK) return rc;
@@ -181,8 +191,10 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
   ra.weights = weights;
   ra.status = status_ptr(ws);
   ra.wait_limit_ns = kWaitLimitNs;
+  if ((rc = mark(ev, 0, st)) != MOE_OK) return rc;
   cudaError_t e = launch_router(tm_x, tm_w, ra, st);
   if (e != cudaSuccess) return cuda_fail(e, "router launch");
+  if ((rc = mark(ev, 1, st)) != MOE_OK) return rc;
 
   DispatchArgs da;
   da.ids = ids;
@@ -197,13 +209,13 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
   da.status = status_ptr(ws);
   e = launch_dispatch(da, st);
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
-  return MOE_OK;
+  return mark(ev, 2, st);
 }
 
 int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const uint16_t* w1,
                         const uint16_t* w2, const float* weights, const int32_t* offsets,
                         const int32_t* perm, const int32_t* slot, uint16_t* y, void* ws,
-                        cudaStream_t st) {
+                        cudaStream_t st, void* const* ev = nullptr) {
   int rc;
   const uint64_t rows = (uint64_t)s->T * s->k;
   uint16_t* h = h_ptr(ws);
@@ -230,6 +242,7 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   int64_t ub = row_blocks_ub * ((s->F + kGemmBN - 1) / kGemmBN);
   cudaError_t e = launch_grouped_gemm(true, tm_xg, tm_w1, g, (int)(ub < sms ? ub : sms), st);
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM1 launch");
+  if ((rc = mark(ev, 3, st)) != MOE_OK) return rc;
 
   g.N = s->H;
   g.K = s->F;
@@ -237,6 +250,7 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   ub = row_blocks_ub * ((s->H + kGemmBN - 1) / kGemmBN);
   e = launch_grouped_gemm(false, tm_h, tm_w2, g, (int)(ub < sms ? ub : sms), st);
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM2 launch");
+  if ((rc = mark(ev, 4, st)) != MOE_OK) return rc;
 
   CombineArgs ca;
   ca.Y = Y;
@@ -248,7 +262,7 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   ca.y = y;
   e = launch_combine(ca, st);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-  return MOE_OK;
+  return mark(ev, 5, st);
 }
 
 int clear_status(void* ws, cudaStream_t st) {
@@ -366,6 +380,15 @@ int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
                 const float* b_router, const uint16_t* w1, const uint16_t* w2, uint16_t* y,
                 int32_t* ids, float* weights, int32_t* counts, int32_t* offsets, int32_t* perm,
                 int32_t* slot, void* ws, size_t ws_bytes, void* stream) {
+  return moe_forward_profiled(s, x, w_router, b_router, w1, w2, y, ids, weights, counts, offsets,
+                              perm, slot, ws, ws_bytes, stream, nullptr);
+}
+
+int moe_forward_profiled(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
+                         const float* b_router, const uint16_t* w1, const uint16_t* w2,
+                         uint16_t* y, int32_t* ids, float* weights, int32_t* counts,
+                         int32_t* offsets, int32_t* perm, int32_t* slot, void* ws,
+                         size_t ws_bytes, void* stream, void* const* events) {
   int rc = check_shape(s, true);
   if (rc != MOE_OK) return rc;
   REQUIRE_PTR(ws);
@@ -388,9 +411,10 @@ int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
   REQUIRE_PTR(weights);
   REQUIRE_PTR(perm);
   REQUIRE_PTR(slot);
-  rc = enqueue_route(s, sms, x, w_router, b_router, ids, weights, counts, offsets, perm, slot, ws, st);
+  rc = enqueue_route(s, sms, x, w_router, b_router, ids, weights, counts, offsets, perm, slot, ws, st,
+                     events);
   if (rc != MOE_OK) return rc;
-  return enqueue_ffn_combine(s, sms, x, w1, w2, weights, offsets, perm, slot, y, ws, st);
+  return enqueue_ffn_combine(s, sms, x, w1, w2, weights, offsets, perm, slot, y, ws, st, events);
 }
 
 int moe_get_device_status(void* ws, void* stream, int32_t* status) {
