@@ -220,8 +220,7 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   const uint64_t rows = (uint64_t)s->T * s->k;
   uint16_t* h = h_ptr(ws);
   uint16_t* Y = y_ptr(ws, s);
-  CUtensorMap tm_xg, tm_w1, tm_h, tm_w2;
-  if ((rc = map_2d(&tm_xg, x, (uint64_t)s->H, (uint64_t)s->T, 64, 1, "x (gather)")) != MOE_OK) return rc;
+  CUtensorMap tm_w1, tm_h, tm_w2;
   if ((rc = map_3d(&tm_w1, w1, (uint64_t)s->F, (uint64_t)s->H, (uint64_t)s->E, 64, 64, "W1")) != MOE_OK) return rc;
   if ((rc = map_2d(&tm_h, h, (uint64_t)s->F, rows, 64, 128, "h")) != MOE_OK) return rc;
   if ((rc = map_3d(&tm_w2, w2, (uint64_t)s->H, (uint64_t)s->F, (uint64_t)s->E, 64, 64, "W2")) != MOE_OK) return rc;
@@ -236,14 +235,17 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   g.status = status_ptr(ws);
   g.wait_limit_ns = kWaitLimitNs;
 
+  g.a = x;
   g.N = s->F;
   g.K = s->H;
   g.out = h;
   int64_t ub = row_blocks_ub * ((s->F + kGemmBN - 1) / kGemmBN);
-  cudaError_t e = launch_grouped_gemm(true, tm_xg, tm_w1, g, (int)(ub < sms ? ub : sms), st);
+  // GEMM1 gathers its A rows itself; tm_h is passed only to fill the slot
+  cudaError_t e = launch_grouped_gemm(true, tm_h, tm_w1, g, (int)(ub < sms ? ub : sms), st);
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM1 launch");
   if ((rc = mark(ev, 3, st)) != MOE_OK) return rc;
 
+  g.a = h;
   g.N = s->H;
   g.K = s->F;
   g.out = Y;

@@ -16,15 +16,19 @@
 //     Tiles are ordered expert-major, row-block fastest, so CTAs working at
 //     the same time share the expert's weight columns through L2 (the
 //     pages' expert-block / token-block tiling, made ragged).
-//   * warp 0: TMA producer.  The A tile of GEMM1 is gathered straight from
-//     x with tile::gather4 (4 token rows per lane, 32 lanes = 128 rows), so
-//     no permuted copy of x exists; GEMM2 reads contiguous rows of h.  The
-//     weight tile is four 64-column boxes of W[e] (N contiguous, MN-major).
-//   * warp 1: allocates 512 TMEM columns (two 128x256 fp32 accumulators)
-//     and one thread issues tcgen05.mma (M=128, N=256, K=16) from a 4-stage
-//     shared-memory ring (load / compute / store overlap of the article's
-//     section 2.2 pipeline).
-//   * warps 2-9: epilogue; tcgen05.ld of the accumulator, GELU(erf) for
+//   * warps 0-3: producers.  The weight tile (four 64-column TMA boxes of
+//     W[e], N contiguous = MN-major operand) is loaded by TMA.  GEMM2's A
+//     tile (contiguous rows of h) is one TMA box.  GEMM1's A tile is
+//     gathered straight from x by the 128 producer threads with 16-byte
+//     cp.async (8 lanes per 128-byte row slice, 128-byte swizzle applied by
+//     hand), so no permuted copy of x exists; each thread waits for its own
+//     copies, fences them into the async proxy and arrives on the stage
+//     barrier.
+//   * warp 4: allocates 512 TMEM columns (two 128x256 fp32 accumulators);
+//     one thread issues tcgen05.mma (M=128, N=256, K=16) from a 4-stage
+//     shared-memory ring (the load / compute / store overlap of the
+//     article's section 2.2 pipeline).
+//   * warps 5-12: epilogue; tcgen05.ld of the accumulator, GELU(erf) for
 //     GEMM1, bf16 rounding and 16-byte stores; double-buffered against the
 //     next tile's MMAs.
 // Every mbarrier wait is bounded (MOE_DEV_TIMEOUT on expiry).
@@ -42,14 +46,21 @@ constexpr int A_BYTES = BM * BK * 2;   // 16 KB: 128 rows x 128 B
 constexpr int B_CHUNK = BK * 64 * 2;   // 8 KB: one 64-column box, 64 K rows
 constexpr int B_BYTES = (BN / 64) * B_CHUNK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int PRODUCER_WARPS = 4;
+constexpr int PRODUCER_THREADS = 32 * PRODUCER_WARPS;
+constexpr int MMA_WARP = PRODUCER_WARPS;
+constexpr int EPI_WARP0 = MMA_WARP + 1;
 constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 32 * (2 + EPI_WARPS);
+constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
 constexpr int TMEM_COLS = ACC * BN;  // 512
+constexpr int GATHER_INFLIGHT = STAGES - 1;  // cp.async groups a producer keeps open
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, /*a_mn=*/false, /*b_mn=*/true);
 
 static_assert(BK == 64, "one 128-byte swizzle atom of K per stage");
 static_assert(BN % 64 == 0 && BN <= 256, "UMMA N");
 static_assert(TMEM_COLS <= 512, "TMEM capacity");
+static_assert(PRODUCER_THREADS == BM, "one gathered row slice per 8 lanes, 4 rows per warp op");
+static_assert(GATHER_INFLIGHT == 3, "cp.async.wait_group immediate below");
 
 struct Ctrl {
   uint64_t full[STAGES];
@@ -106,6 +117,24 @@ __device__ __forceinline__ float gelu_erf(float z) {
   return 0.5f * z * (1.0f + erff(z * 0.70710678118654752440f));
 }
 
+__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_inflight() {
+  asm volatile("cp.async.wait_group 2;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 template <bool GATHER_GELU>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
@@ -159,8 +188,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       c.n_tiles = incl;
     }
   } else if (threadIdx.x == 32) {
+    // GEMM1: one expect-tx arrival (weights) + one arrival per gathering thread
+    const uint32_t full_count = GATHER_GELU ? 1u + PRODUCER_THREADS : 1u;
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&c.full[i], 1);
+      mbar_init(&c.full[i], full_count);
       mbar_init(&c.empty[i], 1);
     }
     for (int i = 0; i < ACC; ++i) {
@@ -175,7 +206,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_tiles = c.n_tiles;
   if ((int)blockIdx.x >= n_tiles) return;  // uniform: nothing allocated yet
 
-  if (warp == 1) {
+  if (warp == MMA_WARP) {
     tmem_alloc(&c.tmem_base, TMEM_COLS);
     tmem_relinquish();
   }
@@ -185,73 +216,97 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = c.tmem_base;
   const WaitCtl wc{&c.abort_flag, p.status, p.wait_limit_ns};
 
-  if (warp == 0) {
-    // ------------------------------------------------ TMA producer warp
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_a);
+  if (warp < PRODUCER_WARPS) {
+    // ------------------------------------------------ producer warps
+    const bool b_loader = (warp == 0 && lane == 0);
+    if (b_loader) {
       tma_prefetch_desc(&tm_b);
+      if constexpr (!GATHER_GELU) tma_prefetch_desc(&tm_a);
     }
-    int stage = 0;
-    uint32_t phase = 0;
-    int armed = 0;
-    int e = 0;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-      const Tile t = decode_tile(c, tile, e);
-      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-      if constexpr (GATHER_GELU) {
-        // rows 4*lane .. 4*lane+3 of the tile; rows past the expert's end
-        // repeat its last row (computed, never stored)
-        int rr[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int row = t.row0 + min(4 * lane + i, t.rows_valid - 1);
-          const int tok = __ldg(p.perm + row) / p.k;
-          rr[i] = min(max(tok, 0), p.T - 1);
-        }
-        r0 = rr[0];
-        r1 = rr[1];
-        r2 = rr[2];
-        r3 = rr[3];
-      }
+    if (GATHER_GELU || warp == 0) {  // GEMM2: warp 0 alone (one TMA thread)
+      // gather geometry: lane -> (row within a 4-row group, 16-byte chunk)
+      const int sub = lane >> 3;
+      const int chunk = lane & 7;
+      const uint32_t a_base = smem_u32(sA);
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;    // k-blocks issued (all tiles)
+      int signaled = 0;  // k-blocks whose A slice this thread has published
+      int e = 0;
       bool ok = true;
-      for (int kb = 0; kb < KB; ++kb) {
-        int got = 1;
-        if (lane == 0) {
-          got = mbar_wait(&c.empty[stage], phase ^ 1u, wc);
-          if (got) mbar_arrive_expect_tx(&c.full[stage], STAGE_BYTES);
-        }
-        got = __shfl_sync(0xffffffffu, got, 0);
-        if (!got) {
-          ok = false;
-          break;
-        }
-        uint8_t* a = sA + stage * A_BYTES;
-        uint8_t* b = sB + stage * B_BYTES;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const Tile t = decode_tile(c, tile, e);
+        const uint16_t* src[8];
+        uint32_t dst[8];
         if constexpr (GATHER_GELU) {
-          tma_gather4(a + lane * 4 * 128, &tm_a, &c.full[stage], kb * BK, r0, r1, r2, r3);
-        } else {
-          if (lane == 0) tma_load_2d(a, &tm_a, &c.full[stage], kb * BK, t.row0);
+          // rows 32*warp + 4*i + sub; rows past the expert's end repeat its
+          // last row (computed, never stored)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int row = 32 * warp + 4 * i + sub;
+            const int prow = t.row0 + min(row, t.rows_valid - 1);
+            const int tok = min(max(__ldg(p.perm + prow) / p.k, 0), p.T - 1);
+            src[i] = p.a + (size_t)tok * (size_t)p.K + chunk * 8;
+            dst[i] = (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+          }
         }
-        if (lane < BN / 64)
-          tma_load_3d(b + lane * B_CHUNK, &tm_b, &c.full[stage], t.nb * BN + lane * 64, kb * BK,
-                      t.e);
-        ++armed;
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
+        for (int kb = 0; kb < KB; ++kb) {
+          int got = 1;
+          if (lane == 0) got = mbar_wait(&c.empty[stage], phase ^ 1u, wc);
+          got = __shfl_sync(0xffffffffu, got, 0);
+          if (!got) {
+            ok = false;
+            break;
+          }
+          if (b_loader) {
+            mbar_arrive_expect_tx(&c.full[stage], GATHER_GELU ? B_BYTES : STAGE_BYTES);
+            if constexpr (!GATHER_GELU)
+              tma_load_2d(sA + stage * A_BYTES, &tm_a, &c.full[stage], kb * BK, t.row0);
+#pragma unroll
+            for (int cb = 0; cb < BN / 64; ++cb)
+              tma_load_3d(sB + stage * B_BYTES + cb * B_CHUNK, &tm_b, &c.full[stage],
+                          t.nb * BN + cb * 64, kb * BK, t.e);
+          }
+          if constexpr (GATHER_GELU) {
+            // 16-byte chunk (kb*64 + chunk*8 .. +7) of each of this lane's rows;
+            // chunks past K are zero-filled (K % 8 == 0)
+            const uint32_t nbytes = (kb * BK + chunk * 8 < p.K) ? 16u : 0u;
+            const uint32_t sbase = a_base + (uint32_t)(stage * A_BYTES);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              cp_async_16(sbase + dst[i], nbytes ? (const void*)(src[i] + kb * BK) : (const void*)src[i],
+                          nbytes);
+            cp_async_commit();
+            if (issued + 1 - signaled == GATHER_INFLIGHT) {
+              cp_async_wait_inflight();  // the oldest open group has landed
+              fence_proxy_async_smem();
+              mbar_arrive(&c.full[signaled % STAGES]);
+              ++signaled;
+            }
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
-      if (!ok) break;
+      if constexpr (GATHER_GELU) {
+        cp_async_wait_all();
+        fence_proxy_async_smem();
+        for (; signaled < issued; ++signaled) mbar_arrive(&c.full[signaled % STAGES]);
+      }
+      // Drain: the TMA bytes of the last STAGES armed stages must have landed
+      // before shared memory is released (returns at once on the normal path,
+      // where the MMA consumed every stage).
+      if (b_loader) {
+        for (int m = max(0, issued - STAGES); m < issued; ++m)
+          mbar_wait_drain(&c.full[m % STAGES], (uint32_t)((m / STAGES) & 1), p.wait_limit_ns,
+                          p.status);
+      }
+      __syncwarp();
     }
-    // Drain: every armed stage's bytes must have landed before this CTA's
-    // shared memory can be released (a no-op on the normal path).
-    if (lane == 0) {
-      for (int m = max(0, armed - STAGES); m < armed; ++m)
-        mbar_wait_drain(&c.full[m % STAGES], (uint32_t)((m / STAGES) & 1), p.wait_limit_ns,
-                        p.status);
-    }
-    __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == MMA_WARP) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       int stage = 0;
@@ -299,8 +354,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------ epilogue warps
-    const int q = warp & 3;            // TMEM lane quadrant this warp may read
-    const int half = (warp - 2) >> 2;  // column half of the 256-wide tile
+    const int q = warp & 3;                    // TMEM lane quadrant this warp may read
+    const int half = (warp - EPI_WARP0) >> 2;  // column half of the 256-wide tile
     int acc = 0;
     uint32_t acc_phase = 0;
     int e = 0;
@@ -354,7 +409,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }

@@ -48,6 +48,7 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st);
 
 // ---- grouped expert GEMM (tcgen05 + TMA, persistent ragged scheduler).
 struct GemmArgs {
+  const uint16_t* a;       // gather mode: x [T, K] bf16 (rows gathered with cp.async)
   const int32_t* offsets;  // [E+1] dispatch offsets (device)
   const int32_t* perm;     // gather mode: token row of output row r is perm[r] / k
   int k;
@@ -59,8 +60,8 @@ struct GemmArgs {
   int* status;
   uint64_t wait_limit_ns;
 };
-// GEMM1: A rows gathered from x through perm, GELU epilogue.
-//   tm_a: x [T, H], box {64, 1} (gather4), tm_b: W1 [E, H, F] box {64, 64, 1}.
+// GEMM1: A rows gathered from x (GemmArgs::a) through perm, GELU epilogue.
+//   tm_a: unused, tm_b: W1 [E, H, F] box {64, 64, 1}.
 // GEMM2: A rows contiguous (dispatch order), no activation.
 //   tm_a: h [T*k, F], box {64, 128}, tm_b: W2 [E, F, H] box {64, 64, 1}.
 cudaError_t launch_grouped_gemm(bool gather_gelu, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
