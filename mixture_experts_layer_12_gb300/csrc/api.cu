@@ -225,7 +225,8 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   if ((rc = map_2d(&tm_h, h, (uint64_t)s->F, rows, 64, 128, "h")) != MOE_OK) return rc;
   if ((rc = map_3d(&tm_w2, w2, (uint64_t)s->H, (uint64_t)s->F, (uint64_t)s->E, 64, 64, "W2")) != MOE_OK) return rc;
 
-  const int64_t row_blocks_ub = ((int64_t)rows + kGemmBM - 1) / kGemmBM + s->E;
+  // pair tiles are 2*kGemmBM rows: an expert with n rows owns ceil(n / 256)
+  const int64_t row_blocks_ub = ((int64_t)rows + 2 * kGemmBM - 1) / (2 * kGemmBM) + s->E;
   GemmArgs g;
   g.offsets = offsets;
   g.perm = perm;
@@ -241,7 +242,7 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   g.out = h;
   int64_t ub = row_blocks_ub * ((s->F + kGemmBN - 1) / kGemmBN);
   // GEMM1 gathers its A rows itself; tm_h is passed only to fill the slot
-  cudaError_t e = launch_grouped_gemm(true, tm_h, tm_w1, g, (int)(ub < sms ? ub : sms), st);
+  cudaError_t e = launch_grouped_gemm(true, tm_h, tm_w1, g, (int)(ub < (1 << 30) ? ub : (1 << 30)), st);
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM1 launch");
   if ((rc = mark(ev, 3, st)) != MOE_OK) return rc;
 
@@ -250,7 +251,7 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   g.K = s->F;
   g.out = Y;
   ub = row_blocks_ub * ((s->H + kGemmBN - 1) / kGemmBN);
-  e = launch_grouped_gemm(false, tm_h, tm_w2, g, (int)(ub < sms ? ub : sms), st);
+  e = launch_grouped_gemm(false, tm_h, tm_w2, g, (int)(ub < (1 << 30) ? ub : (1 << 30)), st);
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM2 launch");
   if ((rc = mark(ev, 4, st)) != MOE_OK) return rc;
 

@@ -10,41 +10,47 @@
 // then N = hidden_dim, K = ffn_hidden_dim, with GELU in between).
 //
 // Design (sm_103a):
-//   * persistent CTAs, one per SM; tiles of 128 rows x 256 columns; the
-//     tile list is ragged per expert (ceil(n_e/128) row blocks) and is built
-//     on the device from `offsets`, so no host synchronisation is needed.
-//     Tiles are ordered expert-major, row-block fastest, so CTAs working at
-//     the same time share the expert's weight columns through L2 (the
-//     pages' expert-block / token-block tiling, made ragged).
-//   * warps 0-3: producers.  The weight tile (four 64-column TMA boxes of
-//     W[e], N contiguous = MN-major operand) is loaded by TMA.  GEMM2's A
-//     tile (contiguous rows of h) is one TMA box.  GEMM1's A tile is
-//     gathered straight from x by the 128 producer threads with 16-byte
-//     cp.async (8 lanes per 128-byte row slice, 128-byte swizzle applied by
-//     hand), so no permuted copy of x exists; each thread waits for its own
-//     copies, fences them into the async proxy and arrives on the stage
-//     barrier.
-//   * warp 4: allocates 512 TMEM columns (two 128x256 fp32 accumulators);
-//     one thread issues tcgen05.mma (M=128, N=256, K=16) from a 4-stage
-//     shared-memory ring (the load / compute / store overlap of the
-//     article's section 2.2 pipeline).
-//   * warps 5-12: epilogue; tcgen05.ld of the accumulator, GELU(erf) for
-//     GEMM1, bf16 rounding and 16-byte stores; double-buffered against the
-//     next tile's MMAs.
+//   * CTA pairs (clusters of 2) run the 2-SM form of tcgen05.mma
+//     (cta_group::2, M = 256, N = 256, K = 16): each CTA holds 128 rows of A
+//     and 128 columns of B per stage, so a 256x256 tile costs each SM 32 KB
+//     of operands per 64-wide K step instead of 48 KB for 128x256.
+//   * persistent pairs, tiles ordered expert-major and row-block fastest,
+//     so pairs working at the same time share the expert's weight columns
+//     through L2 (the pages' expert-block / token-block tiling, made ragged:
+//     an expert owns ceil(n_e / 256) row blocks); the tile list is built on
+//     the device from `offsets`, with no host synchronisation.
+//   * warps 0-3: producers.  Weight tiles (two 64-column TMA boxes of W[e]
+//     per CTA, N contiguous = MN-major operand) and GEMM2's A tile (rows of
+//     h, one box) are TMA loads that signal the leader CTA's stage barrier.
+//     GEMM1's A tile is gathered straight from x by the 128 producer threads
+//     with 16-byte cp.async (8 lanes per 128-byte row slice, 128-byte
+//     swizzle applied by hand), so no permuted copy of x exists; each lane
+//     waits for its own copies and fences them into the async proxy, then
+//     one lane per warp arrives on the leader's stage barrier.
+//   * warp 4: TMEM (two 128x256 fp32 accumulators per CTA, 512 columns);
+//     in the leader one thread issues the MMAs from a 6-stage ring (the
+//     load / compute / store overlap of the article's section 2.2
+//     pipeline) and its commits release the stage / publish the
+//     accumulator in both CTAs.
+//   * warps 5-12: epilogue; tcgen05.ld of the CTA's 128 accumulator rows,
+//     GELU(erf) for GEMM1, bf16 rounding and 16-byte stores; double-buffered
+//     against the next tile's MMAs.
 // Every mbarrier wait is bounded (MOE_DEV_TIMEOUT on expiry).
 #include "tc_common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int BM = kGemmBM;
-constexpr int BN = kGemmBN;
+constexpr int BM = kGemmBM;         // rows per CTA
+constexpr int PAIR_M = 2 * BM;      // rows per pair tile (UMMA M)
+constexpr int BN = kGemmBN;         // columns per pair tile (UMMA N)
+constexpr int BN_CTA = BN / 2;      // B columns each CTA holds
 constexpr int BK = kGemmBK;
-constexpr int STAGES = 4;
+constexpr int STAGES = 6;
 constexpr int ACC = 2;
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB: 128 rows x 128 B
 constexpr int B_CHUNK = BK * 64 * 2;   // 8 KB: one 64-column box, 64 K rows
-constexpr int B_BYTES = (BN / 64) * B_CHUNK;
+constexpr int B_BYTES = (BN_CTA / 64) * B_CHUNK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int PRODUCER_WARPS = 4;
 constexpr int PRODUCER_THREADS = 32 * PRODUCER_WARPS;
@@ -53,14 +59,15 @@ constexpr int EPI_WARP0 = MMA_WARP + 1;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
 constexpr int TMEM_COLS = ACC * BN;  // 512
-constexpr int GATHER_INFLIGHT = STAGES - 1;  // cp.async groups a producer keeps open
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, /*a_mn=*/false, /*b_mn=*/true);
+constexpr int GATHER_INFLIGHT = 4;   // cp.async groups a producer keeps open
+constexpr uint16_t PAIR_MASK = 0x3;
+constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, BN, /*a_mn=*/false, /*b_mn=*/true);
 
 static_assert(BK == 64, "one 128-byte swizzle atom of K per stage");
-static_assert(BN % 64 == 0 && BN <= 256, "UMMA N");
+static_assert(BN_CTA % 64 == 0 && BN <= 256, "UMMA N");
 static_assert(TMEM_COLS <= 512, "TMEM capacity");
-static_assert(PRODUCER_THREADS == BM, "one gathered row slice per 8 lanes, 4 rows per warp op");
-static_assert(GATHER_INFLIGHT == 3, "cp.async.wait_group immediate below");
+static_assert(PRODUCER_THREADS == BM, "8 lanes per row slice, 4 rows per warp op, 8 ops");
+static_assert(GATHER_INFLIGHT == 4 && GATHER_INFLIGHT < STAGES, "cp.async.wait_group immediate");
 
 struct Ctrl {
   uint64_t full[STAGES];
@@ -80,12 +87,15 @@ struct Ctrl {
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctrl);
 
 struct Tile {
-  int e, nb, row0, rows_valid;
+  int e, nb;
+  int row0;        // this CTA's first dispatch row
+  int rows_valid;  // rows of this CTA's half that belong to the expert (may be <= 0)
+  int last_row;    // the expert's last dispatch row (gather clamp)
 };
 
-// Tiles of one CTA increase monotonically, so the expert cursor only moves
+// Tiles of one pair increase monotonically, so the expert cursor only moves
 // forward; experts without rows own no tiles and are skipped.
-__device__ __forceinline__ Tile decode_tile(const Ctrl& c, int tile, int& e) {
+__device__ __forceinline__ Tile decode_tile(const Ctrl& c, int tile, int& e, int rank) {
   while (tile >= c.tile_start[e + 1]) ++e;
   const int local = tile - c.tile_start[e];
   const int mbs = c.mblocks[e];
@@ -93,8 +103,9 @@ __device__ __forceinline__ Tile decode_tile(const Ctrl& c, int tile, int& e) {
   Tile t;
   t.e = e;
   t.nb = local / mbs;
-  t.row0 = c.row_off[e] + mb * BM;
-  t.rows_valid = min(BM, c.rows[e] - mb * BM);
+  t.row0 = c.row_off[e] + mb * PAIR_M + rank * BM;
+  t.rows_valid = min(BM, c.rows[e] - mb * PAIR_M - rank * BM);
+  t.last_row = c.row_off[e] + c.rows[e] - 1;
   return t;
 }
 
@@ -126,7 +137,7 @@ __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
 __device__ __forceinline__ void cp_async_wait_inflight() {
-  asm volatile("cp.async.wait_group 2;" ::: "memory");
+  asm volatile("cp.async.wait_group 3;" ::: "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -148,6 +159,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = (int)cluster_ctarank();  // 0 = leader of the pair
+  const int pair = blockIdx.x >> 1;
+  const int n_pairs = gridDim.x >> 1;
   const int NB = (p.N + BN - 1) / BN;
   const int KB = (p.K + BK - 1) / BK;
 
@@ -162,7 +176,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (e < p.E) {
         const int o0 = __ldg(p.offsets + e);
         const int n = max(__ldg(p.offsets + e + 1) - o0, 0);
-        const int mbs = (n + BM - 1) / BM;
+        const int mbs = (n + PAIR_M - 1) / PAIR_M;
         c.row_off[e] = o0;
         c.rows[e] = n;
         c.mblocks[e] = mbs;
@@ -188,27 +202,30 @@ __global__ void __launch_bounds__(THREADS, 1)
       c.n_tiles = incl;
     }
   } else if (threadIdx.x == 32) {
-    // GEMM1: one expect-tx arrival (weights) + one arrival per gathering thread
-    const uint32_t full_count = GATHER_GELU ? 1u + PRODUCER_THREADS : 1u;
+    // Only the leader's `full`, `tempty` and `drain` are used.  full: one
+    // expect-tx arrival per CTA (+ one arrival per gathering warp of both
+    // CTAs for GEMM1); tempty: every epilogue warp of both CTAs.
+    const uint32_t full_count = GATHER_GELU ? 2u + 2u * PRODUCER_WARPS : 2u;
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&c.full[i], full_count);
       mbar_init(&c.empty[i], 1);
     }
     for (int i = 0; i < ACC; ++i) {
       mbar_init(&c.tfull[i], 1);
-      mbar_init(&c.tempty[i], EPI_WARPS);
+      mbar_init(&c.tempty[i], 2 * EPI_WARPS);
     }
     mbar_init(&c.drain, 1);
     c.abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
+  cluster_sync_all();  // the leader's barriers exist before the peer signals them
   const int n_tiles = c.n_tiles;
-  if ((int)blockIdx.x >= n_tiles) return;  // uniform: nothing allocated yet
+  if (pair >= n_tiles) return;  // uniform across the pair: nothing allocated yet
 
   if (warp == MMA_WARP) {
-    tmem_alloc(&c.tmem_base, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(&c.tmem_base, TMEM_COLS);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
@@ -224,27 +241,27 @@ __global__ void __launch_bounds__(THREADS, 1)
       if constexpr (!GATHER_GELU) tma_prefetch_desc(&tm_a);
     }
     if (GATHER_GELU || warp == 0) {  // GEMM2: warp 0 alone (one TMA thread)
-      // gather geometry: lane -> (row within a 4-row group, 16-byte chunk)
-      const int sub = lane >> 3;
-      const int chunk = lane & 7;
+      const int sub = lane >> 3;     // row within a 4-row group
+      const int chunk = lane & 7;    // 16-byte chunk of the 128-byte row slice
       const uint32_t a_base = smem_u32(sA);
+      const uint32_t full0 = dsmem_map(smem_u32(&c.full[0]), 0);  // leader's barriers
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;    // k-blocks issued (all tiles)
       int signaled = 0;  // k-blocks whose A slice this thread has published
       int e = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const Tile t = decode_tile(c, tile, e);
+      for (int tile = pair; tile < n_tiles && ok; tile += n_pairs) {
+        const Tile t = decode_tile(c, tile, e, rank);
         const uint16_t* src[8];
         uint32_t dst[8];
         if constexpr (GATHER_GELU) {
-          // rows 32*warp + 4*i + sub; rows past the expert's end repeat its
-          // last row (computed, never stored)
+          // this CTA's rows 4*i + sub + 32*warp; rows past the expert's end
+          // repeat its last row (computed, never stored)
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int row = 32 * warp + 4 * i + sub;
-            const int prow = t.row0 + min(row, t.rows_valid - 1);
+            const int prow = min(t.row0 + row, t.last_row);
             const int tok = min(max(__ldg(p.perm + prow) / p.k, 0), p.T - 1);
             src[i] = p.a + (size_t)tok * (size_t)p.K + chunk * 8;
             dst[i] = (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
@@ -258,29 +275,34 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
+          const uint32_t full_cl = full0 + (uint32_t)(stage * sizeof(uint64_t));
           if (b_loader) {
-            mbar_arrive_expect_tx(&c.full[stage], GATHER_GELU ? B_BYTES : STAGE_BYTES);
+            mbar_arrive_expect_tx_cluster(full_cl, GATHER_GELU ? B_BYTES : STAGE_BYTES);
             if constexpr (!GATHER_GELU)
-              tma_load_2d(sA + stage * A_BYTES, &tm_a, &c.full[stage], kb * BK, t.row0);
+              tma_load_2d_pair(sA + stage * A_BYTES, &tm_a, full_cl, kb * BK, t.row0);
 #pragma unroll
-            for (int cb = 0; cb < BN / 64; ++cb)
-              tma_load_3d(sB + stage * B_BYTES + cb * B_CHUNK, &tm_b, &c.full[stage],
-                          t.nb * BN + cb * 64, kb * BK, t.e);
+            for (int cb = 0; cb < BN_CTA / 64; ++cb)
+              tma_load_3d_pair(sB + stage * B_BYTES + cb * B_CHUNK, &tm_b, full_cl,
+                               t.nb * BN + rank * BN_CTA + cb * 64, kb * BK, t.e);
           }
           if constexpr (GATHER_GELU) {
-            // 16-byte chunk (kb*64 + chunk*8 .. +7) of each of this lane's rows;
-            // chunks past K are zero-filled (K % 8 == 0)
+            // 16-byte chunk (kb*64 + chunk*8 .. +7) of each of this lane's
+            // rows; chunks past K are zero-filled (K % 8 == 0)
             const uint32_t nbytes = (kb * BK + chunk * 8 < p.K) ? 16u : 0u;
             const uint32_t sbase = a_base + (uint32_t)(stage * A_BYTES);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              cp_async_16(sbase + dst[i], nbytes ? (const void*)(src[i] + kb * BK) : (const void*)src[i],
-                          nbytes);
+              cp_async_16(sbase + dst[i],
+                          nbytes ? (const void*)(src[i] + kb * BK) : (const void*)src[i], nbytes);
             cp_async_commit();
             if (issued + 1 - signaled == GATHER_INFLIGHT) {
-              cp_async_wait_inflight();  // the oldest open group has landed
+              // the oldest open group has landed for every lane: fence each
+              // lane's copies into the async proxy, then one arrival per warp
+              cp_async_wait_inflight();
               fence_proxy_async_smem();
-              mbar_arrive(&c.full[signaled % STAGES]);
+              __syncwarp();
+              if (lane == 0)
+                mbar_arrive_cluster(full0 + (uint32_t)((signaled % STAGES) * sizeof(uint64_t)));
               ++signaled;
             }
           }
@@ -294,12 +316,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       if constexpr (GATHER_GELU) {
         cp_async_wait_all();
         fence_proxy_async_smem();
-        for (; signaled < issued; ++signaled) mbar_arrive(&c.full[signaled % STAGES]);
+        __syncwarp();
+        for (; signaled < issued; ++signaled)
+          if (lane == 0)
+            mbar_arrive_cluster(full0 + (uint32_t)((signaled % STAGES) * sizeof(uint64_t)));
       }
-      // Drain: the TMA bytes of the last STAGES armed stages must have landed
-      // before shared memory is released (returns at once on the normal path,
-      // where the MMA consumed every stage).
-      if (b_loader) {
+      // Drain (leader): the TMA bytes of the last STAGES armed stages of both
+      // CTAs must have landed before shared memory is released (returns at
+      // once on the normal path, where the MMA consumed every stage).
+      if (b_loader && rank == 0) {
         for (int m = max(0, issued - STAGES); m < issued; ++m)
           mbar_wait_drain(&c.full[m % STAGES], (uint32_t)((m / STAGES) & 1), p.wait_limit_ns,
                           p.status);
@@ -307,14 +332,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
     }
   } else if (warp == MMA_WARP) {
-    // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------ MMA issuer (leader)
+    if (rank == 0 && lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+      for (int tile = pair; tile < n_tiles && ok; tile += n_pairs) {
         if (!mbar_wait(&c.tempty[acc], acc_phase ^ 1u, wc)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * BN);
@@ -332,23 +357,23 @@ __global__ void __launch_bounds__(THREADS, 1)
             // B: MN-major, advance 16 K rows = two 1024-byte atoms.
             const uint64_t ad = sdesc_sw128(a0 + j * 32, 16, 1024);
             const uint64_t bd = sdesc_sw128(b0 + j * 2048, B_CHUNK, 1024);
-            umma_bf16(d, ad, bd, IDESC, (kb | j) != 0 ? 1u : 0u);
+            umma_bf16_pair(d, ad, bd, IDESC, (kb | j) != 0 ? 1u : 0u);
           }
-          umma_commit(&c.empty[stage]);
+          umma_commit_pair_mc(&c.empty[stage], PAIR_MASK);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        umma_commit(&c.tfull[acc]);
+        umma_commit_pair_mc(&c.tfull[acc], PAIR_MASK);
         if (++acc == ACC) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
       // all MMAs issued by this thread have completed once `drain` fires
-      umma_commit(&c.drain);
+      umma_commit_pair_mc(&c.drain, 0x1);
       mbar_wait_drain(&c.drain, 0, p.wait_limit_ns, p.status);
     }
     __syncwarp();
@@ -356,11 +381,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------ epilogue warps
     const int q = warp & 3;                    // TMEM lane quadrant this warp may read
     const int half = (warp - EPI_WARP0) >> 2;  // column half of the 256-wide tile
+    const uint32_t tempty0 = dsmem_map(smem_u32(&c.tempty[0]), 0);
     int acc = 0;
     uint32_t acc_phase = 0;
     int e = 0;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-      const Tile t = decode_tile(c, tile, e);
+    for (int tile = pair; tile < n_tiles; tile += n_pairs) {
+      const Tile t = decode_tile(c, tile, e, rank);
       int got = 1;
       if (lane == 0) got = mbar_wait(&c.tfull[acc], acc_phase, wc);
       got = __shfl_sync(0xffffffffu, got, 0);
@@ -368,7 +394,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const int row = q * 32 + lane;
       const bool row_ok = row < t.rows_valid;
-      uint16_t* orow = p.out + (size_t)(t.row0 + (row_ok ? row : 0)) * (size_t)p.N;
+      uint16_t* orow = p.out + (size_t)(row_ok ? t.row0 + row : 0) * (size_t)p.N;
       const uint32_t tbase = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
@@ -399,7 +425,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&c.tempty[acc]);
+      if (lane == 0) mbar_arrive_cluster(tempty0 + (uint32_t)(acc * sizeof(uint64_t)));
       if (++acc == ACC) {
         acc = 0;
         acc_phase ^= 1u;
@@ -407,12 +433,62 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
 
+  // Both CTAs finish all remote signalling and the leader's MMAs before TMEM
+  // is released and before either CTA's shared memory goes away.
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();
   if (warp == MMA_WARP) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    tmem_dealloc_pair(tmem, TMEM_COLS);
   }
+  cluster_sync_all();
+}
+
+template <bool G>
+cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const GemmArgs& a,
+                        int pairs, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<G>, tm_a, tm_b, a);
+}
+
+// Co-resident CTA pairs of the GEMM kernel on this device (one per TPC).
+int max_pairs_cache[64];
+
+cudaError_t query_max_pairs(int dev, int* out) {
+  if (dev >= 0 && dev < 64 && max_pairs_cache[dev] > 0) {
+    *out = max_pairs_cache[dev];
+    return cudaSuccess;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  cudaError_t e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<true>, &cfg);
+  if (e != cudaSuccess) return e;
+  if (n < 1) return cudaErrorInvalidConfiguration;
+  if (dev >= 0 && dev < 64) max_pairs_cache[dev] = n;
+  *out = n;
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -420,14 +496,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 size_t grouped_gemm_smem_bytes() { return SMEM_BYTES; }
 
 cudaError_t launch_grouped_gemm(bool gather_gelu, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
-                                const GemmArgs& a, int grid, cudaStream_t st) {
-  if (grid <= 0) return cudaSuccess;
-  if (gather_gelu) {
-    grouped_gemm_kernel<true><<<grid, THREADS, SMEM_BYTES, st>>>(tm_a, tm_b, a);
-  } else {
-    grouped_gemm_kernel<false><<<grid, THREADS, SMEM_BYTES, st>>>(tm_a, tm_b, a);
-  }
-  return cudaGetLastError();
+                                const GemmArgs& a, int max_tiles, cudaStream_t st) {
+  if (max_tiles <= 0) return cudaSuccess;
+  int dev = 0, pairs = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = query_max_pairs(dev, &pairs)) != cudaSuccess) return e;
+  if (pairs > max_tiles) pairs = max_tiles;
+  return gather_gelu ? launch_pair<true>(tm_a, tm_b, a, pairs, st)
+                     : launch_pair<false>(tm_a, tm_b, a, pairs, st);
 }
 
 cudaError_t grouped_gemm_set_attributes() {

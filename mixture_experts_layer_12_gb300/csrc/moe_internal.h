@@ -64,10 +64,12 @@ struct GemmArgs {
 //   tm_a: unused, tm_b: W1 [E, H, F] box {64, 64, 1}.
 // GEMM2: A rows contiguous (dispatch order), no activation.
 //   tm_a: h [T*k, F], box {64, 128}, tm_b: W2 [E, F, H] box {64, 64, 1}.
+// Launches min(max_tiles, co-resident CTA pairs) persistent pairs
+// (clusters of 2 CTAs); max_tiles bounds the number of 256x256 pair tiles.
 cudaError_t launch_grouped_gemm(bool gather_gelu, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
-                                const GemmArgs& a, int grid, cudaStream_t st);
+                                const GemmArgs& a, int max_tiles, cudaStream_t st);
 size_t grouped_gemm_smem_bytes();
-constexpr int kGemmBM = 128;
+constexpr int kGemmBM = 128;  // rows per CTA; a CTA pair covers 256
 constexpr int kGemmBN = 256;
 constexpr int kGemmBK = 64;
 
