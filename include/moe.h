@@ -166,6 +166,40 @@ MOE_API int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w
                 int32_t* slot, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Bytes of the library's built-in device scratch used by
+ * moe_expert_ffn_combine_noalloc (held on every GPU that loads the library
+ * until the process exits).
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * moe_expert_ffn_combine for callers that cannot allocate device memory.
+ * The pages have no counterpart: it exists for hosts that own only their
+ * input and output buffers -- e.g. a runtime that reserves all device memory
+ * at start-up and forbids cudaMalloc afterwards, or a plain C caller with no
+ * device allocator at hand -- and so cannot provide the `ws` workspace.
+ * Same arguments and results as moe_expert_ffn_combine, without `ws`: the
+ * hidden activations and expert outputs live in a static device array of
+ * MOE_NOALLOC_SCRATCH_BYTES bytes inside the library.
+ *   - Shapes whose workspace (moe_workspace_size) exceeds
+ *     MOE_NOALLOC_SCRATCH_BYTES are rejected with MOE_ERR_UNSUPPORTED
+ *     (about T*k*(F+H)*2 bytes: e.g. T*k = 64 rows at H = 4096, F = 14336).
+ *   - Nothing is allocated or freed.  The first call on a device looks up
+ *     the scratch's device address (cudaGetSymbolAddress) with that device
+ *     current; make that first call before any stream capture.
+ *   - Every call on a device shares the one scratch array: calls that
+ *     overlap on the GPU (different streams, or different host threads)
+ *     race and corrupt each other's results; serialise them.
+ *   - Device status bits of this call are kept in the scratch and are not
+ *     readable through moe_get_device_status.
+ */
+MOE_API int moe_expert_ffn_combine_noalloc(const moe_shape* s, const uint16_t* x,
+                                           const uint16_t* w1, const uint16_t* w2,
+                                           const float* weights, const int32_t* offsets,
+                                           const int32_t* perm, const int32_t* slot, uint16_t* y,
+                                           void* stream);
+
+/*
  * moe_forward with timing hooks (no counterpart on the pages): `events`
  * points to 6 cudaEvent_t handles (any may be NULL; `events` itself may be
  * NULL), recorded on `stream` before the router kernel and after each of

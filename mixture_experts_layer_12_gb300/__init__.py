@@ -37,7 +37,9 @@ MOE_WS_MIN_BYTES = 256
 # Every symbol include/moe.h declares.
 EXPORTS = ("moe_version", "moe_last_error_string", "moe_expert_capacity", "moe_workspace_size",
            "moe_route", "moe_dispatch", "moe_expert_ffn_combine", "moe_forward",
-           "moe_get_device_status", "moe_selftest_wait_timeout", "moe_forward_profiled")
+           "moe_get_device_status", "moe_selftest_wait_timeout", "moe_forward_profiled",
+           "moe_expert_ffn_combine_noalloc")
+MOE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class MoEError(RuntimeError):
@@ -85,6 +87,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "moe_selftest_wait_timeout": ([P, ctypes.c_size_t, ctypes.c_uint64, P], ctypes.c_int),
             "moe_forward_profiled": ([S, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P],
                                      ctypes.c_int),
+            "moe_expert_ffn_combine_noalloc": ([S, P, P, P, P, P, P, P, P, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -165,6 +168,18 @@ def moe_expert_ffn_combine(shape, x, w1, w2, weights, offsets, perm, slot, y, ws
         _ptr(weights, f32, "weights"), _ptr(offsets, i32, "offsets"), _ptr(perm, i32, "perm"),
         _ptr(slot, i32, "slot"), _ptr(y, bf, "y"), _ptr(ws, None, "ws"),
         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_expert_ffn_combine_noalloc(shape, x, w1, w2, weights, offsets, perm, slot, y, stream=None):
+    """moe_expert_ffn_combine without a caller workspace: the library's
+    built-in device scratch (MOE_NOALLOC_SCRATCH_BYTES) holds the
+    intermediates, for callers that cannot allocate device memory.  Calls
+    that overlap on the GPU share that scratch and must be serialised."""
+    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+    _check(load_library().moe_expert_ffn_combine_noalloc(
+        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(w1, bf, "w1"), _ptr(w2, bf, "w2"),
+        _ptr(weights, f32, "weights"), _ptr(offsets, i32, "offsets"), _ptr(perm, i32, "perm"),
+        _ptr(slot, i32, "slot"), _ptr(y, bf, "y"), _stream(stream)))
 
 
 def moe_forward(shape, x, w_router, b_router, w1, w2, y, ids, weights, counts, offsets, perm,

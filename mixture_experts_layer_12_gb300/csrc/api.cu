@@ -279,6 +279,30 @@ int empty_routing(const moe_shape* s, int32_t* counts, int32_t* offsets, cudaStr
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "cudaMemsetAsync(counts/offsets)");
 }
 
+// ------------------------------------------------- allocation-free scratch --
+// Scratch of moe_expert_ffn_combine_noalloc: the status block, h and the
+// expert outputs, laid out as in a caller workspace.  In host code this name
+// is only a handle: its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+void* g_noalloc_ptr[kMaxDevices];  // device address per device, set once (g_mu)
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(MOE_ERR_UNSUPPORTED, "device %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+
 }  // namespace
 
 // =================================================================== C ABI
@@ -377,6 +401,37 @@ int moe_expert_ffn_combine(const moe_shape* s, const uint16_t* x, const uint16_t
   REQUIRE_PTR(slot);
   REQUIRE_PTR(y);
   return enqueue_ffn_combine(s, sms, x, w1, w2, weights, offsets, perm, slot, y, ws, st);
+}
+
+int moe_expert_ffn_combine_noalloc(const moe_shape* s, const uint16_t* x, const uint16_t* w1,
+                                   const uint16_t* w2, const float* weights,
+                                   const int32_t* offsets, const int32_t* perm,
+                                   const int32_t* slot, uint16_t* y, void* stream) {
+  int rc = check_shape(s, true);
+  if (rc != MOE_OK) return rc;
+  const size_t need = ws_bytes_for(s);
+  if (need > (size_t)MOE_NOALLOC_SCRATCH_BYTES)
+    return fail(MOE_ERR_UNSUPPORTED,
+                "moe_expert_ffn_combine_noalloc: T*k = %lld rows at H = %d, F = %d need %zu "
+                "bytes of scratch; the built-in scratch holds %u (use moe_expert_ffn_combine "
+                "with a workspace)",
+                (long long)s->T * s->k, s->H, s->F, need, (unsigned)MOE_NOALLOC_SCRATCH_BYTES);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int sms = 0;
+  if ((rc = device_setup(&sms)) != MOE_OK) return rc;
+  void* scratch = nullptr;
+  if ((rc = noalloc_scratch(&scratch)) != MOE_OK) return rc;
+  if ((rc = clear_status(scratch, st)) != MOE_OK) return rc;  // starts at zero every call
+  if (s->T == 0) return MOE_OK;
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(w1);
+  REQUIRE_PTR(w2);
+  REQUIRE_PTR(weights);
+  REQUIRE_PTR(offsets);
+  REQUIRE_PTR(perm);
+  REQUIRE_PTR(slot);
+  REQUIRE_PTR(y);
+  return enqueue_ffn_combine(s, sms, x, w1, w2, weights, offsets, perm, slot, y, scratch, st);
 }
 
 int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
