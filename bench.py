@@ -49,7 +49,7 @@ def parse_args():
     p.add_argument("--workload", choices=WORKLOADS, default="prefill")
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-sample-tokens", type=int, default=512,
+    p.add_argument("--cpu-sample-tokens", type=int, default=1366,
                    help="tokens of the workload the oracle runs for cpu_baseline")
     return p.parse_args()
 
@@ -335,7 +335,11 @@ def run_ours(args):
                       "tflops": round(work[n]["flops"] / (ms * 1e-3) / 1e12, 2),
                       "gbs": round(work[n]["bytes"] / (ms * 1e-3) / 1e9, 1)}
     dk = work[dominant]
-    if dominant.startswith("expert_gemm"):
+    # tensor-bound when the kernel's arithmetic intensity exceeds the ridge
+    # point of the measured peaks, HBM-bound otherwise
+    ridge = (peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) * 1e12 /
+             (peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]) * 1e9))
+    if dk["flops"] / max(dk["bytes"], 1.0) > ridge:
         ach = dk["flops"] / (per_kernel[dominant] * 1e-3) / 1e12
         peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
         roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
