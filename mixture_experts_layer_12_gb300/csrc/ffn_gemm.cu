@@ -90,7 +90,6 @@ struct Tile {
   int e, nb;
   int row0;        // this CTA's first dispatch row
   int rows_valid;  // rows of this CTA's half that belong to the expert (may be <= 0)
-  int last_row;    // the expert's last dispatch row (gather clamp)
 };
 
 // Tiles of one pair increase monotonically, so the expert cursor only moves
@@ -105,7 +104,6 @@ __device__ __forceinline__ Tile decode_tile(const Ctrl& c, int tile, int& e, int
   t.nb = local / mbs;
   t.row0 = c.row_off[e] + mb * PAIR_M + rank * BM;
   t.rows_valid = min(BM, c.rows[e] - mb * PAIR_M - rank * BM);
-  t.last_row = c.row_off[e] + c.rows[e] - 1;
   return t;
 }
 
@@ -255,14 +253,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         const Tile t = decode_tile(c, tile, e, rank);
         const uint16_t* src[8];
         uint32_t dst[8];
+        uint32_t live = 0;  // bit i: row i of this lane belongs to the expert
         if constexpr (GATHER_GELU) {
-          // this CTA's rows 4*i + sub + 32*warp; rows past the expert's end
-          // repeat its last row (computed, never stored)
+          // this CTA's rows 32*warp + 4*i + sub; rows past the expert's end
+          // are zero-filled without touching memory (computed, never stored)
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             const int row = 32 * warp + 4 * i + sub;
-            const int prow = min(t.row0 + row, t.last_row);
-            const int tok = min(max(__ldg(p.perm + prow) / p.k, 0), p.T - 1);
+            int tok = 0;
+            if (row < t.rows_valid) {
+              tok = min(max(__ldg(p.perm + t.row0 + row) / p.k, 0), p.T - 1);
+              live |= 1u << i;
+            }
             src[i] = p.a + (size_t)tok * (size_t)p.K + chunk * 8;
             dst[i] = (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
           }
@@ -287,13 +289,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           if constexpr (GATHER_GELU) {
             // 16-byte chunk (kb*64 + chunk*8 .. +7) of each of this lane's
-            // rows; chunks past K are zero-filled (K % 8 == 0)
-            const uint32_t nbytes = (kb * BK + chunk * 8 < p.K) ? 16u : 0u;
+            // rows; chunks past K and rows past the expert are zero-filled
+            // (K % 8 == 0)
+            const bool in_k = kb * BK + chunk * 8 < p.K;
             const uint32_t sbase = a_base + (uint32_t)(stage * A_BYTES);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t nbytes = (in_k && ((live >> i) & 1u)) ? 16u : 0u;
               cp_async_16(sbase + dst[i],
                           nbytes ? (const void*)(src[i] + kb * BK) : (const void*)src[i], nbytes);
+            }
             cp_async_commit();
             if (issued + 1 - signaled == GATHER_INFLIGHT) {
               // the oldest open group has landed for every lane: fence each
