@@ -31,7 +31,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer tokens/sec at 1 GB300 + % of bf16 tensor/HBM roofline"
 UNIT = "tokens/s"
-WORKLOADS = ("prefill", "decode", "skewed", "skewed_cf1.2", "tiny")
+WORKLOADS = ("prefill", "decode", "skewed", "skewed_cf1.2", "tiny", "router_k1", "router_k2",
+             "router_k4", "router_k8")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
@@ -236,6 +237,63 @@ def run_reference(args):
 
 # -------------------------------------------------------------------- ours --
 
+def run_route_only(args, cfg, device):
+    """Router sweep: one step = moe_route (router + dispatch) over T tokens.
+    Rotates through enough copies of x that the set exceeds L2."""
+    import torch
+    import mixture_experts_layer_12_gb300 as moe
+    import moe_synth
+    inputs = moe_synth.make_inputs(cfg, with_ffn=False)
+    x0 = inputs["x"].to(device)
+    copies = max(2, int(4 * 129e6 // (x0.numel() * 2)) + 1)
+    xs = [x0] + [x0.roll(i, dims=1).contiguous() for i in range(1, copies)]
+    wr = inputs["w_router"].to(device)
+    s = moe.make_shape(cfg.T, cfg.H, 8, cfg.E, cfg.k, cfg.capacity_factor)
+    r = moe.alloc_routing(cfg.T, cfg.E, cfg.k, device)
+    ws = moe.alloc_route_workspace(s, device)
+    stream = torch.cuda.current_stream(device)
+    for i in range(max(3, args.warmup)):
+        moe.moe_route(s, xs[i % copies], wr, None, r.ids, r.weights, r.counts, r.offsets, r.perm,
+                      r.slot, ws, stream)
+    torch.cuda.synchronize(device)
+    K = args.steps
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    clocks = ClockSampler(gpu_id_for(device))
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize(device)
+    ev[0].record(stream)
+    for i in range(K):
+        moe.moe_route(s, xs[i % copies], wr, None, r.ids, r.weights, r.counts, r.offsets, r.perm,
+                      r.slot, ws, stream)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(device)
+    clk = clocks.stop()
+    if moe.moe_get_device_status(ws, stream) != 0:
+        raise RuntimeError("device status set during the timed region")
+    elapsed = ev[0].elapsed_time(ev[K])
+    ms = elapsed / K
+    peaks, src = load_peaks()
+    w = kernel_work(cfg, cfg.T * cfg.k, 0)
+    route_bytes = w["router"]["bytes"] + w["dispatch"]["bytes"]
+    ach = route_bytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": cfg.T / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(cfg), "step": "moe_route (router + dispatch)",
+                   "l2": f"{copies} rotating copies of x ({copies * x0.numel() * 2 / 1e6:.0f} MB > L2)"},
+        "gpu_launches": 2 * K,
+        "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks.get("hbm_gbs"),
+                     "unit": "GB/s", "frac": round(ach / peaks.get("hbm_gbs", 6800.0), 4),
+                     "peak_kind": f"HBM copy ({src})", "kernel": "router+dispatch",
+                     "bytes_per_launch": route_bytes, "traffic": None},
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -254,6 +312,8 @@ def run_ours(args):
     import moe_synth
 
     cfg = workload_cfg(args.workload)
+    if not cfg.has_ffn:
+        return run_route_only(args, cfg, device)
     if world > 1:  # each replica routes its own tokens
         cfg_rank = cfg.with_(seed=cfg.seed + 1000 * rank)
         inputs = moe_synth.make_inputs(cfg)

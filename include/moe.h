@@ -40,9 +40,9 @@
  *     synchronise the host, except moe_get_device_status.
  *   - `ws` is a caller-owned device workspace of `ws_bytes` bytes, at least
  *     moe_workspace_size() for moe_forward / moe_expert_ffn_combine and at
- *     least MOE_WS_MIN_BYTES for moe_route / moe_dispatch; its first bytes
- *     hold the device status word of the most recent call.  Concurrent calls
- *     must not share a workspace.
+ *     least moe_route_workspace_size() for moe_route / moe_dispatch; its
+ *     first bytes hold the device status word of the most recent call.
+ *     Concurrent calls must not share a workspace.
  *   - Return value: MOE_OK or an MOE_ERR_* code.  Arguments are validated on
  *     the host before anything is enqueued; on an error nothing is launched
  *     and moe_last_error_string() describes the problem.
@@ -82,7 +82,8 @@ extern "C" {
 #define MOE_DEV_TIMEOUT 0x1 /* a kernel's bounded wait gave up */
 #define MOE_DEV_BAD_ID 0x2  /* an expert id outside [0, E) reached dispatch */
 
-/* Smallest workspace accepted by moe_route and moe_dispatch. */
+/* Smallest workspace accepted by moe_get_device_status and
+ * moe_selftest_wait_timeout. */
 #define MOE_WS_MIN_BYTES 256
 
 typedef struct moe_shape {
@@ -103,10 +104,16 @@ MOE_API const char* moe_last_error_string(void);
 /* Expert capacity C for the shape (see above), or -1 for no limit. */
 MOE_API int64_t moe_expert_capacity(const moe_shape* s);
 
-/* Workspace bytes needed by moe_forward and moe_expert_ffn_combine:
- * the status word, h [T*k, F] bf16 and the expert outputs [T*k, H] bf16.
- * Returns 0 for an invalid shape. */
+/* Workspace bytes needed by moe_forward and moe_expert_ffn_combine (and
+ * enough for every other entry point): a 1 KB status block, per-128-token
+ * expert counts [ceil(T/128), E] int32, h [T*k, F] bf16 and the expert
+ * outputs [T*k, H] bf16.  Returns 0 for an invalid shape. */
 MOE_API size_t moe_workspace_size(const moe_shape* s);
+
+/* Workspace bytes needed by moe_route and moe_dispatch (status block and
+ * per-128-token expert counts; F is ignored).  Returns 0 for an invalid
+ * shape. */
+MOE_API size_t moe_route_workspace_size(const moe_shape* s);
 
 /*
  * Steps 1-3 (the router kernel "MoERouterKernel::Process": x × W_router on

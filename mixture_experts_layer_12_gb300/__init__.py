@@ -38,7 +38,7 @@ MOE_WS_MIN_BYTES = 256
 EXPORTS = ("moe_version", "moe_last_error_string", "moe_expert_capacity", "moe_workspace_size",
            "moe_route", "moe_dispatch", "moe_expert_ffn_combine", "moe_forward",
            "moe_get_device_status", "moe_selftest_wait_timeout", "moe_forward_profiled",
-           "moe_expert_ffn_combine_noalloc")
+           "moe_expert_ffn_combine_noalloc", "moe_route_workspace_size")
 MOE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -79,6 +79,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "moe_last_error_string": ([], ctypes.c_char_p),
             "moe_expert_capacity": ([S], ctypes.c_int64),
             "moe_workspace_size": ([S], ctypes.c_size_t),
+            "moe_route_workspace_size": ([S], ctypes.c_size_t),
             "moe_route": ([S, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "moe_dispatch": ([S, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "moe_expert_ffn_combine": ([S, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
@@ -137,6 +138,13 @@ def moe_expert_capacity(shape: moe_shape) -> int:
 
 def moe_workspace_size(shape: moe_shape) -> int:
     n = int(load_library().moe_workspace_size(ctypes.byref(shape)))
+    if n == 0:
+        _check(MOE_ERR_UNSUPPORTED)
+    return n
+
+
+def moe_route_workspace_size(shape: moe_shape) -> int:
+    n = int(load_library().moe_route_workspace_size(ctypes.byref(shape)))
     if n == 0:
         _check(MOE_ERR_UNSUPPORTED)
     return n
@@ -253,7 +261,14 @@ def alloc_routing(T: int, E: int, k: int, device) -> RoutingBuffers:
 
 
 def alloc_workspace(shape: moe_shape, device) -> torch.Tensor:
+    """Workspace for moe_forward / moe_expert_ffn_combine (and all others)."""
     n = max(moe_workspace_size(shape), MOE_WS_MIN_BYTES)
+    return torch.empty((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
+
+
+def alloc_route_workspace(shape: moe_shape, device) -> torch.Tensor:
+    """Workspace for moe_route / moe_dispatch."""
+    n = max(moe_route_workspace_size(shape), MOE_WS_MIN_BYTES)
     return torch.empty((n + 15) // 16 * 16, dtype=torch.uint8, device=device)
 
 
@@ -296,5 +311,6 @@ def roofline_flops(N_rows: int, H: int, F: int) -> float:
 
 
 __all__ = [n for n in EXPORTS] + ["MoEError", "moe_shape", "make_shape", "load_library",
-                                   "alloc_routing", "alloc_workspace", "MoELayer", "RoutingBuffers",
+                                   "alloc_routing", "alloc_workspace", "alloc_route_workspace",
+                                   "MoELayer", "RoutingBuffers",
                                    "capacity", "roofline_flops"]

@@ -142,17 +142,33 @@ int64_t capacity_of(const moe_shape* s) {
 
 // --------------------------------------------------------------- workspace --
 
-constexpr size_t kStatusBytes = 1024;  // status word + padding (keeps h 1024-aligned)
+// Workspace: [status block | per-tile expert counts | h | Y].  The status
+// block holds the device status word (byte 0) and the router's completion
+// ticket (byte 64); both are cleared at the start of every call.
+constexpr size_t kStatusBytes = 1024;
+constexpr size_t kTicketOffset = 64;
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+size_t hist_bytes(const moe_shape* s) {
+  return align_up((size_t)((s->T + kSegTokens - 1) / kSegTokens) * s->E * 4, 1024);
+}
 size_t h_bytes(const moe_shape* s) { return align_up((size_t)s->T * s->k * s->F * 2, 1024); }
 size_t y_bytes(const moe_shape* s) { return align_up((size_t)s->T * s->k * s->H * 2, 1024); }
-size_t ws_bytes_for(const moe_shape* s) { return kStatusBytes + h_bytes(s) + y_bytes(s); }
+size_t route_ws_bytes(const moe_shape* s) { return kStatusBytes + hist_bytes(s); }
+size_t ws_bytes_for(const moe_shape* s) { return route_ws_bytes(s) + h_bytes(s) + y_bytes(s); }
 
 int* status_ptr(void* ws) { return reinterpret_cast<int*>(ws); }
-uint16_t* h_ptr(void* ws) { return reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + kStatusBytes); }
+unsigned int* ticket_ptr(void* ws) {
+  return reinterpret_cast<unsigned int*>(static_cast<char*>(ws) + kTicketOffset);
+}
+int32_t* hist_ptr(void* ws) {
+  return reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kStatusBytes);
+}
+uint16_t* h_ptr(void* ws, const moe_shape* s) {
+  return reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + route_ws_bytes(s));
+}
 uint16_t* y_ptr(void* ws, const moe_shape* s) {
-  return reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + kStatusBytes + h_bytes(s));
+  return reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + route_ws_bytes(s) + h_bytes(s));
 }
 
 // ------------------------------------------------------------------ steps --
@@ -186,9 +202,14 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
   const int kblocks = (s->H + 63) / 64;
   ra.splits = 1;
   while (ra.splits < 8 && mtiles * ra.splits * 2 <= sms && ra.splits * 2 <= kblocks) ra.splits *= 2;
+  ra.capacity = (int)capacity_of(s);
   ra.bias = b_router;
   ra.ids = ids;
   ra.weights = weights;
+  ra.hist = hist_ptr(ws);
+  ra.counts = counts;
+  ra.offsets = offsets;
+  ra.ticket = ticket_ptr(ws);
   ra.status = status_ptr(ws);
   ra.wait_limit_ns = kWaitLimitNs;
   if ((rc = mark(ev, 0, st)) != MOE_OK) return rc;
@@ -201,8 +222,9 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
   da.T = s->T;
   da.k = s->k;
   da.E = s->E;
-  da.capacity = (int)capacity_of(s);
-  da.counts = counts;
+  da.capacity = ra.capacity;
+  da.seg_tokens = kSegTokens;
+  da.base = hist_ptr(ws);
   da.offsets = offsets;
   da.perm = perm;
   da.slot = slot;
@@ -218,7 +240,7 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
                         cudaStream_t st, void* const* ev = nullptr) {
   int rc;
   const uint64_t rows = (uint64_t)s->T * s->k;
-  uint16_t* h = h_ptr(ws);
+  uint16_t* h = h_ptr(ws, s);
   uint16_t* Y = y_ptr(ws, s);
   CUtensorMap tm_w1, tm_h, tm_w2;
   if ((rc = map_3d(&tm_w1, w1, (uint64_t)s->F, (uint64_t)s->H, (uint64_t)s->E, 64, 64, "W1")) != MOE_OK) return rc;
@@ -269,7 +291,7 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
 }
 
 int clear_status(void* ws, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(int), st);
+  cudaError_t e = cudaMemsetAsync(ws, 0, 128, st);  // status word and ticket
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "cudaMemsetAsync(status)");
 }
 
@@ -323,13 +345,20 @@ size_t moe_workspace_size(const moe_shape* s) {
   return ws_bytes_for(s);
 }
 
+size_t moe_route_workspace_size(const moe_shape* s) {
+  if (check_shape(s, false) != MOE_OK) return 0;
+  return route_ws_bytes(s);
+}
+
 int moe_route(const moe_shape* s, const uint16_t* x, const uint16_t* w_router, const float* b_router,
               int32_t* ids, float* weights, int32_t* counts, int32_t* offsets, int32_t* perm,
               int32_t* slot, void* ws, size_t ws_bytes, void* stream) {
   int rc = check_shape(s, false);
   if (rc != MOE_OK) return rc;
   REQUIRE_PTR(ws);
-  if (ws_bytes < MOE_WS_MIN_BYTES) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
+  if (ws_bytes < route_ws_bytes(s))
+    return fail(MOE_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed (moe_route_workspace_size)",
+                ws_bytes, route_ws_bytes(s));
   REQUIRE_PTR(counts);
   REQUIRE_PTR(offsets);
   if (b_router && !aligned16(b_router)) return fail(MOE_ERR_INVALID_ARG, "b_router is not 16-byte aligned");
@@ -352,7 +381,9 @@ int moe_dispatch(const moe_shape* s, const int32_t* ids, int32_t* counts, int32_
   int rc = check_shape(s, false);
   if (rc != MOE_OK) return rc;
   REQUIRE_PTR(ws);
-  if (ws_bytes < MOE_WS_MIN_BYTES) return fail(MOE_ERR_INVALID_ARG, "workspace too small");
+  if (ws_bytes < route_ws_bytes(s))
+    return fail(MOE_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed (moe_route_workspace_size)",
+                ws_bytes, route_ws_bytes(s));
   REQUIRE_PTR(counts);
   REQUIRE_PTR(offsets);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -363,18 +394,34 @@ int moe_dispatch(const moe_shape* s, const int32_t* ids, int32_t* counts, int32_
   REQUIRE_PTR(ids);
   REQUIRE_PTR(perm);
   REQUIRE_PTR(slot);
+  const int cap = (int)capacity_of(s);
+  HistArgs ha;
+  ha.ids = ids;
+  ha.T = s->T;
+  ha.k = s->k;
+  ha.E = s->E;
+  ha.seg_tokens = kSegTokens;
+  ha.capacity = cap;
+  ha.hist = hist_ptr(ws);
+  ha.counts = counts;
+  ha.offsets = offsets;
+  ha.ticket = ticket_ptr(ws);
+  ha.status = status_ptr(ws);
+  cudaError_t e = launch_histogram(ha, st);
+  if (e != cudaSuccess) return cuda_fail(e, "histogram launch");
   DispatchArgs da;
   da.ids = ids;
   da.T = s->T;
   da.k = s->k;
   da.E = s->E;
-  da.capacity = (int)capacity_of(s);
-  da.counts = counts;
+  da.capacity = cap;
+  da.seg_tokens = kSegTokens;
+  da.base = hist_ptr(ws);
   da.offsets = offsets;
   da.perm = perm;
   da.slot = slot;
   da.status = status_ptr(ws);
-  cudaError_t e = launch_dispatch(da, st);
+  e = launch_dispatch(da, st);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "dispatch launch");
 }
 

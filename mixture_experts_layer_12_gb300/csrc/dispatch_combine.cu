@@ -6,11 +6,12 @@
 // expert e's rows are its assignments in ascending (token, slot) order, each
 // recorded with its original position (token_indices) and its top-k slot
 // (token_weight_indices) -- here packed as perm[r] = t*k + j, with the
-// inverse map slot[t][j].  Instead of one O(T*k) scan per expert, one pass
-// ranks every assignment among the earlier assignments of its expert
-// (warp match + per-warp counts + a scan across warps), which yields the
-// same order.  Assignments ranked at or beyond the capacity are dropped
-// (token dropping, "CANN ops-transformer：MoE 路由算子的负载均衡策略",
+// inverse map slot[t][j].  Instead of one O(T*k) scan per expert, every
+// assignment is ranked among the earlier assignments of its expert: per
+// 128-token segment counts (from the router, or the histogram kernel) are
+// scanned across segments, then one CTA per segment adds the in-segment
+// rank -- the same order.  Assignments ranked at or beyond the capacity are
+// dropped (token dropping, "CANN ops-transformer：MoE 路由算子的负载均衡策略",
 // section "负载不均衡的根源"; capacity_factor of the article's section 4.3).
 //
 // Combine restates ScatterWithWeights (listing "Scatter + 加权":
@@ -26,118 +27,68 @@ namespace {
 constexpr int DTHREADS = 1024;
 constexpr int DWARPS = DTHREADS / 32;
 
+// One CTA per segment of seg_tokens tokens (seg_tokens * k <= 1024
+// assignments, one per thread).  An assignment's rank within its expert is
+// the segment's exclusive base (all earlier segments' assignments to that
+// expert, from the scan) + the assignments to the same expert earlier in
+// this segment (warp match + per-warp counts scanned across warps).
 __global__ void __launch_bounds__(DTHREADS, 1) dispatch_kernel(const DispatchArgs a) {
-  __shared__ int s_cnt[kMaxExperts];
+  __shared__ int s_base[kMaxExperts];
   __shared__ int s_off[kMaxExperts + 1];
-  __shared__ int s_run[kMaxExperts];
   __shared__ int s_wc[DWARPS * kMaxExperts];  // [warp][expert]
-  __shared__ int s_bad;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int E = a.E;
+  const int seg = blockIdx.x;
   const int Tk = a.T * a.k;
-  const int cap = a.capacity;  // -1: unlimited
+  const int i0 = seg * a.seg_tokens * a.k;
+  const int n = min(a.seg_tokens * a.k, Tk - i0);
 
   for (int e = tid; e < E; e += DTHREADS) {
-    s_cnt[e] = 0;
-    s_run[e] = 0;
+    s_base[e] = a.base[(size_t)seg * E + e];
+    s_off[e] = a.offsets[e];
   }
-  if (tid == 0) s_bad = 0;
+  if (tid == 0) s_off[E] = a.offsets[E];
+  for (int idx = tid; idx < DWARPS * E; idx += DTHREADS) s_wc[idx] = 0;
   __syncthreads();
 
-  // 1. histogram of assignments per expert
-  for (int i = tid; i < Tk; i += DTHREADS) {
-    const int e = __ldg(a.ids + i);
-    if (e >= 0 && e < E)
-      atomicAdd(&s_cnt[e], 1);
-    else
-      s_bad = 1;
+  int e = -1;
+  if (tid < n) {
+    e = __ldg(a.ids + i0 + tid);
+    if (e < 0 || e >= E) e = -1;
   }
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const int rank_w = __popc(peers & ((1u << lane) - 1u));
+  if (e >= 0 && rank_w == 0) s_wc[warp * E + e] = __popc(peers);
   __syncthreads();
-
-  // 2. kept counts (capacity clip) and their exclusive scan (warp 0)
-  if (warp == 0) {
-    int loc[8];
-    int sum = 0;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int e = lane * 8 + u;
-      int n = 0;
-      if (e < E) {
-        n = s_cnt[e];
-        if (cap >= 0) n = min(n, cap);
-      }
-      loc[u] = n;
-      sum += n;
-    }
-    int incl = sum;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += y;
-    }
-    int run = incl - sum;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int e = lane * 8 + u;
-      if (e < E) {
-        s_off[e] = run;
-        a.offsets[e] = run;
-        a.counts[e] = loc[u];
-      }
-      run += loc[u];
-    }
-    if (lane == 31) {
-      s_off[E] = incl;
-      a.offsets[E] = incl;
+  for (int ee = tid; ee < E; ee += DTHREADS) {  // exclusive scan across warps
+    int run = 0;
+    for (int w = 0; w < DWARPS; ++w) {
+      const int c = s_wc[w * E + ee];
+      s_wc[w * E + ee] = run;
+      run += c;
     }
   }
   __syncthreads();
-
-  // 3. stable rank of every assignment within its expert, 1024 at a time
-  for (int base = 0; base < Tk; base += DTHREADS) {
-    for (int idx = tid; idx < DWARPS * E; idx += DTHREADS) s_wc[idx] = 0;
-    __syncthreads();
-    const int i = base + tid;
-    int e = -1;
-    if (i < Tk) {
-      e = __ldg(a.ids + i);
-      if (e < 0 || e >= E) e = -1;
-    }
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank_w = __popc(peers & ((1u << lane) - 1u));
-    if (e >= 0 && rank_w == 0) s_wc[warp * E + e] = __popc(peers);
-    __syncthreads();
-    // exclusive scan across warps per expert, continuing the running count
-    for (int ee = tid; ee < E; ee += DTHREADS) {
-      int run = s_run[ee];
-      for (int w = 0; w < DWARPS; ++w) {
-        const int c = s_wc[w * E + ee];
-        s_wc[w * E + ee] = run;
-        run += c;
+  if (tid < n) {
+    int sl = -1;
+    if (e >= 0) {
+      const int r = s_base[e] + s_wc[warp * E + e] + rank_w;
+      if (a.capacity < 0 || r < a.capacity) {
+        sl = s_off[e] + r;
+        a.perm[sl] = i0 + tid;
       }
-      s_run[ee] = run;
     }
-    __syncthreads();
-    if (i < Tk) {
-      int sl = -1;
-      if (e >= 0) {
-        const int r = s_wc[warp * E + e] + rank_w;
-        if (cap < 0 || r < cap) {
-          sl = s_off[e] + r;
-          a.perm[sl] = i;
-        }
-      }
-      a.slot[i] = sl;
-    }
-    __syncthreads();
+    a.slot[i0 + tid] = sl;
   }
-
-  // 4. unused tail of perm
-  for (int i = s_off[E] + tid; i < Tk; i += DTHREADS) a.perm[i] = -1;
-  if (tid == 0 && s_bad) record_status(a.status, MOE_DEV_BAD_ID);
+  // unused tail of perm, split across the segments
+  const int N = s_off[E];
+  const int per = (Tk - N + (int)gridDim.x - 1) / (int)gridDim.x;
+  const int lo = N + seg * per;
+  const int hi = min(Tk, lo + per);
+  for (int i = lo + tid; i < hi; i += DTHREADS) a.perm[i] = -1;
 }
 
 constexpr int CTHREADS = 128;
@@ -194,7 +145,8 @@ __global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
 }  // namespace
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st) {
-  dispatch_kernel<<<1, DTHREADS, 0, st>>>(a);
+  const int nseg = (a.T + a.seg_tokens - 1) / a.seg_tokens;
+  dispatch_kernel<<<nseg, DTHREADS, 0, st>>>(a);
   return cudaGetLastError();
 }
 

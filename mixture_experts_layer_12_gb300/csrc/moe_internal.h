@@ -16,16 +16,26 @@ constexpr int kMaxTopK = 8;
 // Default limit of every bounded device wait (one second).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
+// Token segments of the routing path: 128 tokens (one router tile).
+constexpr int kSegTokens = 128;
+
 // ---- router: logits (tcgen05, split-K over a thread-block cluster),
-//      TopK and the top-k softmax, fused; logits stay on chip.
+//      TopK and the top-k softmax, fused; logits stay on chip.  Also writes
+//      each tile's per-expert counts to `hist`; the last tile to finish
+//      scans them into counts / offsets and per-tile exclusive bases.
 struct RouterArgs {
   int T, H, E, k;
   int npad;        // E rounded up to 16 (the MMA N)
   int tmem_cols;   // power of two >= max(32, npad)
   int splits;      // cluster size along K (1, 2, 4 or 8)
+  int capacity;    // -1: unlimited
   const float* bias;  // [E] or null
   int32_t* ids;       // [T, k]
   float* weights;     // [T, k]
+  int32_t* hist;      // [ceil(T/128)][E] workspace
+  int32_t* counts;    // [E]
+  int32_t* offsets;   // [E+1]
+  unsigned int* ticket;  // zero before the launch
   int* status;
   uint64_t wait_limit_ns;
 };
@@ -36,12 +46,30 @@ cudaError_t launch_router(const CUtensorMap& tm_x, const CUtensorMap& tm_w, cons
                           cudaStream_t st);
 size_t router_smem_bytes(int E);
 
-// ---- dispatch: histogram, capacity clip, scan, stable counting sort.
+// ---- per-segment expert counts of caller-provided ids + the same scan.
+struct HistArgs {
+  const int32_t* ids;
+  int T, k, E;
+  int seg_tokens;
+  int capacity;  // -1: unlimited
+  int32_t* hist;
+  int32_t* counts;
+  int32_t* offsets;
+  unsigned int* ticket;  // zero before the launch
+  int* status;
+};
+cudaError_t launch_histogram(const HistArgs& a, cudaStream_t st);
+
+// ---- dispatch: one CTA per segment ranks its assignments within each
+//      expert and scatters perm / slot (capacity clip applied).
 struct DispatchArgs {
   const int32_t* ids;
   int T, k, E;
   int capacity;  // -1: unlimited
-  int32_t *counts, *offsets, *perm, *slot;
+  int seg_tokens;
+  const int32_t* base;     // [nseg][E] exclusive bases from the scan
+  const int32_t* offsets;  // [E+1]
+  int32_t *perm, *slot;
   int* status;
 };
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st);

@@ -1,6 +1,8 @@
 // router.cu -- fused router: logits = x · W_router (+ bias) on the tensor
 // cores, per-token TopK (ties to the lower expert index) and the softmax
 // over the k selected logits, in one kernel; the logits never reach HBM.
+// The kernel also counts each 128-token tile's assignments per expert and
+// the last tile to finish turns those counts into the dispatch offsets.
 //
 // Follows the router kernel of "用Ascend C写一个MoE融合算子", section
 // "1. Routing + Gating 合并" (Mmad for x × W_router, TopK per sample, then
@@ -11,35 +13,116 @@
 //
 // Design (sm_103a):
 //   * a tile of 128 tokens x E experts (E <= 256) is one tcgen05.mma
-//     accumulator (M = 128, N = E rounded up to 16) in TMEM;
+//     accumulator (M = 128, N = E rounded up to 16) in TMEM, fed by a TMA
+//     ring of up to 8 stages;
 //   * the K = H reduction is split across a cluster of S CTAs (S = 1..8) so
-//     that ceil(T/128) x S CTAs stream x from HBM in parallel; each CTA
-//     copies its fp32 partial from TMEM to shared memory and the cluster
-//     reduces the partials through distributed shared memory in a fixed
-//     rank order (deterministic);
-//   * CTA rank s then owns 128/S token rows: one warp per token, lane l
-//     holds experts l, l+32, ...; k rounds of a warp-shuffle argmax
-//     ((value, index) pairs, larger value wins, equal values -> lower
-//     index) give the ids in descending-logit order; the softmax over those
-//     k logits uses fp32 expf.
+//     that ceil(T/128) x S CTAs stream x from HBM in parallel.  Each CTA
+//     pushes the fp32 partial rows owned by rank r (rows [r*128/S, ...))
+//     into rank r's shared memory with DSMEM stores; after one cluster
+//     barrier every rank sums its rows' S partials locally in rank order
+//     (deterministic);
+//   * TopK: for E <= 64 one thread per token streams the E logits through a
+//     k-entry insertion list; for larger E one warp per token (lane l holds
+//     experts l, l+32, ...) runs k rounds of a shuffle argmax over (value,
+//     index) pairs.  Larger value first, equal values -> lower index.  The
+//     softmax over the k logits uses fp32 expf;
+//   * per-tile expert counts go to the workspace (summed through DSMEM
+//     atomics into rank 0); the last tile to finish (an atomic ticket, no
+//     waiting) scans them into counts / offsets (with the capacity clip) and
+//     per-tile exclusive bases for the dispatch kernel.
 #include <math.h>
 
 #include "tc_common.cuh"
 
 namespace moe {
+
+// hist[seg][e] (assignment counts per 128-token segment) -> exclusive bases
+// across segments, in place; counts[e] = min(total_e, cap); offsets =
+// exclusive scan of counts.  Run by one whole CTA (blockDim.x threads) after
+// every segment's counts are visible; `part` holds blockDim.x ints, `tot` E.
+__device__ void scan_segment_counts(int32_t* hist, int nseg, int E, int cap, int32_t* counts,
+                                    int32_t* offsets, int* part, int* tot) {
+  const int tid = threadIdx.x;
+  const int nt = blockDim.x;
+  const int G = max(1, nt / E);       // threads per expert column
+  const int cols = nt / G;            // columns per pass
+  for (int e0 = 0; e0 < E; e0 += cols) {
+    const int c = tid / G;
+    const int g = tid % G;
+    const int e = e0 + c;
+    const bool act = c < cols && e < E;
+    const int L = (nseg + G - 1) / G;
+    const int s0 = min(nseg, g * L);
+    const int s1 = min(nseg, s0 + L);
+    int sum = 0;
+    if (act)
+      for (int sg = s0; sg < s1; ++sg) sum += __ldcg(hist + (size_t)sg * E + e);
+    part[tid] = sum;
+    __syncthreads();
+    if (act) {
+      int run = 0;
+      for (int gg = 0; gg < g; ++gg) run += part[c * G + gg];
+      for (int sg = s0; sg < s1; ++sg) {
+        const int v = __ldcg(hist + (size_t)sg * E + e);
+        hist[(size_t)sg * E + e] = run;
+        run += v;
+      }
+      if (g == G - 1) tot[e] = run;
+    }
+    __syncthreads();
+  }
+  if (tid < 32) {
+    const int lane = tid;
+    int loc[8];
+    int sum = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = lane * 8 + u;
+      int n = 0;
+      if (e < E) {
+        n = tot[e];
+        if (cap >= 0) n = min(n, cap);
+      }
+      loc[u] = n;
+      sum += n;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = lane * 8 + u;
+      if (e < E) {
+        offsets[e] = run;
+        counts[e] = loc[u];
+      }
+      run += loc[u];
+    }
+    if (lane == 31) offsets[E] = incl;
+  }
+}
+
 namespace {
 
 constexpr int RBM = 128;
 constexpr int RBK = 64;
-constexpr int RSTAGES = 4;
 constexpr int RTHREADS = 128;
+constexpr int RMAX_STAGES = 8;
 
 struct RCtrl {
-  uint64_t full[RSTAGES];
-  uint64_t empty[RSTAGES];
+  uint64_t full[RMAX_STAGES];
+  uint64_t empty[RMAX_STAGES];
   uint64_t done;
   uint32_t tmem_base;
   int abort_flag;
+  int is_last;
+  int hist[kMaxExperts];
+  int part[RTHREADS];
+  int tot[kMaxExperts];
 };
 
 template <int NB64>
@@ -48,10 +131,11 @@ struct RCfg {
   static constexpr int B_CHUNK = RBK * 64 * 2;          // 8 KB
   static constexpr int B_BYTES = NB64 * B_CHUNK;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int PIPE = RSTAGES * STAGE;
+  static constexpr int STAGES = (196608 / STAGE) < RMAX_STAGES ? (196608 / STAGE) : RMAX_STAGES;
+  static constexpr int PIPE = STAGES * STAGE;
   static constexpr int PITCH = NB64 * 64 + 4;           // floats per partial row
-  static constexpr int PART = RBM * PITCH * 4;
-  static constexpr int DATA = PIPE > PART ? PIPE : PART;
+  static constexpr int RECV = RBM * PITCH * 4;          // S slots x 128/S rows = 128 rows
+  static constexpr int DATA = PIPE > RECV ? PIPE : RECV;
   static constexpr size_t SMEM = 1024 + (size_t)DATA + sizeof(RCtrl);
 };
 
@@ -68,6 +152,43 @@ __device__ bool rwait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns, i
   return true;
 }
 
+// k-entry insertion list: larger value first, equal values keep the
+// earlier (lower) expert; fully unrolled so it stays in registers.
+struct TopK8 {
+  float v[kMaxTopK];
+  int id[kMaxTopK];
+  int n;
+  __device__ __forceinline__ void init() {
+    n = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      v[j] = -INFINITY;
+      id[j] = 0;
+    }
+  }
+  // Inserts (val, e) before the first entry it beats strictly (or at the
+  // end); from there every entry shifts down one slot unconditionally, so
+  // displaced entries keep their order relative to equal values.
+  __device__ __forceinline__ void push(float val, int e, int k) {
+    float cv = val;
+    int ci = e;
+    bool shifting = false;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < k && (shifting || j >= n || cv > v[j])) {
+        shifting = true;
+        const float tv = v[j];
+        const int ti = id[j];
+        v[j] = cv;
+        id[j] = ci;
+        cv = tv;
+        ci = ti;
+      }
+    }
+    n = min(n + 1, k);
+  }
+};
+
 template <int NB64>
 __global__ void __launch_bounds__(RTHREADS)
     router_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
@@ -77,14 +198,15 @@ __global__ void __launch_bounds__(RTHREADS)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + RSTAGES * C::A_BYTES;
-  float* part = reinterpret_cast<float*>(smem);  // reuses the pipeline buffers afterwards
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+  float* recv = reinterpret_cast<float*>(smem);  // reuses the pipeline buffers afterwards
   RCtrl& c = *reinterpret_cast<RCtrl*>(smem + C::DATA);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = a.splits;
   const int s = (int)cluster_ctarank();
+  const int rpc = RBM / S;  // token rows owned by each rank
   const int m0 = blockIdx.y * RBM;
   const int KB = (a.H + RBK - 1) / RBK;
   const int kb0 = (int)(((long long)KB * s) / S);
@@ -92,7 +214,7 @@ __global__ void __launch_bounds__(RTHREADS)
   const int nkb = kb1 - kb0;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < RSTAGES; ++i) {
+    for (int i = 0; i < C::STAGES; ++i) {
       mbar_init(&c.full[i], 1);
       mbar_init(&c.empty[i], 1);
     }
@@ -100,6 +222,7 @@ __global__ void __launch_bounds__(RTHREADS)
     c.abort_flag = 0;
     fence_mbar_init();
   }
+  for (int e = threadIdx.x; e < a.E; e += RTHREADS) c.hist[e] = 0;
   if (warp == 1) {
     tmem_alloc(&c.tmem_base, (uint32_t)a.tmem_cols);
     tmem_relinquish();
@@ -126,13 +249,14 @@ __global__ void __launch_bounds__(RTHREADS)
         tma_load_2d(sB + stage * C::B_BYTES + cb * C::B_CHUNK, &tm_w, &c.full[stage], cb * 64,
                     kb * RBK);
       ++armed;
-      if (++stage == RSTAGES) {
+      if (++stage == C::STAGES) {
         stage = 0;
         phase ^= 1u;
       }
     }
-    for (int m = max(0, armed - RSTAGES); m < armed; ++m)
-      rwait_drain(&c.full[m % RSTAGES], (uint32_t)((m / RSTAGES) & 1), a.wait_limit_ns, a.status);
+    for (int m = max(0, armed - C::STAGES); m < armed; ++m)
+      rwait_drain(&c.full[m % C::STAGES], (uint32_t)((m / C::STAGES) & 1), a.wait_limit_ns,
+                  a.status);
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer: logits[128 x npad] += x_tile · W_tile
     const uint32_t idesc = idesc_bf16_f32(RBM, a.npad, false, true);
@@ -150,7 +274,7 @@ __global__ void __launch_bounds__(RTHREADS)
         umma_bf16(tmem, ad, bd, idesc, (i | j) != 0 ? 1u : 0u);
       }
       umma_commit(&c.empty[stage]);
-      if (++stage == RSTAGES) {
+      if (++stage == C::STAGES) {
         stage = 0;
         phase ^= 1u;
       }
@@ -159,17 +283,21 @@ __global__ void __launch_bounds__(RTHREADS)
   }
   __syncwarp();
 
-  // ---- all warps: wait for the accumulator, dump it to shared memory
+  // ---- all warps: accumulator complete; every rank's pipeline is idle
   int ok = 1;
   if (lane == 0) ok = rwait_drain(&c.done, 0, a.wait_limit_ns, a.status);
   ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncthreads();  // the producer's drain is complete too
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc_fence_after();
   const bool have = ok && nkb > 0 && c.abort_flag == 0;
+  cluster_sync_all();  // no rank still reads its pipeline buffers (now receive buffers)
+
+  // ---- push this rank's partial of row `row` to the rank that owns it
   {
     const int row = warp * 32 + lane;
-    float* dst = part + row * C::PITCH;
+    const int owner = row / rpc;
+    const uint32_t dst =
+        dsmem_map(smem_u32(recv + (size_t)(s * rpc + row % rpc) * C::PITCH), (uint32_t)owner);
     const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16);
     for (int col = 0; col < a.npad; col += 16) {
       uint32_t v[16];
@@ -177,12 +305,11 @@ __global__ void __launch_bounds__(RTHREADS)
       tmem_ld_wait();
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        float4 f;
-        f.x = have ? __uint_as_float(v[4 * g + 0]) : 0.f;
-        f.y = have ? __uint_as_float(v[4 * g + 1]) : 0.f;
-        f.z = have ? __uint_as_float(v[4 * g + 2]) : 0.f;
-        f.w = have ? __uint_as_float(v[4 * g + 3]) : 0.f;
-        *reinterpret_cast<float4*>(dst + col + 4 * g) = f;
+        const float f0 = have ? __uint_as_float(v[4 * g + 0]) : 0.f;
+        const float f1 = have ? __uint_as_float(v[4 * g + 1]) : 0.f;
+        const float f2 = have ? __uint_as_float(v[4 * g + 2]) : 0.f;
+        const float f3 = have ? __uint_as_float(v[4 * g + 3]) : 0.f;
+        dsmem_st_v4(dst + (uint32_t)((col + 4 * g) * 4), f0, f1, f2, f3);
       }
     }
   }
@@ -192,74 +319,122 @@ __global__ void __launch_bounds__(RTHREADS)
     tc_fence_after();
     tmem_dealloc(tmem, (uint32_t)a.tmem_cols);
   }
+  cluster_sync_all();  // every partial of this rank's rows has arrived
 
-  // ---- cluster: partials of every rank are complete and visible
-  cluster_sync_all();
-
-  constexpr int NU = 2 * NB64;  // 32-expert groups per lane
-  const int rows_per_cta = RBM / S;
-  for (int ri = warp; ri < rows_per_cta; ri += RTHREADS / 32) {
-    const int row = s * rows_per_cta + ri;
-    const int t = m0 + row;
-    if (t >= a.T) continue;  // warp-uniform
-    const uint32_t lbase = smem_u32(part + row * C::PITCH);
-    float v[NU];
-    uint32_t taken = 0;  // bit u: expert lane + 32u unavailable
+  // ---- reduce the S partials of each owned row, TopK, softmax
+  // logit of owned row li, expert e: sum over ranks r ascending, then + bias
+  auto logit = [&](int li, int e) -> float {
+    float sum = recv[(size_t)li * C::PITCH + e];
+    for (int r = 1; r < S; ++r) sum += recv[(size_t)(r * rpc + li) * C::PITCH + e];
+    if (a.bias) sum += __ldg(a.bias + e);
+    return isnan(sum) ? -INFINITY : sum;
+  };
+  if (a.E <= 64) {
+    for (int li = threadIdx.x; li < rpc; li += RTHREADS) {
+      const int t = m0 + s * rpc + li;
+      if (t >= a.T) continue;
+      TopK8 tk;
+      tk.init();
+      for (int e = 0; e < a.E; ++e) tk.push(logit(li, e), e, a.k);
+      const float mx = tk.v[0];
+      float ex[kMaxTopK];
+      float z = 0.f;
 #pragma unroll
-    for (int u = 0; u < NU; ++u) {
-      const int e = lane + 32 * u;
-      v[u] = -INFINITY;
-      if (e < a.E) {
-        float sum = dsmem_ld_f32(dsmem_map(lbase + 4u * (uint32_t)e, 0));
-        for (int r = 1; r < S; ++r) sum += dsmem_ld_f32(dsmem_map(lbase + 4u * (uint32_t)e, (uint32_t)r));
-        if (a.bias) sum += __ldg(a.bias + e);
-        v[u] = isnan(sum) ? -INFINITY : sum;
-      } else {
-        taken |= 1u << u;
+      for (int j = 0; j < kMaxTopK; ++j) {
+        ex[j] = j < a.k ? expf(tk.v[j] - mx) : 0.f;
+        z += ex[j];
+      }
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j) {
+        if (j < a.k) {
+          a.ids[(size_t)t * a.k + j] = tk.id[j];
+          a.weights[(size_t)t * a.k + j] = ex[j] / z;
+          atomicAdd(&c.hist[tk.id[j]], 1);
+        }
       }
     }
-    int my_id = 0;
-    float my_val = 0.f;
-    for (int j = 0; j < a.k; ++j) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
+  } else {
+    constexpr int NU = 2 * NB64;  // 32-expert groups per lane
+    for (int li = warp; li < rpc; li += RTHREADS / 32) {
+      const int t = m0 + s * rpc + li;
+      if (t >= a.T) continue;  // warp-uniform
+      float v[NU];
+      uint32_t taken = 0;  // bit u: expert lane + 32u unavailable
 #pragma unroll
       for (int u = 0; u < NU; ++u) {
         const int e = lane + 32 * u;
-        if (!((taken >> u) & 1u) && (v[u] > bv || (v[u] == bv && e < be))) {
-          bv = v[u];
-          be = e;
+        v[u] = -INFINITY;
+        if (e < a.E)
+          v[u] = logit(li, e);
+        else
+          taken |= 1u << u;
+      }
+      int my_id = 0;
+      float my_val = 0.f;
+      for (int j = 0; j < a.k; ++j) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+          const int e = lane + 32 * u;
+          if (!((taken >> u) & 1u) && (v[u] > bv || (v[u] == bv && e < be))) {
+            bv = v[u];
+            be = e;
+          }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+          const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+          if (ov > bv || (ov == bv && oe < be)) {
+            bv = ov;
+            be = oe;
+          }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        if (lane == j) {
+          my_id = be;
+          my_val = bv;
         }
       }
+      const float mx = __shfl_sync(0xffffffffu, my_val, 0);
+      float ex = lane < a.k ? expf(my_val - mx) : 0.f;
+      float z = ex;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (ov > bv || (ov == bv && oe < be)) {
-          bv = ov;
-          be = oe;
-        }
+      for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+      if (lane < a.k) {
+        a.ids[(size_t)t * a.k + lane] = my_id;
+        a.weights[(size_t)t * a.k + lane] = ex / z;
+        atomicAdd(&c.hist[my_id], 1);
       }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (lane == j) {
-        my_id = be;
-        my_val = bv;
-      }
-    }
-    // softmax over the k selected logits; column 0 holds the maximum
-    const float mx = __shfl_sync(0xffffffffu, my_val, 0);
-    float ex = lane < a.k ? expf(my_val - mx) : 0.f;
-    float z = ex;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-    if (lane < a.k) {
-      a.ids[(size_t)t * a.k + lane] = my_id;
-      a.weights[(size_t)t * a.k + lane] = ex / z;
     }
   }
+  __syncthreads();
 
-  // keep this CTA's partial alive until every rank has read it
-  cluster_sync_all();
+  // ---- this tile's expert counts: sum into rank 0, which publishes them
+  if (S > 1) {
+    const uint32_t h0 = dsmem_map(smem_u32(&c.hist[0]), 0);
+    if (s != 0)
+      for (int e = threadIdx.x; e < a.E; e += RTHREADS)
+        if (c.hist[e]) atomicAdd_cluster_u32(h0 + 4u * (uint32_t)e, (uint32_t)c.hist[e]);
+    cluster_sync_all();
+  }
+  if (s == 0) {
+    for (int e = threadIdx.x; e < a.E; e += RTHREADS)
+      a.hist[(size_t)blockIdx.y * a.E + e] = c.hist[e];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const unsigned prev = atomicAdd(a.ticket, 1u);
+      c.is_last = (prev == gridDim.y - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (c.is_last) {
+      __threadfence();
+      scan_segment_counts(a.hist, (int)gridDim.y, a.E, a.capacity, a.counts, a.offsets, c.part,
+                          c.tot);
+    }
+  }
 }
 
 template <int NB64>
@@ -285,6 +460,41 @@ template <int NB64>
 cudaError_t set_attr_nb() {
   return cudaFuncSetAttribute(router_kernel<NB64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)RCfg<NB64>::SMEM);
+}
+
+// ---- histogram of caller-provided ids (moe_dispatch): one CTA per
+// 128-token segment, then the last CTA scans as the router does.
+constexpr int HTHREADS = 1024;
+
+__global__ void __launch_bounds__(HTHREADS) histogram_kernel(const HistArgs a) {
+  __shared__ int s_hist[kMaxExperts];
+  __shared__ int s_part[HTHREADS];
+  __shared__ int s_tot[kMaxExperts];
+  __shared__ int s_last;
+  for (int e = threadIdx.x; e < a.E; e += HTHREADS) s_hist[e] = 0;
+  __syncthreads();
+  const int n = min(a.seg_tokens, a.T - (int)blockIdx.x * a.seg_tokens) * a.k;
+  const int32_t* ids = a.ids + (size_t)blockIdx.x * a.seg_tokens * a.k;
+  bool bad = false;
+  for (int i = threadIdx.x; i < n; i += HTHREADS) {
+    const int e = __ldg(ids + i);
+    if (e >= 0 && e < a.E)
+      atomicAdd(&s_hist[e], 1);
+    else
+      bad = true;
+  }
+  if (bad) record_status(a.status, MOE_DEV_BAD_ID);
+  __syncthreads();
+  for (int e = threadIdx.x; e < a.E; e += HTHREADS) a.hist[(size_t)blockIdx.x * a.E + e] = s_hist[e];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(a.ticket, 1u) == gridDim.x - 1) ? 1 : 0;
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    scan_segment_counts(a.hist, (int)gridDim.x, a.E, a.capacity, a.counts, a.offsets, s_part,
+                        s_tot);
+  }
 }
 
 }  // namespace
@@ -315,6 +525,12 @@ cudaError_t launch_router(const CUtensorMap& tm_x, const CUtensorMap& tm_w, cons
     case 3: return launch_nb<3>(tm_x, tm_w, a, st);
     default: return launch_nb<4>(tm_x, tm_w, a, st);
   }
+}
+
+cudaError_t launch_histogram(const HistArgs& a, cudaStream_t st) {
+  const int nseg = (a.T + a.seg_tokens - 1) / a.seg_tokens;
+  histogram_kernel<<<nseg, HTHREADS, 0, st>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace moe

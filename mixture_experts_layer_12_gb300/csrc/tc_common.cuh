@@ -259,6 +259,21 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t local_saddr, uint32_t ran
   return r;
 }
 
+// Store 16 bytes into (possibly another CTA's) shared memory of the cluster.
+__device__ __forceinline__ void dsmem_st_v4(uint32_t cluster_saddr, float a, float b, float c,
+                                            float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_saddr), "f"(a),
+               "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+// Relaxed atomic add on a 32-bit word in (possibly another CTA's) shared
+// memory of the cluster; made visible by the next cluster barrier.
+__device__ __forceinline__ void atomicAdd_cluster_u32(uint32_t cluster_saddr, uint32_t v) {
+  asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(cluster_saddr), "r"(v)
+               : "memory");
+}
+
 __device__ __forceinline__ float dsmem_ld_f32(uint32_t cluster_saddr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_saddr) : "memory");

@@ -34,7 +34,7 @@ def exported_symbols(path):
 
 def test_exports_match_header(lib):
     decl = declared_symbols()
-    assert len(decl) == 12
+    assert len(decl) == 13
     assert decl == set(moe.EXPORTS)
     exported = {s for s in exported_symbols(moe.LIB_PATH) if s.startswith("moe_")}
     assert exported == decl
@@ -48,8 +48,11 @@ def test_version(lib):
 
 def test_workspace_size_and_capacity_host_only(lib):
     s = moe.make_shape(4096, 4096, 14336, 8, 2)
-    # status block + h [T*k, F] + Y [T*k, H], bf16
-    assert moe.moe_workspace_size(s) == 1024 + 8192 * 14336 * 2 + 8192 * 4096 * 2
+    # status block + per-128-token expert counts + h [T*k, F] + Y [T*k, H], bf16
+    assert moe.moe_workspace_size(s) == 1024 + 1024 + 8192 * 14336 * 2 + 8192 * 4096 * 2
+    assert moe.moe_route_workspace_size(s) == 1024 + 1024  # 32 tiles x 8 experts x 4 B
+    s3 = moe.make_shape(2048, 4096, 0, 128, 8)
+    assert moe.moe_route_workspace_size(s3) == 1024 + 16 * 128 * 4
     assert moe.moe_expert_capacity(moe.make_shape(8192, 2048, 1408, 64, 4, 1.2)) == 615
     assert moe.moe_expert_capacity(moe.make_shape(8192, 2048, 1408, 64, 4, None)) == -1
     assert moe.moe_expert_capacity(moe.make_shape(64, 128, 256, 8, 2, 1.0)) == 16
@@ -95,6 +98,9 @@ def test_null_and_misaligned_pointers_rejected(lib):
     # route: null counts
     rc = lib.moe_route(ctypes.byref(s), *([None] * 9), ctypes.c_void_p(0x1000), 4096, None)
     assert rc == moe.MOE_ERR_INVALID_ARG
+    # route: workspace smaller than moe_route_workspace_size
+    rc = lib.moe_route(ctypes.byref(s), *([None] * 9), ctypes.c_void_p(0x1000), 1024, None)
+    assert rc == moe.MOE_ERR_INVALID_ARG and b"moe_route_workspace_size" in lib.moe_last_error_string()
     # self-test limit outside its range
     rc = lib.moe_selftest_wait_timeout(ctypes.c_void_p(0x1000), 4096, 10, None)
     assert rc == moe.MOE_ERR_INVALID_ARG

@@ -34,7 +34,7 @@ def to_dev(inputs):
 def gpu_route(cfg, dev_in):
     s = moe.make_shape(cfg.T, cfg.H, max(cfg.F, 8), cfg.E, cfg.k, cfg.capacity_factor)
     r = moe.alloc_routing(cfg.T, cfg.E, cfg.k, DEV)
-    ws = torch.empty(1024, dtype=torch.uint8, device=DEV)
+    ws = moe.alloc_route_workspace(s, DEV)
     moe.moe_route(s, dev_in["x"], dev_in["w_router"], dev_in["bias"], r.ids, r.weights, r.counts,
                   r.offsets, r.perm, r.slot, ws)
     assert moe.moe_get_device_status(ws) == 0
@@ -95,7 +95,8 @@ def test_bounded_wait_times_out_and_reports():
 @pytest.mark.parametrize("T,E,k,cf,skew", [
     (1, 8, 1, None, False), (7, 8, 2, None, False), (1000, 64, 4, 1.0, True),
     (8192, 64, 4, 1.2, True), (3000, 256, 8, None, False), (2048, 128, 8, 0.5, False),
-    (4096, 8, 2, None, True), (513, 16, 3, 0.05, False),
+    (4096, 8, 2, None, True), (513, 16, 3, 0.05, False), (20000, 32, 8, 0.9, True),
+    (129, 256, 8, 0.3, False),
 ])
 def test_dispatch_fed_oracle_ids(T, E, k, cf, skew):
     rng = np.random.default_rng(T + E + k)
@@ -108,7 +109,7 @@ def test_dispatch_fed_oracle_ids(T, E, k, cf, skew):
     ids = np.stack([rng.choice(E, size=k, replace=False, p=p) for _ in range(T)]).astype(np.int32)
     s = moe.make_shape(T, 8, 8, E, k, cf)
     r = moe.alloc_routing(T, E, k, DEV)
-    ws = torch.empty(1024, dtype=torch.uint8, device=DEV)
+    ws = moe.alloc_route_workspace(s, DEV)
     moe.moe_dispatch(s, torch.from_numpy(ids).to(DEV), r.counts, r.offsets, r.perm, r.slot, ws)
     assert moe.moe_get_device_status(ws) == 0
     check_dispatch(ids, E, cf, np_(r.counts), np_(r.offsets), np_(r.perm), np_(r.slot))
@@ -118,7 +119,7 @@ def test_dispatch_bad_ids_flagged():
     ids = torch.tensor([[0, 9], [3, 1]], dtype=torch.int32, device=DEV)
     s = moe.make_shape(2, 8, 8, 8, 2)
     r = moe.alloc_routing(2, 8, 2, DEV)
-    ws = torch.empty(1024, dtype=torch.uint8, device=DEV)
+    ws = moe.alloc_route_workspace(s, DEV)
     moe.moe_dispatch(s, ids, r.counts, r.offsets, r.perm, r.slot, ws)
     with pytest.raises(moe.MoEError) as e:
         moe.moe_get_device_status(ws)
