@@ -49,6 +49,8 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=WORKLOADS, default="prefill")
     p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--graph-steps", type=int, default=20,
+                   help="forward steps captured per CUDA graph in the timed region")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-tokens", type=int, default=1366,
                    help="tokens of the workload the oracle runs for cpu_baseline")
@@ -256,22 +258,34 @@ def run_route_only(args, cfg, device):
         moe.moe_route(s, xs[i % copies], wr, None, r.ids, r.weights, r.counts, r.offsets, r.perm,
                       r.slot, ws, stream)
     torch.cuda.synchronize(device)
-    K = args.steps
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    # one CUDA graph holds one pass over all x copies; the timed region
+    # replays it, so host launch overhead does not enter the device time
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(stream)
+    with torch.cuda.graph(graph, stream=cap):
+        for i in range(copies):
+            moe.moe_route(s, xs[i], wr, None, r.ids, r.weights, r.counts, r.offsets, r.perm,
+                          r.slot, ws)
+    torch.cuda.synchronize(device)
+    graph.replay()
+    torch.cuda.synchronize(device)
+    reps = max(1, args.steps // copies)
+    K = reps * copies
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     clocks = ClockSampler(gpu_id_for(device))
     clocks.start()
     time.sleep(0.3)
     torch.cuda.synchronize(device)
     ev[0].record(stream)
-    for i in range(K):
-        moe.moe_route(s, xs[i % copies], wr, None, r.ids, r.weights, r.counts, r.offsets, r.perm,
-                      r.slot, ws, stream)
-        ev[i + 1].record(stream)
+    for _ in range(reps):
+        graph.replay()
+    ev[1].record(stream)
     torch.cuda.synchronize(device)
     clk = clocks.stop()
     if moe.moe_get_device_status(ws, stream) != 0:
         raise RuntimeError("device status set during the timed region")
-    elapsed = ev[0].elapsed_time(ev[K])
+    elapsed = ev[0].elapsed_time(ev[1])
     ms = elapsed / K
     peaks, src = load_peaks()
     w = kernel_work(cfg, cfg.T * cfg.k, 0)
@@ -327,15 +341,17 @@ def run_ours(args):
     stream = torch.cuda.current_stream(device)
 
     def step(events=None):
+        # stream=None: the binding uses torch's current stream (the capture
+        # stream while a CUDA graph is being captured)
         layer._ensure(cfg.T, device)
         r = layer.routing
         if events is None:
             moe.moe_forward(layer.shape, x, layer.w_router, layer.bias, layer.w1, layer.w2, layer.y,
-                            r.ids, r.weights, r.counts, r.offsets, r.perm, r.slot, layer.ws, stream)
+                            r.ids, r.weights, r.counts, r.offsets, r.perm, r.slot, layer.ws)
         else:
             moe.moe_forward_profiled(layer.shape, x, layer.w_router, layer.bias, layer.w1, layer.w2,
                                      layer.y, r.ids, r.weights, r.counts, r.offsets, r.perm, r.slot,
-                                     layer.ws, events, stream)
+                                     layer.ws, events)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -343,14 +359,29 @@ def run_ours(args):
     if moe.moe_get_device_status(layer.ws, stream) != 0:
         raise RuntimeError("device status set during warm-up")
 
-    K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
-    for row in evs:  # materialise the event handles outside the timed region
+    # The timed steps replay a CUDA graph of R consecutive forward steps (the
+    # same five kernels per step, with the library's per-kernel events), so
+    # host launch overhead does not enter the device time.
+    R = max(1, min(args.steps, args.graph_steps))
+    reps = max(1, args.steps // R)
+    K = R * reps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(R)]
+    for row in evs:  # materialise the event handles before capture
         for e in row:
             e.record(stream)
+    torch.cuda.synchronize(device)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(stream)
+    with torch.cuda.graph(graph, stream=cap):
+        for i in range(R):
+            step(evs[i])
+    torch.cuda.synchronize(device)
+    for _ in range(2):  # warm replays
+        graph.replay()
+    torch.cuda.synchronize(device)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(device)
 
     clocks = ClockSampler(gpu_id_for(device))
     clocks.start()
@@ -359,8 +390,8 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize(device)
     t_start.record(stream)
-    for i in range(K):
-        step(evs[i])
+    for _ in range(reps):
+        graph.replay()
     t_end.record(stream)
     torch.cuda.synchronize(device)
     if world > 1:
@@ -379,8 +410,8 @@ def run_ours(args):
 
     # per-kernel device time (averaged over the timed steps)
     names = moe.KERNEL_NAMES
-    per_kernel = {n: statistics.fmean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K))
-                  for j, n in enumerate(names)}
+    per_kernel = {n: statistics.fmean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(R))
+                  for j, n in enumerate(names)}  # the last replay's R steps
     counts = layer.routing.counts.cpu()
     n_rows = int(counts.sum().item())
     experts_hit = int((counts > 0).sum().item())
@@ -459,6 +490,7 @@ def run_ours(args):
         "config": {"workload": workload_desc(cfg), "tokens_per_gpu": cfg.T,
                    "parallelism": f"replicas x{world} (token data-parallel, no collective)",
                    "kept_rows": n_rows, "experts_hit": experts_hit,
+                   "timing": f"CUDA events around {reps} replays of a CUDA graph of {R} forward steps",
                    "l2": "inputs larger than L2: every step streams all expert weights "
                          f"({2 * 2 * cfg.E * cfg.H * cfg.F / 1e9:.2f} GB)"},
         "gpu_launches": len(names) * K,

@@ -15,6 +15,7 @@
 namespace moe {
 cudaError_t grouped_gemm_set_attributes();
 cudaError_t router_set_attributes();
+cudaError_t dispatch_combine_set_attributes();
 }  // namespace moe
 
 using namespace moe;
@@ -62,6 +63,8 @@ int device_setup(int* sms) {
       return fail(MOE_ERR_UNSUPPORTED, "built for sm_103a; device %d is sm_%d%d", dev, major, minor);
     if ((e = router_set_attributes()) != cudaSuccess) return cuda_fail(e, "router attributes");
     if ((e = grouped_gemm_set_attributes()) != cudaSuccess) return cuda_fail(e, "gemm attributes");
+    if ((e = dispatch_combine_set_attributes()) != cudaSuccess)
+      return cuda_fail(e, "dispatch/combine attributes");
     if (!g_encode) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -175,10 +178,12 @@ uint16_t* y_ptr(void* ws, const moe_shape* s) {
 
 // Optional timing hooks: ev[i] (a cudaEvent_t, may be null) is recorded on
 // the stream at kernel boundary i (0 = before the router, 1..5 = after the
-// router, dispatch, GEMM1, GEMM2 and combine).
+// router, dispatch, GEMM1, GEMM2 and combine).  Recorded as external events
+// so that, inside a stream capture, they become timed event-record nodes.
 int mark(void* const* ev, int i, cudaStream_t st) {
   if (!ev || !ev[i]) return MOE_OK;
-  cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+  cudaError_t e =
+      cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev[i]), st, cudaEventRecordExternal);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "cudaEventRecord");
 }
 
@@ -200,8 +205,16 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
   while (ra.tmem_cols < ra.npad) ra.tmem_cols *= 2;
   const int mtiles = (s->T + 127) / 128;
   const int kblocks = (s->H + 63) / 64;
+  // K splits per 128-token tile: as many as keep every cluster resident in a
+  // single wave (a second wave would double the router's time)
   ra.splits = 1;
-  while (ra.splits < 8 && mtiles * ra.splits * 2 <= sms && ra.splits * 2 <= kblocks) ra.splits *= 2;
+  while (ra.splits < 8 && mtiles * ra.splits * 2 <= sms && ra.splits * 2 <= kblocks) {
+    int fit = 0;
+    cudaError_t ce = router_max_clusters(s->E, ra.splits * 2, &fit);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaOccupancyMaxActiveClusters(router)");
+    if (fit < mtiles) break;
+    ra.splits *= 2;
+  }
   ra.capacity = (int)capacity_of(s);
   ra.bias = b_router;
   ra.ids = ids;

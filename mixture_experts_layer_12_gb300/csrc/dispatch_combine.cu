@@ -144,6 +144,18 @@ __global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
 
 }  // namespace
 
+// The router and GEMM kernels need the maximum shared-memory carveout; the
+// small kernels between them ask for the same so the SMs are not
+// reconfigured at every kernel boundary.
+cudaError_t dispatch_combine_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  return e;
+}
+
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st) {
   const int nseg = (a.T + a.seg_tokens - 1) / a.seg_tokens;
   dispatch_kernel<<<nseg, DTHREADS, 0, st>>>(a);

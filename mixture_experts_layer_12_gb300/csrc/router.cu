@@ -110,7 +110,7 @@ namespace {
 
 constexpr int RBM = 128;
 constexpr int RBK = 64;
-constexpr int RTHREADS = 128;
+constexpr int RTHREADS = 256;  // warps 0-3: pipeline and TMEM; all 8: epilogue
 constexpr int RMAX_STAGES = 8;
 
 struct RCtrl {
@@ -293,7 +293,8 @@ __global__ void __launch_bounds__(RTHREADS)
   cluster_sync_all();  // no rank still reads its pipeline buffers (now receive buffers)
 
   // ---- push this rank's partial of row `row` to the rank that owns it
-  {
+  // (warps 0-3: warp w may read TMEM lanes 32w .. 32w+31)
+  if (warp < 4) {
     const int row = warp * 32 + lane;
     const int owner = row / rpc;
     const uint32_t dst =
@@ -321,14 +322,18 @@ __global__ void __launch_bounds__(RTHREADS)
   }
   cluster_sync_all();  // every partial of this rank's rows has arrived
 
-  // ---- reduce the S partials of each owned row, TopK, softmax
-  // logit of owned row li, expert e: sum over ranks r ascending, then + bias
-  auto logit = [&](int li, int e) -> float {
+  // ---- reduce the S partials of each owned row in place (slot 0): sum over
+  // ranks ascending, then + bias; all threads, one (row, expert) each
+  for (int idx = threadIdx.x; idx < rpc * a.E; idx += RTHREADS) {
+    const int li = idx / a.E;
+    const int e = idx - li * a.E;
     float sum = recv[(size_t)li * C::PITCH + e];
     for (int r = 1; r < S; ++r) sum += recv[(size_t)(r * rpc + li) * C::PITCH + e];
     if (a.bias) sum += __ldg(a.bias + e);
-    return isnan(sum) ? -INFINITY : sum;
-  };
+    recv[(size_t)li * C::PITCH + e] = isnan(sum) ? -INFINITY : sum;
+  }
+  __syncthreads();
+  auto logit = [&](int li, int e) -> float { return recv[(size_t)li * C::PITCH + e]; };
   if (a.E <= 64) {
     for (int li = threadIdx.x; li < rpc; li += RTHREADS) {
       const int t = m0 + s * rpc + li;
@@ -457,6 +462,23 @@ cudaError_t launch_nb(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const Ro
 }
 
 template <int NB64>
+cudaError_t max_clusters_nb(int splits, int* out) {
+  using C = RCfg<NB64>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)splits, 1, 1);
+  cfg.blockDim = dim3(RTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(out, router_kernel<NB64>, &cfg);
+}
+
+template <int NB64>
 cudaError_t set_attr_nb() {
   return cudaFuncSetAttribute(router_kernel<NB64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)RCfg<NB64>::SMEM);
@@ -510,7 +532,9 @@ size_t router_smem_bytes(int E) {
 }
 
 cudaError_t router_set_attributes() {
-  cudaError_t e;
+  cudaError_t e = cudaFuncSetAttribute(histogram_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
   if ((e = set_attr_nb<1>()) != cudaSuccess) return e;
   if ((e = set_attr_nb<2>()) != cudaSuccess) return e;
   if ((e = set_attr_nb<3>()) != cudaSuccess) return e;
@@ -525,6 +549,32 @@ cudaError_t launch_router(const CUtensorMap& tm_x, const CUtensorMap& tm_w, cons
     case 3: return launch_nb<3>(tm_x, tm_w, a, st);
     default: return launch_nb<4>(tm_x, tm_w, a, st);
   }
+}
+
+// Co-resident clusters of `splits` router CTAs for E experts (cached per
+// device, E bucket and cluster size).
+cudaError_t router_max_clusters(int E, int splits, int* out) {
+  static int cache[64][4][4];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int nb = (E + 63) / 64 - 1;
+  const int si = splits == 1 ? 0 : splits == 2 ? 1 : splits == 4 ? 2 : 3;
+  if (dev >= 0 && dev < 64 && cache[dev][nb][si] > 0) {
+    *out = cache[dev][nb][si];
+    return cudaSuccess;
+  }
+  int n = 0;
+  switch (nb + 1) {
+    case 1: e = max_clusters_nb<1>(splits, &n); break;
+    case 2: e = max_clusters_nb<2>(splits, &n); break;
+    case 3: e = max_clusters_nb<3>(splits, &n); break;
+    default: e = max_clusters_nb<4>(splits, &n); break;
+  }
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) cache[dev][nb][si] = n;
+  *out = n;
+  return cudaSuccess;
 }
 
 cudaError_t launch_histogram(const HistArgs& a, cudaStream_t st) {
