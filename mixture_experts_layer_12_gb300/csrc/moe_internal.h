@@ -45,6 +45,8 @@ struct RouterArgs {
 cudaError_t launch_router(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterArgs& a,
                           cudaStream_t st);
 size_t router_smem_bytes(int E);
+// Clusters of `splits` router CTAs that can be resident at once.
+cudaError_t router_max_clusters(int E, int splits, int* out);
 
 // ---- per-segment expert counts of caller-provided ids + the same scan.
 struct HistArgs {
