@@ -182,8 +182,12 @@ uint16_t* y_ptr(void* ws, const moe_shape* s) {
 // so that, inside a stream capture, they become timed event-record nodes.
 int mark(void* const* ev, int i, cudaStream_t st) {
   if (!ev || !ev[i]) return MOE_OK;
-  cudaError_t e =
-      cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev[i]), st, cudaEventRecordExternal);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  e = cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev[i]), st,
+                               cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal
+                                                                   : cudaEventRecordDefault);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "cudaEventRecord");
 }
 

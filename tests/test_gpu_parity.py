@@ -280,3 +280,29 @@ def test_split_entry_points_match_forward():
     assert torch.equal(y, y2)
     for a, b in [(r.ids, layer.routing.ids), (r.slot, layer.routing.slot), (r.perm, layer.routing.perm)]:
         assert torch.equal(a, b)
+
+
+def test_profiled_forward_eager_and_captured():
+    cfg = moe_synth.MoEConfig("prof", T=256, H=128, F=256, E=8, k=2, seed=25)
+    dev_in = to_dev(moe_synth.make_inputs(cfg))
+    layer, y_ref = gpu_forward(cfg, dev_in)
+    y_ref = y_ref.clone()
+    r = layer.routing
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    for e in evs:
+        e.record()
+    args = (layer.shape, dev_in["x"], layer.w_router, layer.bias, layer.w1, layer.w2, layer.y, r.ids,
+            r.weights, r.counts, r.offsets, r.perm, r.slot, layer.ws)
+    moe.moe_forward_profiled(*args, evs)  # eager
+    torch.cuda.synchronize()
+    times = [evs[i].elapsed_time(evs[i + 1]) for i in range(5)]
+    assert all(t >= 0 for t in times)
+    assert torch.equal(layer.y, y_ref)
+    g = torch.cuda.CUDAGraph()  # captured: events become timed graph nodes
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        moe.moe_forward_profiled(*args, evs)
+    layer.y.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert all(evs[i].elapsed_time(evs[i + 1]) >= 0 for i in range(5))
+    assert torch.equal(layer.y, y_ref)
