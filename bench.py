@@ -152,6 +152,34 @@ def gpu_id_for(device):
         return vis.split(",")[idx] if vis else str(idx)
 
 
+# ------------------------------------------------------------- multi-rank --
+
+def rank_inputs(cfg, rank: int, world: int) -> dict:
+    """Inputs of one data-parallel replica: the layer's weights are shared,
+    the tokens x are drawn per rank (seed offset 1000*rank) when world > 1."""
+    import moe_synth
+    inputs = moe_synth.make_inputs(cfg)
+    if world > 1:
+        inputs["x"] = moe_synth.make_x(cfg.with_(seed=cfg.seed + 1000 * rank))
+    return inputs
+
+
+def max_over_ranks(value: float, device) -> float:
+    """Max of a per-rank float over the process group (identity at N = 1)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_throughput(tokens_per_rank: int, world: int, steps: int, max_elapsed_ms: float) -> float:
+    """Tokens/s of the whole job: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank * steps / (max_elapsed_ms / 1e3)
+
+
 # --------------------------------------------------------- work per kernel --
 
 def kernel_work(cfg, n_rows, experts_hit):
@@ -328,12 +356,7 @@ def run_ours(args):
     cfg = workload_cfg(args.workload)
     if not cfg.has_ffn:
         return run_route_only(args, cfg, device)
-    if world > 1:  # each replica routes its own tokens
-        cfg_rank = cfg.with_(seed=cfg.seed + 1000 * rank)
-        inputs = moe_synth.make_inputs(cfg)
-        inputs["x"] = moe_synth.make_x(cfg_rank)
-    else:
-        inputs = moe_synth.make_inputs(cfg)
+    inputs = rank_inputs(cfg, rank, world)
     dev = {k: (None if v is None else v.to(device)) for k, v in inputs.items()}
     layer = moe.MoELayer(dev["w_router"], dev["w1"], dev["w2"], cfg.k, bias=dev["bias"],
                          capacity_factor=cfg.capacity_factor)
@@ -401,12 +424,9 @@ def run_ours(args):
     if moe.moe_get_device_status(layer.ws, stream) != 0:
         raise RuntimeError("device status set during the timed region")
 
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, device)
     ms_per_step = elapsed_ms / K
-    value = world * cfg.T * K / (elapsed_ms / 1e3)
+    value = whole_job_throughput(cfg.T, world, K, elapsed_ms)
 
     # per-kernel device time (averaged over the timed steps)
     names = moe.KERNEL_NAMES
@@ -467,11 +487,8 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize(device)
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": world * cfg.T * E2E / (e2e_ms / 1e3), "unit": UNIT,
+    e2e_ms = max_over_ranks(e2e_ms, device)
+    e2e = {"value": whole_job_throughput(cfg.T, world, E2E, e2e_ms), "unit": UNIT,
            "h2d_bytes_per_step": cfg.T * cfg.H * 2, "d2h_bytes_per_step": cfg.T * cfg.H * 2,
            "steps": E2E}
 
