@@ -35,10 +35,15 @@ WORKLOADS = ("prefill", "decode", "skewed", "skewed_cf1.2", "tiny", "router_k1",
              "router_k4", "router_k8")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
-# dominant kernel from one ncu capture, keyed by the sha256 of the kernel
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
+# one ncu capture, keyed by workload/kernel and by the sha256 of the kernel
 # source it was taken on; reported as null once the source changes.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # prefill workload, `ncu --set full` (profiles/expert_gemm_prefill.md, profiles/router_prefill.md)
+    "prefill/expert_gemm1": {"bytes": 1025576e3 + 222542592, "src": "ffn_gemm.cu", "src_sha": "7c00d930c3d66624"},
+    "prefill/expert_gemm2": {"bytes": 1434461e3 + 66115328, "src": "ffn_gemm.cu", "src_sha": "7c00d930c3d66624"},
+    "prefill/router": {"bytes": 33683200, "src": "router.cu", "src_sha": "cbbe0469d985a570"},
+}
 
 
 def parse_args():
@@ -217,7 +222,7 @@ def cpu_baseline(inputs, cfg, n_tokens):
     rows = list(range(0, cfg.T, stride))[:n_tokens]
     dt = oracle_sample_run(inputs, cfg, rows)
     return {"value": len(rows) / dt, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"{len(rows)} of {cfg.T} tokens (every {stride}th): routing, dispatch, "
+            "sample": f"{len(rows)} of {cfg.T} tokens (token stride {stride}): routing, dispatch, "
                       f"fp64 expert FFN and combine for those tokens; {dt:.1f} s"}
 
 
@@ -464,7 +469,7 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "peak_kind": f"HBM copy ({peak_src})",
                 "kernel": dominant, "bytes_per_launch": dk["bytes"]}
-    tr = NCU_TRAFFIC.get(dominant)
+    tr = NCU_TRAFFIC.get(f"{cfg.name}/{dominant}")
     roof["traffic"] = tr["bytes"] if tr and tr.get("src_sha") == src_sha(tr["src"]) else None
 
     # end to end through the public API with host buffers: H2D of x, the
