@@ -15,6 +15,8 @@ Parity status of each function (what pins it, in ``tests/test_oracle.py``):
   router_logits  fp64 dot product vs numpy fp64 matmul; hand-derived golden.
   topk           brute-force full sort and k-pass strict argmax; exact ties.
   gate_softmax   closed forms (k=1, equal logits), sum to 1, shift invariance.
+  gate_softmax_all  scipy softmax over all E (library routine as a step);
+                 k = E reduces to gate_softmax; renormalised = gate_softmax.
   capacity       hand-computed values (1.2*8192*4/64 -> 615, exact integers).
   dispatch       brute-force enumerate-then-stable-sort; invariants.
   expert_ffn     identity experts (GELU(z)-GELU(-z)=z); numpy fp64 FFN with
@@ -61,6 +63,7 @@ def _load():
         lib.oracle_router_logits.argtypes = [I, I, I, P, P, P, P, I]
         lib.oracle_topk.argtypes = [I, I, I, P, P, P]
         lib.oracle_gate_softmax.argtypes = [I, I, P, P]
+        lib.oracle_gate_softmax_all.argtypes = [I, I, I, P, P, I, P]
         lib.oracle_capacity.argtypes = [I, I, I, ctypes.c_double]
         lib.oracle_capacity.restype = ctypes.c_long
         lib.oracle_dispatch.argtypes = [I, I, I, ctypes.c_long, P, P, P, P, P]
@@ -68,6 +71,7 @@ def _load():
         lib.oracle_combine_rows.argtypes = [I, I, I, I, I, P, P, P, P, P, P, I, P, P, I]
         lib.oracle_max_threads.argtypes = []
         for name in ("oracle_router_logits", "oracle_topk", "oracle_gate_softmax",
+                     "oracle_gate_softmax_all",
                      "oracle_dispatch", "oracle_expert_ffn", "oracle_combine_rows",
                      "oracle_max_threads"):
             getattr(lib, name).restype = ctypes.c_int
@@ -129,6 +133,24 @@ def gate_softmax(top_logits: np.ndarray) -> np.ndarray:
     return w
 
 
+def gate_softmax_all(logits: np.ndarray, ids: np.ndarray, mode: int) -> np.ndarray:
+    """Softmax over all E logits, then the k selected probabilities (mode 1)
+    or those renormalised to sum 1 (mode 2)."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    idz = np.ascontiguousarray(ids, dtype=np.int32)
+    T, E = lg.shape
+    k = idz.shape[1]
+    w = np.empty((T, k), dtype=np.float32)
+    _check(_load().oracle_gate_softmax_all(T, E, k, _ptr(lg), _ptr(idz), int(mode), _ptr(w)),
+           "gate_softmax_all")
+    return w
+
+
+def gate_weights(logits: np.ndarray, ids: np.ndarray, top_logits: np.ndarray, gating: int = 0):
+    """Gate weights for gating mode 0 (softmax over the k selected), 1 or 2."""
+    return gate_softmax(top_logits) if gating == 0 else gate_softmax_all(logits, ids, gating)
+
+
 def capacity(T: int, k: int, E: int, capacity_factor) -> int:
     """Expert capacity, or -1 for no limit (cf None, <= 0 or NaN)."""
     cf = -1.0 if capacity_factor is None else float(capacity_factor)
@@ -178,18 +200,18 @@ def combine_rows(x, w1, w2, ids, w, slot, rows=None, nthreads: int = 0) -> np.nd
     return y
 
 
-def route(x, w_router, k: int, bias=None, nthreads: int = 0):
+def route(x, w_router, k: int, bias=None, nthreads: int = 0, gating: int = 0):
     """Steps 1-2: logits, TopK ids, top logits and gate weights (all tokens)."""
     logits = router_logits(x, w_router, bias, nthreads)
     ids, vals = topk(logits, k)
-    return logits, ids, vals, gate_softmax(vals)
+    return logits, ids, vals, gate_weights(logits, ids, vals, gating)
 
 
 def moe_forward(x, w_router, w1, w2, k: int, bias=None, capacity_factor=None,
-                rows=None, nthreads: int = 0) -> dict:
+                rows=None, nthreads: int = 0, gating: int = 0) -> dict:
     """The whole layer: routing and dispatch for all tokens, FFN and combine
     for ``rows`` (all tokens when None; tokens are independent once routed)."""
-    logits, ids, vals, w = route(x, w_router, k, bias, nthreads)
+    logits, ids, vals, w = route(x, w_router, k, bias, nthreads, gating)
     E = logits.shape[1]
     counts, offsets, perm, slot = dispatch(ids, E, capacity_factor)
     y = combine_rows(x, w1, w2, ids, w, slot, rows, nthreads)

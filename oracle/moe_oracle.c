@@ -164,6 +164,36 @@ int oracle_gate_softmax(int T, int k, const float *top_logits, float *w)
 }
 
 /*
+ * Step 2 variant, the Softmax -> Top-k order of the CANN MoE article's
+ * section 2.1: the softmax runs over all E logits of the token and the k
+ * selected experts keep their probabilities,
+ *   p_e = exp(l_e - max_i l_i) / sum_i exp(l_i - max_i l_i),   w[t][j] = p_{ids[t][j]},
+ * (mode 1), or those k probabilities divided by their sum (mode 2).  In
+ * double, stored as fp32.  Selection is unchanged (softmax is monotonic).
+ */
+int oracle_gate_softmax_all(int T, int E, int k, const float *logits, const int32_t *ids,
+                            int mode, float *w)
+{
+    if (T < 0 || E < 1 || k < 1 || k > E || !logits || !ids || !w) return 1;
+    if (mode != 1 && mode != 2) return 1;
+    for (int t = 0; t < T; t++) {
+        const float *l = logits + (size_t)t * E;
+        double m = (double)l[0];
+        for (int e = 1; e < E; e++)
+            if ((double)l[e] > m) m = (double)l[e];
+        double z = 0.0;
+        for (int e = 0; e < E; e++) z += exp((double)l[e] - m);
+        double sel = 0.0;
+        for (int j = 0; j < k; j++) sel += exp((double)l[ids[(size_t)t * k + j]] - m) / z;
+        for (int j = 0; j < k; j++) {
+            double p = exp((double)l[ids[(size_t)t * k + j]] - m) / z;
+            w[(size_t)t * k + j] = (float)(mode == 1 ? p : p / sel);
+        }
+    }
+    return 0;
+}
+
+/*
  * Expert capacity from the capacity factor (article section 4.3,
  * capacity_factor = 1.2; the blocked dispatch buffer of the compute flow is
  * [num_experts, expert_capacity]).  Reading: C = ceil(cf*T*k/E - 1e-9); the

@@ -188,6 +188,24 @@ def test_bias_shift_leaves_routing_unchanged():
     np.testing.assert_allclose(w0, w1, atol=1e-6)
 
 
+def test_softmax_over_all_experts_variant():
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(3)
+    lg = rng.normal(size=(60, 12)).astype(np.float32)
+    for k in (1, 3, 12):
+        ids, vals = oracle.topk(lg, k)
+        w1 = oracle.gate_softmax_all(lg, ids, 1)
+        p = special.softmax(lg.astype(np.float64), axis=1)  # library softmax over all E
+        np.testing.assert_allclose(w1, np.take_along_axis(p, ids.astype(np.int64), 1), rtol=1e-6)
+        assert np.all(w1.astype(np.float64).sum(1) <= 1 + 1e-6)
+        w2 = oracle.gate_softmax_all(lg, ids, 2)
+        np.testing.assert_allclose(w2, oracle.gate_softmax(vals), rtol=0, atol=2e-7)
+        if k == 12:  # selecting every expert: no renormalisation needed
+            np.testing.assert_allclose(w1, oracle.gate_softmax(vals), rtol=0, atol=2e-7)
+    with pytest.raises(RuntimeError):
+        oracle.gate_softmax_all(lg, ids, 0)
+
+
 # -------------------------------------------------------------- capacity ----
 
 def test_capacity_values():
