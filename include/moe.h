@@ -21,6 +21,8 @@
  *     Column j of ids/weights is the j-th best expert.
  *   - Router logits and the gate softmax are fp32 (bf16 inputs, fp32
  *     accumulation); an optional fp32 bias b[E] is added to the logits.
+ *     The gate weights follow moe_shape.gating (default: softmax over the
+ *     k selected logits).
  *   - GELU is the exact form 0.5 z (1 + erf(z / sqrt 2)).
  *   - capacity C = ceil(capacity_factor * T * k / E - 1e-9) when
  *     capacity_factor > 0, else unlimited.  The first C assignments of each
@@ -86,6 +88,20 @@ extern "C" {
  * moe_selftest_wait_timeout. */
 #define MOE_WS_MIN_BYTES 256
 
+/* Gate weights (moe_shape.gating).
+ * MOE_GATE_TOPK_SOFTMAX (0, default): softmax over the k selected logits
+ *   (the router kernel of "用Ascend C写一个MoE融合算子", section "1. Routing +
+ *   Gating 合并": Softmax over the top-k scores only).
+ * MOE_GATE_SOFTMAX_TOPK (1): softmax over all E logits, then the k selected
+ *   probabilities as they are (the Softmax -> Top-k order of the article's
+ *   section 2.1); a token's weights sum to less than 1 unless k = E.
+ * MOE_GATE_SOFTMAX_TOPK_RENORM (2): as 1, then the k probabilities divided
+ *   by their sum (mathematically equal to 0; computed in this order).
+ * The selected experts are the same in all three modes. */
+#define MOE_GATE_TOPK_SOFTMAX 0
+#define MOE_GATE_SOFTMAX_TOPK 1
+#define MOE_GATE_SOFTMAX_TOPK_RENORM 2
+
 typedef struct moe_shape {
   int32_t T; /* tokens */
   int32_t H; /* hidden size */
@@ -93,6 +109,7 @@ typedef struct moe_shape {
   int32_t E; /* experts */
   int32_t k; /* experts per token */
   double capacity_factor; /* <= 0 or NaN: no capacity limit */
+  int32_t gating; /* MOE_GATE_*; 0 (zero-initialised) = softmax over the k selected */
 } moe_shape;
 
 /* Library version, (major << 16) | minor. */

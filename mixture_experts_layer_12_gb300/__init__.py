@@ -48,14 +48,21 @@ class MoEError(RuntimeError):
         self.code = code
 
 
+MOE_GATE_TOPK_SOFTMAX = 0
+MOE_GATE_SOFTMAX_TOPK = 1
+MOE_GATE_SOFTMAX_TOPK_RENORM = 2
+
+
 class moe_shape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("F", ctypes.c_int32),
-                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("capacity_factor", ctypes.c_double)]
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("capacity_factor", ctypes.c_double),
+                ("gating", ctypes.c_int32)]
 
 
-def make_shape(T: int, H: int, F: int, E: int, k: int, capacity_factor=None) -> moe_shape:
+def make_shape(T: int, H: int, F: int, E: int, k: int, capacity_factor=None,
+               gating: int = MOE_GATE_TOPK_SOFTMAX) -> moe_shape:
     cf = -1.0 if capacity_factor is None else float(capacity_factor)
-    return moe_shape(int(T), int(H), int(F), int(E), int(k), cf)
+    return moe_shape(int(T), int(H), int(F), int(E), int(k), cf, int(gating))
 
 
 _lock = threading.Lock()
@@ -276,17 +283,20 @@ class MoELayer:
     """Holds a layer's weights (device tensors) and reusable buffers; calling
     it runs moe_forward on the current stream."""
 
-    def __init__(self, w_router, w1, w2, k: int, bias=None, capacity_factor=None):
+    def __init__(self, w_router, w1, w2, k: int, bias=None, capacity_factor=None,
+                 gating: int = MOE_GATE_TOPK_SOFTMAX):
         self.w_router, self.w1, self.w2, self.bias = w_router, w1, w2, bias
         self.E, self.H, self.F = w1.shape[0], w1.shape[1], w1.shape[2]
         self.k = int(k)
         self.capacity_factor = capacity_factor
+        self.gating = int(gating)
         self._T = None
 
     def _ensure(self, T: int, device):
         if self._T == T:
             return
-        self.shape = make_shape(T, self.H, self.F, self.E, self.k, self.capacity_factor)
+        self.shape = make_shape(T, self.H, self.F, self.E, self.k, self.capacity_factor,
+                                self.gating)
         self.ws = alloc_workspace(self.shape, device)
         self.routing = alloc_routing(T, self.E, self.k, device)
         self.y = torch.empty(T, self.H, dtype=torch.bfloat16, device=device)
@@ -305,6 +315,15 @@ def capacity(T: int, E: int, k: int, capacity_factor) -> int:
     return moe_expert_capacity(make_shape(T, 8, 8, E, k, capacity_factor))
 
 
+def load_cv(counts) -> float:
+    """Coefficient of variation (std / mean) of the per-expert kept counts:
+    the load-balance diagnostic of the article's section 4.3 (its auxiliary
+    loss is 0.01 * cv(experts_load)).  Host-side arithmetic on an output."""
+    c = counts.detach().double().cpu()
+    m = c.mean().item()
+    return float(c.std(unbiased=False).item() / m) if m > 0 else 0.0
+
+
 def roofline_flops(N_rows: int, H: int, F: int) -> float:
     """Algorithmic FLOPs of the two expert GEMMs for N_rows kept rows."""
     return 4.0 * N_rows * H * F
@@ -313,4 +332,6 @@ def roofline_flops(N_rows: int, H: int, F: int) -> float:
 __all__ = [n for n in EXPORTS] + ["MoEError", "moe_shape", "make_shape", "load_library",
                                    "alloc_routing", "alloc_workspace", "alloc_route_workspace",
                                    "MoELayer", "RoutingBuffers",
-                                   "capacity", "roofline_flops"]
+                                   "capacity", "roofline_flops", "load_cv",
+                                   "MOE_GATE_TOPK_SOFTMAX", "MOE_GATE_SOFTMAX_TOPK",
+                                   "MOE_GATE_SOFTMAX_TOPK_RENORM"]

@@ -122,6 +122,8 @@ int check_shape(const moe_shape* s, bool need_ffn) {
   if (s->H < 8 || s->H % 8 != 0) return fail(MOE_ERR_UNSUPPORTED, "H = %d: need H >= 8, H %% 8 == 0", s->H);
   if (need_ffn && (s->F < 8 || s->F % 8 != 0))
     return fail(MOE_ERR_UNSUPPORTED, "F = %d: need F >= 8, F %% 8 == 0", s->F);
+  if (s->gating < MOE_GATE_TOPK_SOFTMAX || s->gating > MOE_GATE_SOFTMAX_TOPK_RENORM)
+    return fail(MOE_ERR_INVALID_ARG, "gating = %d: not a MOE_GATE_* value", s->gating);
   if ((int64_t)s->T * s->k > (int64_t)1 << 24)
     return fail(MOE_ERR_UNSUPPORTED, "T * k = %lld exceeds 2^24", (long long)s->T * s->k);
   return MOE_OK;
@@ -220,6 +222,7 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
     ra.splits *= 2;
   }
   ra.capacity = (int)capacity_of(s);
+  ra.gating = s->gating;
   ra.bias = b_router;
   ra.ids = ids;
   ra.weights = weights;

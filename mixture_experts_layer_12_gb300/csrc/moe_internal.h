@@ -29,6 +29,7 @@ struct RouterArgs {
   int tmem_cols;   // power of two >= max(32, npad)
   int splits;      // cluster size along K (1, 2, 4 or 8)
   int capacity;    // -1: unlimited
+  int gating;      // MOE_GATE_*
   const float* bias;  // [E] or null
   int32_t* ids;       // [T, k]
   float* weights;     // [T, k]

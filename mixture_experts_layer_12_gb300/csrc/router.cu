@@ -24,8 +24,10 @@
 //   * TopK: for E <= 64 one thread per token streams the E logits through a
 //     k-entry insertion list; for larger E one warp per token (lane l holds
 //     experts l, l+32, ...) runs k rounds of a shuffle argmax over (value,
-//     index) pairs.  Larger value first, equal values -> lower index.  The
-//     softmax over the k logits uses fp32 expf;
+//     index) pairs.  Larger value first, equal values -> lower index.  Gate
+//     weights (fp32 expf): softmax over the k logits, or (the article's
+//     section 2.1 order) softmax over all E then the k probabilities, with
+//     or without renormalisation;
 //   * per-tile expert counts go to the workspace (summed through DSMEM
 //     atomics into rank 0); the last tile to finish (an atomic ticket, no
 //     waiting) scans them into counts / offsets (with the capacity clip) and
@@ -349,6 +351,18 @@ __global__ void __launch_bounds__(RTHREADS)
         ex[j] = j < a.k ? expf(tk.v[j] - mx) : 0.f;
         z += ex[j];
       }
+      if (a.gating != MOE_GATE_TOPK_SOFTMAX) {
+        // softmax over all E logits first: p_j = exp(l_j - max) / sum_e exp(l_e - max)
+        float zall = 0.f;
+        for (int e = 0; e < a.E; ++e) zall += expf(logit(li, e) - mx);
+        float zsel = 0.f;
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+          ex[j] = ex[j] / zall;
+          zsel += ex[j];
+        }
+        z = a.gating == MOE_GATE_SOFTMAX_TOPK ? 1.f : zsel;
+      }
 #pragma unroll
       for (int j = 0; j < kMaxTopK; ++j) {
         if (j < a.k) {
@@ -407,6 +421,20 @@ __global__ void __launch_bounds__(RTHREADS)
       float z = ex;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+      if (a.gating != MOE_GATE_TOPK_SOFTMAX) {
+        // softmax over all E logits first (lane sums its experts, warp reduces)
+        float zall = 0.f;
+#pragma unroll
+        for (int u = 0; u < NU; ++u)
+          if (lane + 32 * u < a.E) zall += expf(v[u] - mx);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) zall += __shfl_xor_sync(0xffffffffu, zall, off);
+        ex = ex / zall;
+        float zsel = ex;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) zsel += __shfl_xor_sync(0xffffffffu, zsel, off);
+        z = a.gating == MOE_GATE_SOFTMAX_TOPK ? 1.f : zsel;
+      }
       if (lane < a.k) {
         a.ids[(size_t)t * a.k + lane] = my_id;
         a.weights[(size_t)t * a.k + lane] = ex / z;

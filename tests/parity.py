@@ -50,7 +50,7 @@ def _softmax_at(logits: np.ndarray, ids: np.ndarray) -> np.ndarray:
 
 
 def check_routing(logits: np.ndarray, ora_ids: np.ndarray, ora_w: np.ndarray,
-                  gpu_ids: np.ndarray, gpu_w: np.ndarray) -> dict:
+                  gpu_ids: np.ndarray, gpu_w: np.ndarray, gating: int = 0) -> dict:
     """Returns a report; raises AssertionError on a parity failure."""
     T, k = ora_ids.shape
     E = logits.shape[1]
@@ -70,7 +70,8 @@ def check_routing(logits: np.ndarray, ora_ids: np.ndarray, ora_w: np.ndarray,
     werr_far = float(np.max(np.abs(gpu_w[far] - ora_w[far]))) if far.any() else 0.0
     assert werr_far <= W_TOL, f"gate weight error {werr_far} > {W_TOL}"
     if near.any():
-        ref_near = _softmax_at(logits[near], gpu_ids[near])
+        ref_near = (_softmax_at(logits[near], gpu_ids[near]) if gating == 0 else
+                    oracle.gate_softmax_all(logits[near], gpu_ids[near], gating))
         werr_near = float(np.max(np.abs(gpu_w[near] - ref_near)))
         assert werr_near <= W_TOL, f"near-tie gate weight error {werr_near}"
     return dict(near_tie_tokens=int(near.sum()), ids_exact_tokens=int(far.sum()), w_max_err=werr_far)
@@ -105,8 +106,9 @@ def check_y(y_gpu: np.ndarray, y_ref: np.ndarray) -> dict:
 
 
 def reference_y(inputs: dict, logits: np.ndarray, gpu_ids: np.ndarray, gpu_slot: np.ndarray,
-                rows, nthreads: int = 0) -> np.ndarray:
+                rows, nthreads: int = 0, gating: int = 0) -> np.ndarray:
     """Oracle combine on the GPU's routing decisions with oracle gate weights."""
-    w_ref = oracle.gate_softmax(np.take_along_axis(logits, gpu_ids.astype(np.int64), axis=1))
+    w_ref = oracle.gate_weights(logits, gpu_ids,
+                                np.take_along_axis(logits, gpu_ids.astype(np.int64), axis=1), gating)
     return oracle.combine_rows(inputs["x"], inputs["w1"], inputs["w2"], gpu_ids, w_ref, gpu_slot,
                                rows, nthreads)

@@ -70,6 +70,7 @@ def test_capacity_matches_oracle(lib, T, k, E, cf):
     (dict(k=9), moe.MOE_ERR_UNSUPPORTED), (dict(k=0), moe.MOE_ERR_UNSUPPORTED),
     (dict(H=100), moe.MOE_ERR_UNSUPPORTED), (dict(F=12), moe.MOE_ERR_UNSUPPORTED),
     (dict(T=-1), moe.MOE_ERR_INVALID_ARG), (dict(T=1 << 22, k=8), moe.MOE_ERR_UNSUPPORTED),
+    (dict(gating=3), moe.MOE_ERR_INVALID_ARG), (dict(gating=-1), moe.MOE_ERR_INVALID_ARG),
 ])
 def test_bad_shapes_rejected_before_launch(lib, kw, code):
     base = dict(T=64, H=128, F=256, E=8, k=2)

@@ -31,8 +31,8 @@ def to_dev(inputs):
     return {k: (None if v is None else v.to(DEV)) for k, v in inputs.items()}
 
 
-def gpu_route(cfg, dev_in):
-    s = moe.make_shape(cfg.T, cfg.H, max(cfg.F, 8), cfg.E, cfg.k, cfg.capacity_factor)
+def gpu_route(cfg, dev_in, gating=0):
+    s = moe.make_shape(cfg.T, cfg.H, max(cfg.F, 8), cfg.E, cfg.k, cfg.capacity_factor, gating)
     r = moe.alloc_routing(cfg.T, cfg.E, cfg.k, DEV)
     ws = moe.alloc_route_workspace(s, DEV)
     moe.moe_route(s, dev_in["x"], dev_in["w_router"], dev_in["bias"], r.ids, r.weights, r.counts,
@@ -41,9 +41,9 @@ def gpu_route(cfg, dev_in):
     return r
 
 
-def gpu_forward(cfg, dev_in):
+def gpu_forward(cfg, dev_in, gating=0):
     layer = moe.MoELayer(dev_in["w_router"], dev_in["w1"], dev_in["w2"], cfg.k, bias=dev_in["bias"],
-                         capacity_factor=cfg.capacity_factor)
+                         capacity_factor=cfg.capacity_factor, gating=gating)
     y = layer(dev_in["x"])
     assert moe.moe_get_device_status(layer.ws) == 0
     return layer, y
@@ -53,24 +53,25 @@ def np_(t):
     return t.detach().cpu().numpy()
 
 
-def routing_parity(cfg, inputs, r, nthreads=0):
+def routing_parity(cfg, inputs, r, nthreads=0, gating=0):
     logits = oracle.router_logits(inputs["x"], inputs["w_router"], inputs["bias"], nthreads)
     o_ids, o_vals = oracle.topk(logits, cfg.k)
-    o_w = oracle.gate_softmax(o_vals)
+    o_w = oracle.gate_weights(logits, o_ids, o_vals, gating)
     gids = np_(r.ids)
-    rep = check_routing(logits, o_ids, o_w, gids, np_(r.weights))
+    rep = check_routing(logits, o_ids, o_w, gids, np_(r.weights), gating)
     rep.update(check_dispatch(gids, cfg.E, cfg.capacity_factor, np_(r.counts), np_(r.offsets),
                               np_(r.perm), np_(r.slot)))
     return logits, rep
 
 
-def forward_parity(cfg, stride=1, nthreads=0):
+def forward_parity(cfg, stride=1, nthreads=0, gating=0):
     inputs = moe_synth.make_inputs(cfg)
     dev_in = to_dev(inputs)
-    layer, y = gpu_forward(cfg, dev_in)
-    logits, rep = routing_parity(cfg, inputs, layer.routing, nthreads)
+    layer, y = gpu_forward(cfg, dev_in, gating)
+    logits, rep = routing_parity(cfg, inputs, layer.routing, nthreads, gating)
     rows = np.arange(0, cfg.T, stride, dtype=np.int32)
-    y_ref = reference_y(inputs, logits, np_(layer.routing.ids), np_(layer.routing.slot), rows, nthreads)
+    y_ref = reference_y(inputs, logits, np_(layer.routing.ids), np_(layer.routing.slot), rows, nthreads,
+                        gating)
     y_gpu = y.float().cpu().numpy()[rows]
     rep.update(check_y(y_gpu, y_ref))
     print(cfg.name, rep)
@@ -306,3 +307,37 @@ def test_profiled_forward_eager_and_captured():
     torch.cuda.synchronize()
     assert all(evs[i].elapsed_time(evs[i + 1]) >= 0 for i in range(5))
     assert torch.equal(layer.y, y_ref)
+
+
+# ------------------------------------------------------- gating variants --
+
+@pytest.mark.parametrize("gating", [moe.MOE_GATE_SOFTMAX_TOPK, moe.MOE_GATE_SOFTMAX_TOPK_RENORM])
+@pytest.mark.parametrize("E,k", [(8, 2), (64, 4), (128, 8), (16, 16)])
+def test_router_softmax_over_all_experts(gating, E, k):
+    if k > 8:
+        k = 8
+    cfg = moe_synth.MoEConfig("gate", T=300, H=256, F=0, E=E, k=k, seed=40 + E, bias0=0.5)
+    inputs = moe_synth.make_inputs(cfg, with_ffn=False)
+    r = gpu_route(cfg, to_dev(inputs), gating)
+    routing_parity(cfg, inputs, r, gating=gating)
+    w = np_(r.weights).astype(np.float64).sum(1)
+    if gating == moe.MOE_GATE_SOFTMAX_TOPK:
+        assert np.all(w <= 1 + 1e-5) and (k == E or np.all(w < 1))
+    else:
+        np.testing.assert_allclose(w, 1.0, atol=1e-5)
+
+
+@pytest.mark.parametrize("gating", [moe.MOE_GATE_SOFTMAX_TOPK, moe.MOE_GATE_SOFTMAX_TOPK_RENORM])
+def test_forward_softmax_over_all_experts(gating):
+    cfg = moe_synth.MoEConfig("gatefwd", T=200, H=256, F=384, E=16, k=4, seed=44,
+                              capacity_factor=1.1)
+    forward_parity(cfg, gating=gating)
+
+
+def test_load_cv_diagnostic():
+    cfg = moe_synth.SKEWED
+    inputs = moe_synth.make_inputs(cfg, with_ffn=False)
+    r = gpu_route(cfg, to_dev(inputs))
+    counts = np_(r.counts).astype(np.float64)
+    assert moe.load_cv(r.counts) == pytest.approx(counts.std() / counts.mean(), rel=1e-9)
+    assert moe.load_cv(r.counts) > 1.0  # expert 0 takes ~99% of the tokens
