@@ -22,6 +22,8 @@ Parity status of each function (what pins it, in ``tests/test_oracle.py``):
   expert_ffn     identity experts (GELU(z)-GELU(-z)=z); numpy fp64 FFN with
                  math.erf; GELU fixed points.
   combine_rows   dense masked formulation; identical experts; permutation.
+  expert_swiglu  numpy fp64 gated FFN with np.exp; SiLU fixed points; a zero
+                 gate or zero up projection gives 0; swapped halves differ.
 """
 from __future__ import annotations
 
@@ -69,10 +71,13 @@ def _load():
         lib.oracle_dispatch.argtypes = [I, I, I, ctypes.c_long, P, P, P, P, P]
         lib.oracle_expert_ffn.argtypes = [I, I, P, P, P, P]
         lib.oracle_combine_rows.argtypes = [I, I, I, I, I, P, P, P, P, P, P, I, P, P, I]
+        lib.oracle_combine_rows_act.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, I, P, P, I]
+        lib.oracle_expert_swiglu.argtypes = [I, I, P, P, P, P]
         lib.oracle_max_threads.argtypes = []
         for name in ("oracle_router_logits", "oracle_topk", "oracle_gate_softmax",
                      "oracle_gate_softmax_all",
                      "oracle_dispatch", "oracle_expert_ffn", "oracle_combine_rows",
+                     "oracle_combine_rows_act", "oracle_expert_swiglu",
                      "oracle_max_threads"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -182,11 +187,26 @@ def expert_ffn(xrow, w1e, w2e) -> np.ndarray:
     return out
 
 
-def combine_rows(x, w1, w2, ids, w, slot, rows=None, nthreads: int = 0) -> np.ndarray:
-    """y[rows] in fp64: sum over kept slots j of w[t,j] * FFN_{ids[t,j]}(x[t])."""
+def expert_swiglu(xrow, w1e, w2e) -> np.ndarray:
+    """(SiLU(x W_gate) * (x W_up)) W_down in fp64; W1e = [gate | up] [H, 2F], W2e [F, H]."""
+    xb, w1b, w2b = _bits(xrow).reshape(-1), _bits(w1e), _bits(w2e)
+    H = xb.shape[0]
+    F = w1b.shape[1] // 2
+    assert w1b.shape == (H, 2 * F) and w2b.shape == (F, H)
+    out = np.empty(H, dtype=np.float64)
+    _check(_load().oracle_expert_swiglu(H, F, _ptr(xb), _ptr(w1b), _ptr(w2b), _ptr(out)),
+           "expert_swiglu")
+    return out
+
+
+def combine_rows(x, w1, w2, ids, w, slot, rows=None, nthreads: int = 0, act: str = "gelu") -> np.ndarray:
+    """y[rows] in fp64: sum over kept slots j of w[t,j] * FFN_{ids[t,j]}(x[t]).
+    act "gelu": W1 [E,H,F]; "swiglu": W1 [E,H,2F] = [gate | up]; W2 [E,F,H]."""
     xb, w1b, w2b = _bits(x), _bits(w1), _bits(w2)
     T, H = xb.shape
     E, H2, F = w1b.shape
+    if act == "swiglu":
+        F //= 2
     assert H2 == H and w2b.shape == (E, F, H)
     idz = np.ascontiguousarray(ids, dtype=np.int32)
     k = idz.shape[1]
@@ -194,8 +214,9 @@ def combine_rows(x, w1, w2, ids, w, slot, rows=None, nthreads: int = 0) -> np.nd
     sz = np.ascontiguousarray(slot, dtype=np.int32)
     r = np.arange(T, dtype=np.int32) if rows is None else np.ascontiguousarray(rows, dtype=np.int32)
     y = np.empty((r.shape[0], H), dtype=np.float64)
-    _check(_load().oracle_combine_rows(T, H, F, E, k, _ptr(xb), _ptr(w1b), _ptr(w2b), _ptr(idz),
-                                       _ptr(wz), _ptr(sz), int(r.shape[0]), _ptr(r), _ptr(y), nthreads),
+    _check(_load().oracle_combine_rows_act(T, H, F, E, k, 1 if act == "swiglu" else 0, _ptr(xb),
+                                           _ptr(w1b), _ptr(w2b), _ptr(idz), _ptr(wz), _ptr(sz),
+                                           int(r.shape[0]), _ptr(r), _ptr(y), nthreads),
            "combine_rows")
     return y
 
@@ -208,13 +229,13 @@ def route(x, w_router, k: int, bias=None, nthreads: int = 0, gating: int = 0):
 
 
 def moe_forward(x, w_router, w1, w2, k: int, bias=None, capacity_factor=None,
-                rows=None, nthreads: int = 0, gating: int = 0) -> dict:
+                rows=None, nthreads: int = 0, gating: int = 0, act: str = "gelu") -> dict:
     """The whole layer: routing and dispatch for all tokens, FFN and combine
     for ``rows`` (all tokens when None; tokens are independent once routed)."""
     logits, ids, vals, w = route(x, w_router, k, bias, nthreads, gating)
     E = logits.shape[1]
     counts, offsets, perm, slot = dispatch(ids, E, capacity_factor)
-    y = combine_rows(x, w1, w2, ids, w, slot, rows, nthreads)
+    y = combine_rows(x, w1, w2, ids, w, slot, rows, nthreads, act)
     return dict(logits=logits, ids=ids, top_logits=vals, w=w, counts=counts,
                 offsets=offsets, perm=perm, slot=slot, y=y,
                 rows=np.arange(logits.shape[0]) if rows is None else np.asarray(rows))

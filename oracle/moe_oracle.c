@@ -30,7 +30,8 @@
  * softmax and the combine stay in double.  No blocking, fusion or reordering.
  *
  * Layouts (row-major, contiguous):
- *   x[T][H], w_router[H][E], bias[E] (optional), W1[E][H][F], W2[E][F][H],
+ *   x[T][H], w_router[H][E], bias[E] (optional), W1[E][H][F] (SwiGLU:
+ *   [E][H][2F] = [gate | up]), W2[E][F][H],
  *   logits[T][E], ids[T][k], top_logits[T][k], w[T][k], counts[E],
  *   offsets[E+1], perm[T*k] (entries t*k+j), slot[T][k] (-1 = dropped).
  */
@@ -282,6 +283,48 @@ static void expert_ffn_row(int H, int F, const uint16_t *xrow,
     }
 }
 
+/*
+ * Step 4 with a gated expert (the SwiGLU FFN of the Llama 3 / Mixtral /
+ * DeepSeek models the compute-flow page names): with W1 = [W_gate | W_up]
+ * of shape [H][2F] and W2 = W_down [F][H],
+ *   g = x W_gate,  u = x W_up,  a_f = SiLU(g_f) u_f = g_f / (1 + exp(-g_f)) u_f,
+ *   out = a W_down,
+ * all in double, dot products accumulated in ascending index order.
+ */
+static void expert_swiglu_row(int H, int F, const uint16_t *xrow,
+                              const uint16_t *w1e, const uint16_t *w2e,
+                              double *g, double *out)
+{
+    /* g[0..F) = gate, g[F..2F) = up, both accumulated over h ascending */
+    for (int f = 0; f < 2 * F; f++) g[f] = 0.0;
+    for (int h = 0; h < H; h++) {
+        double xv = bf16_value(xrow[h]);
+        const uint16_t *w1row = w1e + (size_t)h * 2 * F;
+        for (int f = 0; f < 2 * F; f++) g[f] += xv * bf16_value(w1row[f]);
+    }
+    for (int f = 0; f < F; f++) {
+        double gate = g[f];
+        g[f] = gate / (1.0 + exp(-gate)) * g[F + f];
+    }
+    for (int h = 0; h < H; h++) out[h] = 0.0;
+    for (int f = 0; f < F; f++) {
+        double av = g[f];
+        const uint16_t *w2row = w2e + (size_t)f * H;
+        for (int h = 0; h < H; h++) out[h] += av * bf16_value(w2row[h]);
+    }
+}
+
+int oracle_expert_swiglu(int H, int F, const uint16_t *xrow, const uint16_t *w1e,
+                         const uint16_t *w2e, double *out)
+{
+    if (H < 1 || F < 1 || !xrow || !w1e || !w2e || !out) return 1;
+    double *g = (double *)malloc(sizeof(double) * 2 * (size_t)F);
+    if (!g) return 2;
+    expert_swiglu_row(H, F, xrow, w1e, w2e, g, out);
+    free(g);
+    return 0;
+}
+
 /* Exported single-row expert FFN (for the oracle's own pins). */
 int oracle_expert_ffn(int H, int F, const uint16_t *xrow, const uint16_t *w1e,
                       const uint16_t *w2e, double *out)
@@ -302,11 +345,31 @@ int oracle_expert_ffn(int H, int F, const uint16_t *xrow, const uint16_t *w1e,
  * w[t][j] * Expert_{ids[t][j]}(x[t]).  A token with no kept slot gets 0.
  * Computed for the n_rows tokens listed in rows[]; y is [n_rows][H].
  */
+int oracle_combine_rows_act(int T, int H, int F, int E, int k, int act, const uint16_t *x,
+                            const uint16_t *w1, const uint16_t *w2,
+                            const int32_t *ids, const float *w, const int32_t *slot,
+                            int n_rows, const int32_t *rows, double *y, int nthreads);
+
 int oracle_combine_rows(int T, int H, int F, int E, int k, const uint16_t *x,
                         const uint16_t *w1, const uint16_t *w2,
                         const int32_t *ids, const float *w, const int32_t *slot,
                         int n_rows, const int32_t *rows, double *y, int nthreads)
 {
+    return oracle_combine_rows_act(T, H, F, E, k, 0, x, w1, w2, ids, w, slot, n_rows, rows, y,
+                                   nthreads);
+}
+
+/*
+ * As oracle_combine_rows with the expert chosen by `act`: 0 = GELU FFN
+ * (W1 [E][H][F]), 1 = SwiGLU (W1 [E][H][2F] = [gate | up]); W2 [E][F][H].
+ */
+int oracle_combine_rows_act(int T, int H, int F, int E, int k, int act, const uint16_t *x,
+                            const uint16_t *w1, const uint16_t *w2,
+                            const int32_t *ids, const float *w, const int32_t *slot,
+                            int n_rows, const int32_t *rows, double *y, int nthreads)
+{
+    if (act != 0 && act != 1) return 1;
+    const size_t w1_cols = (size_t)(act == 1 ? 2 : 1) * (size_t)F;
     if (T < 0 || H < 1 || F < 1 || E < 1 || k < 1 || n_rows < 0) return 1;
     if (!x || !w1 || !w2 || !ids || !w || !slot || (n_rows && (!rows || !y))) return 1;
     for (int i = 0; i < n_rows; i++)
@@ -315,7 +378,7 @@ int oracle_combine_rows(int T, int H, int F, int E, int k, const uint16_t *x,
     set_threads(nthreads);
 #pragma omp parallel
     {
-        double *g = (double *)malloc(sizeof(double) * (size_t)F);
+        double *g = (double *)malloc(sizeof(double) * w1_cols);
         double *v = (double *)malloc(sizeof(double) * (size_t)H);
         if (!g || !v) {
 #pragma omp atomic write
@@ -331,8 +394,12 @@ int oracle_combine_rows(int T, int H, int F, int E, int k, const uint16_t *x,
                 if (slot[(size_t)t * k + j] < 0) continue; /* dropped */
                 int e = ids[(size_t)t * k + j];
                 if (e < 0 || e >= E) continue;
-                expert_ffn_row(H, F, x + (size_t)t * H,
-                               w1 + (size_t)e * H * F, w2 + (size_t)e * F * H, g, v);
+                if (act == 1)
+                    expert_swiglu_row(H, F, x + (size_t)t * H, w1 + (size_t)e * H * w1_cols,
+                                      w2 + (size_t)e * F * H, g, v);
+                else
+                    expert_ffn_row(H, F, x + (size_t)t * H,
+                                   w1 + (size_t)e * H * F, w2 + (size_t)e * F * H, g, v);
                 double wt = (double)w[(size_t)t * k + j];
                 for (int h = 0; h < H; h++) yt[h] += wt * v[h];
             }

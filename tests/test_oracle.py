@@ -323,6 +323,54 @@ def test_expert_ffn_against_numpy(H, F):
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
 
 
+def _silu_np(z):
+    return z / (1.0 + np.exp(-z))
+
+
+@pytest.mark.parametrize("H,F", [(8, 24), (40, 12)])
+def test_expert_swiglu_against_numpy(H, F):
+    x = rand_bf16((H,), 1.0, 13)
+    w1 = rand_bf16((H, 2 * F), 1.0 / math.sqrt(H), 14)  # [gate | up]
+    w2 = rand_bf16((F, H), 1.0 / math.sqrt(F), 15)
+    got = oracle.expert_swiglu(x, w1, w2)
+    X, W1, W2 = f64(x), f64(w1), f64(w2)
+    ref = (_silu_np(X @ W1[:, :F]) * (X @ W1[:, F:])) @ W2
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+    # the halves are not interchangeable: swapping gate and up changes y
+    swapped = torch.cat([w1[:, F:], w1[:, :F]], dim=1)
+    assert not np.allclose(oracle.expert_swiglu(x, swapped, w2), got)
+    # a zero gate (SiLU(0) = 0) or a zero up projection silences the expert
+    for half in (slice(0, F), slice(F, 2 * F)):
+        z = w1.clone()
+        z[:, half] = 0
+        assert np.all(oracle.expert_swiglu(x, z, w2) == 0.0)
+
+
+def test_swiglu_fixed_points():
+    # 1x1: y = SiLU(g) * u with g = x * wg, u = x * wu; SiLU(1) = 1/(1+e^-1)
+    x = bf16([1.0])
+    y = oracle.expert_swiglu(x, bf16([[1.0, 2.0]]), bf16([[1.0]]))
+    assert abs(y[0] - 2.0 / (1.0 + math.exp(-1.0))) < 1e-15
+    y = oracle.expert_swiglu(bf16([-2.0]), bf16([[1.0, 1.0]]), bf16([[1.0]]))
+    assert abs(y[0] - (-2.0 / (1.0 + math.exp(2.0))) * -2.0) < 1e-15
+
+
+def test_swiglu_combine_dense_masked():
+    cfg = moe_synth.MoEConfig("t", T=20, H=16, F=24, E=4, k=2, seed=9)
+    inp = moe_synth.make_inputs(cfg)
+    g = torch.Generator().manual_seed(5)
+    w1 = (torch.randn(cfg.E, cfg.H, 2 * cfg.F, generator=g) / math.sqrt(cfg.H)).to(torch.bfloat16)
+    out = oracle.moe_forward(inp["x"], inp["w_router"], w1, inp["w2"], cfg.k, act="swiglu")
+    X = f64(inp["x"])
+    ref = np.zeros_like(X)
+    for t in range(cfg.T):
+        for j in range(cfg.k):
+            e = out["ids"][t, j]
+            W1, W2 = f64(w1[e]), f64(inp["w2"][e])
+            ref[t] += out["w"][t, j] * ((_silu_np(X[t] @ W1[:, :cfg.F]) * (X[t] @ W1[:, cfg.F:])) @ W2)
+    np.testing.assert_allclose(out["y"], ref, rtol=1e-10, atol=1e-12)
+
+
 # --------------------------------------------------------------- combine ----
 
 def _dense_masked(x, w1, w2, ids, w, slot, E):
