@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE layer tokens/sec at 1 GB300 + % of bf16 tensor/HBM roofline"
 UNIT = "tokens/s"
 WORKLOADS = ("prefill", "decode", "skewed", "skewed_cf1.2", "tiny", "router_k1", "router_k2",
-             "router_k4", "router_k8")
+             "router_k4", "router_k8", "prefill_swiglu", "decode_swiglu")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from
@@ -80,7 +80,8 @@ def workload_cfg(name):
 def workload_desc(cfg):
     cf = "none" if cfg.capacity_factor is None else cfg.capacity_factor
     return (f"{cfg.name}: T={cfg.T} H={cfg.H} F={cfg.F} E={cfg.E} k={cfg.k} capacity_factor={cf}"
-            + (f" bias0={cfg.bias0}" if cfg.bias0 is not None else ""))
+            + (f" bias0={cfg.bias0}" if cfg.bias0 is not None else "")
+            + (" experts=SwiGLU" if cfg.act == "swiglu" else ""))
 
 
 def src_sha(name):
@@ -190,11 +191,12 @@ def whole_job_throughput(tokens_per_rank: int, world: int, steps: int, max_elaps
 def kernel_work(cfg, n_rows, experts_hit):
     """Algorithmic FLOPs and bytes of one launch of each kernel."""
     T, H, F, E, k = cfg.T, cfg.H, cfg.F, cfg.E, cfg.k
+    F1 = 2 * F if getattr(cfg, "act", "gelu") == "swiglu" else F  # W1 columns (gate | up)
     return {
         "router": dict(flops=2.0 * T * H * E, bytes=2.0 * T * H + 2.0 * H * E + 8.0 * T * k),
         "dispatch": dict(flops=0.0, bytes=4.0 * T * k * 3 + 8.0 * E),
-        "expert_gemm1": dict(flops=2.0 * n_rows * H * F,
-                             bytes=2.0 * experts_hit * H * F + 2.0 * n_rows * H + 2.0 * n_rows * F),
+        "expert_gemm1": dict(flops=2.0 * n_rows * H * F1,
+                             bytes=2.0 * experts_hit * H * F1 + 2.0 * n_rows * H + 2.0 * n_rows * F),
         "expert_gemm2": dict(flops=2.0 * n_rows * F * H,
                              bytes=2.0 * experts_hit * F * H + 2.0 * n_rows * F + 2.0 * n_rows * H),
         "combine": dict(flops=2.0 * n_rows * H, bytes=2.0 * n_rows * H + 2.0 * T * H + 8.0 * T * k),
@@ -211,7 +213,7 @@ def oracle_sample_run(inputs, cfg, rows):
     xs = inputs["x"][rows]
     t0 = time.perf_counter()
     oracle.moe_forward(xs, inputs["w_router"], inputs["w1"], inputs["w2"], cfg.k,
-                       bias=inputs["bias"], capacity_factor=cfg.capacity_factor)
+                       bias=inputs["bias"], capacity_factor=cfg.capacity_factor, act=cfg.act)
     return time.perf_counter() - t0
 
 
@@ -364,7 +366,7 @@ def run_ours(args):
     inputs = rank_inputs(cfg, rank, world)
     dev = {k: (None if v is None else v.to(device)) for k, v in inputs.items()}
     layer = moe.MoELayer(dev["w_router"], dev["w1"], dev["w2"], cfg.k, bias=dev["bias"],
-                         capacity_factor=cfg.capacity_factor)
+                         capacity_factor=cfg.capacity_factor, act=cfg.act)
     x = dev["x"]
     stream = torch.cuda.current_stream(device)
 
@@ -514,7 +516,7 @@ def run_ours(args):
                    "kept_rows": n_rows, "experts_hit": experts_hit,
                    "timing": f"CUDA events around {reps} replays of a CUDA graph of {R} forward steps",
                    "l2": "inputs larger than L2: every step streams all expert weights "
-                         f"({2 * 2 * cfg.E * cfg.H * cfg.F / 1e9:.2f} GB)"},
+                         f"({2 * (3 if cfg.act == 'swiglu' else 2) * cfg.E * cfg.H * cfg.F / 1e9:.2f} GB)"},
         "gpu_launches": len(names) * K,
         "roofline": roof,
         "kernels": kernels,

@@ -102,6 +102,16 @@ extern "C" {
 #define MOE_GATE_SOFTMAX_TOPK 1
 #define MOE_GATE_SOFTMAX_TOPK_RENORM 2
 
+/* Expert FFN (moe_shape.expert_act).
+ * MOE_EXPERT_GELU (0, default): y_e = GELU(x W1[e]) W2[e], W1 [E, H, F]
+ *   (listing "Expert计算" of "用Ascend C写一个MoE融合算子").
+ * MOE_EXPERT_SWIGLU (1): y_e = (SiLU(x W_gate[e]) * (x W_up[e])) W2[e], with
+ *   W1 [E, H, 2F] = [W_gate | W_up] along the last dimension (the gated
+ *   experts of the Llama 3 / Mixtral / DeepSeek models the page names);
+ *   SiLU(z) = z / (1 + exp(-z)).  W2 is [E, F, H] in both. */
+#define MOE_EXPERT_GELU 0
+#define MOE_EXPERT_SWIGLU 1
+
 typedef struct moe_shape {
   int32_t T; /* tokens */
   int32_t H; /* hidden size */
@@ -110,6 +120,7 @@ typedef struct moe_shape {
   int32_t k; /* experts per token */
   double capacity_factor; /* <= 0 or NaN: no capacity limit */
   int32_t gating; /* MOE_GATE_*; 0 (zero-initialised) = softmax over the k selected */
+  int32_t expert_act; /* MOE_EXPERT_*; 0 (zero-initialised) = GELU FFN */
 } moe_shape;
 
 /* Library version, (major << 16) | minor. */
@@ -167,8 +178,9 @@ MOE_API int moe_dispatch(const moe_shape* s, const int32_t* ids, int32_t* counts
  * ScatterWithWeights, written as a gather): for every kept assignment,
  * h = GELU(x[t] × W1[e]) and y_e = h × W2[e]; then
  * y[t] = Σ_{j: slot[t,j] >= 0} weights[t,j] × y_e(t,j).
- *   x [T, H] bf16, W1 [E, H, F] bf16 (F contiguous), W2 [E, F, H] bf16
- *   (H contiguous); weights, offsets, perm, slot as produced by moe_route.
+ *   x [T, H] bf16, W1 [E, H, F] bf16 (F contiguous; [E, H, 2F] for
+ *   MOE_EXPERT_SWIGLU), W2 [E, F, H] bf16 (H contiguous); weights, offsets,
+ *   perm, slot as produced by moe_route.
  *   y [T, H] bf16 (output).
  * perm/offsets must describe a valid dispatch (0 <= perm < T*k, offsets
  * non-decreasing, offsets[E] <= T*k); the library does not re-validate them.

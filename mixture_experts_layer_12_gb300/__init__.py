@@ -53,16 +53,21 @@ MOE_GATE_SOFTMAX_TOPK = 1
 MOE_GATE_SOFTMAX_TOPK_RENORM = 2
 
 
+MOE_EXPERT_GELU = 0
+MOE_EXPERT_SWIGLU = 1
+_ACTS = {"gelu": MOE_EXPERT_GELU, "swiglu": MOE_EXPERT_SWIGLU}
+
+
 class moe_shape(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("H", ctypes.c_int32), ("F", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("capacity_factor", ctypes.c_double),
-                ("gating", ctypes.c_int32)]
+                ("gating", ctypes.c_int32), ("expert_act", ctypes.c_int32)]
 
 
 def make_shape(T: int, H: int, F: int, E: int, k: int, capacity_factor=None,
-               gating: int = MOE_GATE_TOPK_SOFTMAX) -> moe_shape:
+               gating: int = MOE_GATE_TOPK_SOFTMAX, act: str = "gelu") -> moe_shape:
     cf = -1.0 if capacity_factor is None else float(capacity_factor)
-    return moe_shape(int(T), int(H), int(F), int(E), int(k), cf, int(gating))
+    return moe_shape(int(T), int(H), int(F), int(E), int(k), cf, int(gating), _ACTS[act])
 
 
 _lock = threading.Lock()
@@ -284,9 +289,11 @@ class MoELayer:
     it runs moe_forward on the current stream."""
 
     def __init__(self, w_router, w1, w2, k: int, bias=None, capacity_factor=None,
-                 gating: int = MOE_GATE_TOPK_SOFTMAX):
+                 gating: int = MOE_GATE_TOPK_SOFTMAX, act: str = "gelu"):
+        """act "gelu": w1 [E, H, F]; "swiglu": w1 [E, H, 2F] = [gate | up]."""
         self.w_router, self.w1, self.w2, self.bias = w_router, w1, w2, bias
-        self.E, self.H, self.F = w1.shape[0], w1.shape[1], w1.shape[2]
+        self.E, self.H, self.F = w2.shape[0], w2.shape[2], w2.shape[1]
+        self.act = act
         self.k = int(k)
         self.capacity_factor = capacity_factor
         self.gating = int(gating)
@@ -296,7 +303,7 @@ class MoELayer:
         if self._T == T:
             return
         self.shape = make_shape(T, self.H, self.F, self.E, self.k, self.capacity_factor,
-                                self.gating)
+                                self.gating, self.act)
         self.ws = alloc_workspace(self.shape, device)
         self.routing = alloc_routing(T, self.E, self.k, device)
         self.y = torch.empty(T, self.H, dtype=torch.bfloat16, device=device)
@@ -334,4 +341,5 @@ __all__ = [n for n in EXPORTS] + ["MoEError", "moe_shape", "make_shape", "load_l
                                    "MoELayer", "RoutingBuffers",
                                    "capacity", "roofline_flops", "load_cv",
                                    "MOE_GATE_TOPK_SOFTMAX", "MOE_GATE_SOFTMAX_TOPK",
-                                   "MOE_GATE_SOFTMAX_TOPK_RENORM"]
+                                   "MOE_GATE_SOFTMAX_TOPK_RENORM", "MOE_EXPERT_GELU",
+                                   "MOE_EXPERT_SWIGLU"]

@@ -122,6 +122,8 @@ int check_shape(const moe_shape* s, bool need_ffn) {
   if (s->H < 8 || s->H % 8 != 0) return fail(MOE_ERR_UNSUPPORTED, "H = %d: need H >= 8, H %% 8 == 0", s->H);
   if (need_ffn && (s->F < 8 || s->F % 8 != 0))
     return fail(MOE_ERR_UNSUPPORTED, "F = %d: need F >= 8, F %% 8 == 0", s->F);
+  if (s->expert_act != MOE_EXPERT_GELU && s->expert_act != MOE_EXPERT_SWIGLU)
+    return fail(MOE_ERR_INVALID_ARG, "expert_act = %d: not a MOE_EXPERT_* value", s->expert_act);
   if (s->gating < MOE_GATE_TOPK_SOFTMAX || s->gating > MOE_GATE_SOFTMAX_TOPK_RENORM)
     return fail(MOE_ERR_INVALID_ARG, "gating = %d: not a MOE_GATE_* value", s->gating);
   if ((int64_t)s->T * s->k > (int64_t)1 << 24)
@@ -263,7 +265,9 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   uint16_t* h = h_ptr(ws, s);
   uint16_t* Y = y_ptr(ws, s);
   CUtensorMap tm_w1, tm_h, tm_w2;
-  if ((rc = map_3d(&tm_w1, w1, (uint64_t)s->F, (uint64_t)s->H, (uint64_t)s->E, 64, 64, "W1")) != MOE_OK) return rc;
+  const bool swiglu = s->expert_act == MOE_EXPERT_SWIGLU;
+  const uint64_t w1_cols = (uint64_t)s->F * (swiglu ? 2 : 1);  // SwiGLU: [W_gate | W_up]
+  if ((rc = map_3d(&tm_w1, w1, w1_cols, (uint64_t)s->H, (uint64_t)s->E, 64, 64, "W1")) != MOE_OK) return rc;
   if ((rc = map_2d(&tm_h, h, (uint64_t)s->F, rows, 64, 128, "h")) != MOE_OK) return rc;
   if ((rc = map_3d(&tm_w2, w2, (uint64_t)s->H, (uint64_t)s->F, (uint64_t)s->E, 64, 64, "W2")) != MOE_OK) return rc;
 
@@ -282,9 +286,10 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   g.N = s->F;
   g.K = s->H;
   g.out = h;
-  int64_t ub = row_blocks_ub * ((s->F + kGemmBN - 1) / kGemmBN);
+  const int out_cols = swiglu ? kGemmBN / 2 : kGemmBN;  // h columns per pair tile
+  int64_t ub = row_blocks_ub * ((s->F + out_cols - 1) / out_cols);
   // GEMM1 gathers its A rows itself; tm_h is passed only to fill the slot
-  cudaError_t e = launch_grouped_gemm(true, tm_h, tm_w1, g, (int)(ub < (1 << 30) ? ub : (1 << 30)), st);
+  cudaError_t e = launch_grouped_gemm(swiglu ? kGemmGatherSwiGLU : kGemmGatherGelu, tm_h, tm_w1, g, (int)(ub < (1 << 30) ? ub : (1 << 30)), st);
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM1 launch");
   if ((rc = mark(ev, 3, st)) != MOE_OK) return rc;
 
@@ -293,7 +298,7 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   g.K = s->F;
   g.out = Y;
   ub = row_blocks_ub * ((s->H + kGemmBN - 1) / kGemmBN);
-  e = launch_grouped_gemm(false, tm_h, tm_w2, g, (int)(ub < (1 << 30) ? ub : (1 << 30)), st);
+  e = launch_grouped_gemm(kGemmPlain, tm_h, tm_w2, g, (int)(ub < (1 << 30) ? ub : (1 << 30)), st);
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM2 launch");
   if ((rc = mark(ev, 4, st)) != MOE_OK) return rc;
 

@@ -3,6 +3,8 @@
 // Computes, for every expert e and every dispatch row r of e
 // (offsets[e] <= r < offsets[e+1]):
 //   GEMM1 (gather + GELU):  h[r, :] = GELU(x[perm[r] / k, :] · W1[e])
+//   GEMM1 (gather + SwiGLU): h[r, :] = SiLU(x[t] · W_gate[e]) * (x[t] · W_up[e]),
+//                           W1[e] = [W_gate | W_up]  (gated experts)
 //   GEMM2 (plain):          Y[r, :] = h[r, :] · W2[e]
 // which are the two Mmad calls of the expert kernel in "用Ascend C写一个
 // MoE融合算子", section "2. Dispatch + Expert + Combine 流水线" (listing
@@ -126,6 +128,9 @@ __device__ __forceinline__ float gelu_erf(float z) {
   return 0.5f * z * (1.0f + erff(z * 0.70710678118654752440f));
 }
 
+// SiLU(z) = z * sigmoid(z)
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
 __device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src),
                "r"(src_bytes)
@@ -144,7 +149,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-template <bool GATHER_GELU>
+template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                         const __grid_constant__ CUtensorMap tm_b, const GemmArgs p) {
@@ -154,13 +159,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
   Ctrl& c = *reinterpret_cast<Ctrl*>(smem + STAGES * STAGE_BYTES);
+  constexpr bool GATHER = MODE != kGemmPlain;  // A rows gathered from x (GEMM1)
+  constexpr bool SWIGLU = MODE == kGemmGatherSwiGLU;
+  // output columns per pair tile: SwiGLU pairs 128 gate with 128 up columns
+  constexpr int BN_OUT = SWIGLU ? BN / 2 : BN;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int rank = (int)cluster_ctarank();  // 0 = leader of the pair
   const int pair = blockIdx.x >> 1;
   const int n_pairs = gridDim.x >> 1;
-  const int NB = (p.N + BN - 1) / BN;
+  const int NB = (p.N + BN_OUT - 1) / BN_OUT;
   const int KB = (p.K + BK - 1) / BK;
 
   // ---- tile schedule from the dispatch offsets (warp 0), barriers (warp 1)
@@ -203,7 +212,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // Only the leader's `full`, `tempty` and `drain` are used.  full: one
     // expect-tx arrival per CTA (+ one arrival per gathering warp of both
     // CTAs for GEMM1); tempty: every epilogue warp of both CTAs.
-    const uint32_t full_count = GATHER_GELU ? 2u + 2u * PRODUCER_WARPS : 2u;
+    const uint32_t full_count = GATHER ? 2u + 2u * PRODUCER_WARPS : 2u;
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&c.full[i], full_count);
       mbar_init(&c.empty[i], 1);
@@ -236,9 +245,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool b_loader = (warp == 0 && lane == 0);
     if (b_loader) {
       tma_prefetch_desc(&tm_b);
-      if constexpr (!GATHER_GELU) tma_prefetch_desc(&tm_a);
+      if constexpr (!GATHER) tma_prefetch_desc(&tm_a);
     }
-    if (GATHER_GELU || warp == 0) {  // GEMM2: warp 0 alone (one TMA thread)
+    if (GATHER || warp == 0) {  // GEMM2: warp 0 alone (one TMA thread)
       const int sub = lane >> 3;     // row within a 4-row group
       const int chunk = lane & 7;    // 16-byte chunk of the 128-byte row slice
       const uint32_t a_base = smem_u32(sA);
@@ -254,7 +263,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint16_t* src[8];
         uint32_t dst[8];
         uint32_t live = 0;  // bit i: row i of this lane belongs to the expert
-        if constexpr (GATHER_GELU) {
+        if constexpr (GATHER) {
           // this CTA's rows 32*warp + 4*i + sub; rows past the expert's end
           // are zero-filled without touching memory (computed, never stored)
 #pragma unroll
@@ -279,15 +288,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           const uint32_t full_cl = full0 + (uint32_t)(stage * sizeof(uint64_t));
           if (b_loader) {
-            mbar_arrive_expect_tx_cluster(full_cl, GATHER_GELU ? B_BYTES : STAGE_BYTES);
-            if constexpr (!GATHER_GELU)
+            mbar_arrive_expect_tx_cluster(full_cl, GATHER ? B_BYTES : STAGE_BYTES);
+            if constexpr (!GATHER)
               tma_load_2d_pair(sA + stage * A_BYTES, &tm_a, full_cl, kb * BK, t.row0);
+            // B columns of this CTA: its half of the 256-wide tile, or for
+            // SwiGLU the gate (rank 0) / up (rank 1) columns of the same
+            // 128 outputs (W1 = [W_gate | W_up], so up starts at column N)
+            const int bcol = SWIGLU ? rank * p.N + t.nb * BN_OUT : t.nb * BN + rank * BN_CTA;
 #pragma unroll
             for (int cb = 0; cb < BN_CTA / 64; ++cb)
-              tma_load_3d_pair(sB + stage * B_BYTES + cb * B_CHUNK, &tm_b, full_cl,
-                               t.nb * BN + rank * BN_CTA + cb * 64, kb * BK, t.e);
+              tma_load_3d_pair(sB + stage * B_BYTES + cb * B_CHUNK, &tm_b, full_cl, bcol + cb * 64,
+                               kb * BK, t.e);
           }
-          if constexpr (GATHER_GELU) {
+          if constexpr (GATHER) {
             // 16-byte chunk (kb*64 + chunk*8 .. +7) of each of this lane's
             // rows; chunks past K and rows past the expert are zero-filled
             // (K % 8 == 0)
@@ -318,7 +331,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      if constexpr (GATHER_GELU) {
+      if constexpr (GATHER) {
         cp_async_wait_all();
         fence_proxy_async_smem();
         __syncwarp();
@@ -401,6 +414,36 @@ __global__ void __launch_bounds__(THREADS, 1)
       const bool row_ok = row < t.rows_valid;
       uint16_t* orow = p.out + (size_t)(row_ok ? t.row0 + row : 0) * (size_t)p.N;
       const uint32_t tbase = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      if constexpr (SWIGLU) {
+        // accumulator columns [0,128) = x W_gate, [128,256) = x W_up of the
+        // same 128 outputs; this warp's group: outputs [64*half, 64*half+64)
+#pragma unroll 1
+        for (int ch = 0; ch < 2; ++ch) {
+          const int col = half * 64 + ch * 32;
+          uint32_t gv[32], uv[32];
+          tmem_ld_x32(tbase + (uint32_t)col, gv);
+          tmem_ld_x32(tbase + (uint32_t)(BN_OUT + col), uv);
+          tmem_ld_wait();
+          const int gcol = t.nb * BN_OUT + col;
+          if (row_ok) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              if (gcol + g * 8 + 8 <= p.N) {
+                float f[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  f[i] = silu(__uint_as_float(gv[g * 8 + i])) * __uint_as_float(uv[g * 8 + i]);
+                uint4 pk;
+                pk.x = pack_bf16x2(f[0], f[1]);
+                pk.y = pack_bf16x2(f[2], f[3]);
+                pk.z = pack_bf16x2(f[4], f[5]);
+                pk.w = pack_bf16x2(f[6], f[7]);
+                *reinterpret_cast<uint4*>(orow + gcol + g * 8) = pk;
+              }
+            }
+          }
+        }
+      } else {
 #pragma unroll 1
       for (int ch = 0; ch < 4; ++ch) {
         const int col = half * 128 + ch * 32;
@@ -416,7 +459,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 f[i] = __uint_as_float(v[g * 8 + i]);
-                if constexpr (GATHER_GELU) f[i] = gelu_erf(f[i]);
+                if constexpr (MODE == kGemmGatherGelu) f[i] = gelu_erf(f[i]);
               }
               uint4 pk;
               pk.x = pack_bf16x2(f[0], f[1]);
@@ -427,6 +470,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
         }
+      }
       }
       tc_fence_before();
       __syncwarp();
@@ -450,7 +494,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   cluster_sync_all();
 }
 
-template <bool G>
+template <int MODE>
 cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const GemmArgs& a,
                         int pairs, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
@@ -465,7 +509,7 @@ cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<G>, tm_a, tm_b, a);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, tm_a, tm_b, a);
 }
 
 // Co-resident CTA pairs of the GEMM kernel on this device (one per TPC).
@@ -488,7 +532,7 @@ cudaError_t query_max_pairs(int dev, int* out) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  cudaError_t e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<true>, &cfg);
+  cudaError_t e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<kGemmGatherGelu>, &cfg);
   if (e != cudaSuccess) return e;
   if (n < 1) return cudaErrorInvalidConfiguration;
   if (dev >= 0 && dev < 64) max_pairs_cache[dev] = n;
@@ -500,7 +544,7 @@ cudaError_t query_max_pairs(int dev, int* out) {
 
 size_t grouped_gemm_smem_bytes() { return SMEM_BYTES; }
 
-cudaError_t launch_grouped_gemm(bool gather_gelu, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                 const GemmArgs& a, int max_tiles, cudaStream_t st) {
   if (max_tiles <= 0) return cudaSuccess;
   int dev = 0, pairs = 0;
@@ -508,16 +552,23 @@ cudaError_t launch_grouped_gemm(bool gather_gelu, const CUtensorMap& tm_a, const
   if (e != cudaSuccess) return e;
   if ((e = query_max_pairs(dev, &pairs)) != cudaSuccess) return e;
   if (pairs > max_tiles) pairs = max_tiles;
-  return gather_gelu ? launch_pair<true>(tm_a, tm_b, a, pairs, st)
-                     : launch_pair<false>(tm_a, tm_b, a, pairs, st);
+  switch (mode) {
+    case kGemmGatherGelu: return launch_pair<kGemmGatherGelu>(tm_a, tm_b, a, pairs, st);
+    case kGemmGatherSwiGLU: return launch_pair<kGemmGatherSwiGLU>(tm_a, tm_b, a, pairs, st);
+    default: return launch_pair<kGemmPlain>(tm_a, tm_b, a, pairs, st);
+  }
 }
 
 cudaError_t grouped_gemm_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<true>,
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kGemmGatherGelu>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(grouped_gemm_kernel<false>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<kGemmGatherSwiGLU>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<kGemmPlain>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+  return e;
 }
 
 }  // namespace moe

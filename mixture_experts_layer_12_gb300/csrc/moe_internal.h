@@ -84,7 +84,7 @@ struct GemmArgs {
   const int32_t* perm;     // gather mode: token row of output row r is perm[r] / k
   int k;
   int E;
-  int N;                   // output columns
+  int N;                   // output columns (SwiGLU: F; W1 then holds 2F columns)
   int K;                   // reduction length
   int T;                   // rows of the gathered tensor (gather mode)
   uint16_t* out;           // [rows, N] bf16, row r = dispatch row
@@ -97,7 +97,10 @@ struct GemmArgs {
 //   tm_a: h [T*k, F], box {64, 128}, tm_b: W2 [E, F, H] box {64, 64, 1}.
 // Launches min(max_tiles, co-resident CTA pairs) persistent pairs
 // (clusters of 2 CTAs); max_tiles bounds the number of 256x256 pair tiles.
-cudaError_t launch_grouped_gemm(bool gather_gelu, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+constexpr int kGemmPlain = 0;          // GEMM2: A rows of h, no activation
+constexpr int kGemmGatherGelu = 1;     // GEMM1: gathered x rows, GELU epilogue
+constexpr int kGemmGatherSwiGLU = 2;   // GEMM1: gathered x rows, SiLU(gate) * up epilogue
+cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                 const GemmArgs& a, int max_tiles, cudaStream_t st);
 size_t grouped_gemm_smem_bytes();
 constexpr int kGemmBM = 128;  // rows per CTA; a CTA pair covers 256

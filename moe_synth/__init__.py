@@ -6,7 +6,7 @@ bench).  It holds no arithmetic of the method: it only draws random tensors.
 Recipe (the workloads' shapes and distributions):
   x        ~ N(0, 1)          [T, H]
   w_router ~ N(0, 1/H)        [H, E]
-  W1       ~ N(0, 1/H)        [E, H, F]
+  W1       ~ N(0, 1/H)        [E, H, F]    (gated experts: [E, H, 2F] = [gate | up])
   W2       ~ N(0, 1/F)        [E, F, H]
   bias     optional fp32 [E] (the skewed workload puts +4.0 on expert 0)
 Each value is drawn as fp32 from torch's CPU generator and rounded to bf16
@@ -37,6 +37,7 @@ class MoEConfig:
     seed: int = 0
     capacity_factor: float | None = None
     bias0: float | None = None  # router bias on expert 0 (others 0)
+    act: str = "gelu"  # "gelu": W1 [E,H,F]; "swiglu": W1 [E,H,2F] = [gate | up]
     notes: str = ""
 
     @property
@@ -56,7 +57,13 @@ SKEWED = MoEConfig("skewed", T=8192, H=2048, F=1408, E=64, k=4, seed=0, bias0=4.
 SKEWED_CF = SKEWED.with_(name="skewed_cf1.2", capacity_factor=1.2)
 DECODE = MoEConfig("decode", T=32, H=4096, F=14336, E=8, k=2, seed=7)
 
-ALL = {c.name: c for c in [TINY, PREFILL, *ROUTER.values(), SKEWED, SKEWED_CF, DECODE]}
+# Gated (SwiGLU) experts at the same shapes: 3 matrices per expert, so the
+# decode workload streams 2.82 GB of weights.
+PREFILL_SWIGLU = PREFILL.with_(name="prefill_swiglu", act="swiglu")
+DECODE_SWIGLU = DECODE.with_(name="decode_swiglu", act="swiglu")
+
+ALL = {c.name: c for c in [TINY, PREFILL, *ROUTER.values(), SKEWED, SKEWED_CF, DECODE,
+                           PREFILL_SWIGLU, DECODE_SWIGLU]}
 
 
 def _gen(seed: int, tensor: str, part: int = 0) -> torch.Generator:
@@ -87,8 +94,12 @@ def make_bias(cfg: MoEConfig) -> torch.Tensor | None:
     return b
 
 
+def w1_cols(cfg: MoEConfig) -> int:
+    return 2 * cfg.F if cfg.act == "swiglu" else cfg.F
+
+
 def make_w1_expert(cfg: MoEConfig, e: int) -> torch.Tensor:
-    return _normal_bf16((cfg.H, cfg.F), 1.0 / math.sqrt(cfg.H), _gen(cfg.seed, "w1", e))
+    return _normal_bf16((cfg.H, w1_cols(cfg)), 1.0 / math.sqrt(cfg.H), _gen(cfg.seed, "w1", e))
 
 
 def make_w2_expert(cfg: MoEConfig, e: int) -> torch.Tensor:
@@ -114,7 +125,7 @@ def make_inputs(cfg: MoEConfig, with_ffn: bool = True, threads: int = 8) -> dict
     """All inputs of ``cfg`` as CPU tensors (bf16, bias fp32 or None)."""
     d = dict(x=make_x(cfg), w_router=make_w_router(cfg), bias=make_bias(cfg))
     if with_ffn and cfg.has_ffn:
-        d["w1"] = _stack_experts(cfg, make_w1_expert, (cfg.H, cfg.F), threads)
+        d["w1"] = _stack_experts(cfg, make_w1_expert, (cfg.H, w1_cols(cfg)), threads)
         d["w2"] = _stack_experts(cfg, make_w2_expert, (cfg.F, cfg.H), threads)
     return d
 

@@ -110,5 +110,6 @@ def reference_y(inputs: dict, logits: np.ndarray, gpu_ids: np.ndarray, gpu_slot:
     """Oracle combine on the GPU's routing decisions with oracle gate weights."""
     w_ref = oracle.gate_weights(logits, gpu_ids,
                                 np.take_along_axis(logits, gpu_ids.astype(np.int64), axis=1), gating)
+    act = "swiglu" if inputs["w1"].shape[2] == 2 * inputs["w2"].shape[1] else "gelu"
     return oracle.combine_rows(inputs["x"], inputs["w1"], inputs["w2"], gpu_ids, w_ref, gpu_slot,
-                               rows, nthreads)
+                               rows, nthreads, act)

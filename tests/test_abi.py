@@ -114,3 +114,10 @@ def test_python_binding_rejects_host_tensors(lib):
         moe.moe_dispatch(s, torch.zeros(4, 2, dtype=torch.int32), torch.zeros(8, dtype=torch.int32),
                          torch.zeros(9, dtype=torch.int32), torch.zeros(8, dtype=torch.int32),
                          torch.zeros(4, 2, dtype=torch.int32), torch.zeros(256, dtype=torch.uint8))
+
+
+def test_unknown_expert_act_rejected(lib):
+    s = moe.make_shape(64, 128, 256, 8, 2)
+    s.expert_act = 7
+    assert lib.moe_workspace_size(ctypes.byref(s)) == 0
+    assert lib.moe_forward(ctypes.byref(s), *([None] * 13), 0, None) == moe.MOE_ERR_INVALID_ARG

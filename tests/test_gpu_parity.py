@@ -43,7 +43,7 @@ def gpu_route(cfg, dev_in, gating=0):
 
 def gpu_forward(cfg, dev_in, gating=0):
     layer = moe.MoELayer(dev_in["w_router"], dev_in["w1"], dev_in["w2"], cfg.k, bias=dev_in["bias"],
-                         capacity_factor=cfg.capacity_factor, gating=gating)
+                         capacity_factor=cfg.capacity_factor, gating=gating, act=cfg.act)
     y = layer(dev_in["x"])
     assert moe.moe_get_device_status(layer.ws) == 0
     return layer, y
@@ -341,3 +341,24 @@ def test_load_cv_diagnostic():
     counts = np_(r.counts).astype(np.float64)
     assert moe.load_cv(r.counts) == pytest.approx(counts.std() / counts.mean(), rel=1e-9)
     assert moe.load_cv(r.counts) > 1.0  # expert 0 takes ~99% of the tokens
+
+
+# ------------------------------------------------------ gated (SwiGLU) experts --
+
+@pytest.mark.parametrize("T,H,F,E,k,cf", [
+    (64, 128, 256, 8, 2, None),      # tiny shape
+    (300, 136, 200, 16, 4, 0.8),     # ragged H and F (F not a multiple of 128), drops
+    (7, 64, 64, 8, 1, None),         # a few tokens
+])
+def test_forward_swiglu_edge_shapes(T, H, F, E, k, cf):
+    cfg = moe_synth.MoEConfig("swiglu", T=T, H=H, F=F, E=E, k=k, seed=50, capacity_factor=cf,
+                              act="swiglu")
+    forward_parity(cfg)
+
+
+def test_forward_swiglu_decode_all_rows():
+    forward_parity(moe_synth.DECODE_SWIGLU)
+
+
+def test_forward_swiglu_prefill_sampled():
+    forward_parity(moe_synth.PREFILL_SWIGLU, stride=16)
