@@ -195,6 +195,7 @@ def kernel_work(cfg, n_rows, experts_hit):
     return {
         "router": dict(flops=2.0 * T * H * E, bytes=2.0 * T * H + 2.0 * H * E + 8.0 * T * k),
         "dispatch": dict(flops=0.0, bytes=4.0 * T * k * 3 + 8.0 * E),
+        "permute": dict(flops=0.0, bytes=4.0 * n_rows * H + 4.0 * n_rows),
         "expert_gemm1": dict(flops=2.0 * n_rows * H * F1,
                              bytes=2.0 * experts_hit * H * F1 + 2.0 * n_rows * H + 2.0 * n_rows * F),
         "expert_gemm2": dict(flops=2.0 * n_rows * F * H,
@@ -390,12 +391,13 @@ def run_ours(args):
         raise RuntimeError("device status set during warm-up")
 
     # The timed steps replay a CUDA graph of R consecutive forward steps (the
-    # same five kernels per step, with the library's per-kernel events), so
+    # same six kernels per step, with the library's per-kernel events), so
     # host launch overhead does not enter the device time.
     R = max(1, min(args.steps, args.graph_steps))
     reps = max(1, args.steps // R)
     K = R * reps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(R)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(moe.KERNEL_NAMES) + 1)]
+           for _ in range(R)]
     for row in evs:  # materialise the event handles before capture
         for e in row:
             e.record(stream)

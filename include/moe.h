@@ -134,8 +134,9 @@ MOE_API int64_t moe_expert_capacity(const moe_shape* s);
 
 /* Workspace bytes needed by moe_forward and moe_expert_ffn_combine (and
  * enough for every other entry point): a 1 KB status block, per-128-token
- * expert counts [ceil(T/128), E] int32, h [T*k, F] bf16 and the expert
- * outputs [T*k, H] bf16.  Returns 0 for an invalid shape. */
+ * expert counts [ceil(T/128), E] int32, h [T*k, F] bf16 and a [T*k, H]
+ * bf16 region that holds first the token rows in dispatch order, then the
+ * expert outputs.  Returns 0 for an invalid shape. */
 MOE_API size_t moe_workspace_size(const moe_shape* s);
 
 /* Workspace bytes needed by moe_route and moe_dispatch (status block and
@@ -182,8 +183,12 @@ MOE_API int moe_dispatch(const moe_shape* s, const int32_t* ids, int32_t* counts
  *   MOE_EXPERT_SWIGLU), W2 [E, F, H] bf16 (H contiguous); weights, offsets,
  *   perm, slot as produced by moe_route.
  *   y [T, H] bf16 (output).
+ * The kept token rows are first copied in dispatch order into the
+ * workspace (row r = x[perm[r] / k], the dispatch step's x_i of section
+ * "MoE的计算流程"), which both expert GEMMs then read with TMA.
  * perm/offsets must describe a valid dispatch (0 <= perm < T*k, offsets
- * non-decreasing, offsets[E] <= T*k); the library does not re-validate them.
+ * non-decreasing, offsets[E] <= T*k); the library does not re-validate them
+ * (a token index outside [0, T) is clamped, never dereferenced).
  */
 MOE_API int moe_expert_ffn_combine(const moe_shape* s, const uint16_t* x, const uint16_t* w1,
                            const uint16_t* w2, const float* weights, const int32_t* offsets,
@@ -193,7 +198,7 @@ MOE_API int moe_expert_ffn_combine(const moe_shape* s, const uint16_t* x, const 
 /*
  * The whole layer (the op "MoEFusion::Compute(x, w_router, expert_weights,
  * y)" of section "3. 完整调用流程"): moe_route followed by
- * moe_expert_ffn_combine, five kernels on `stream` and no host
+ * moe_expert_ffn_combine, six kernels on `stream` and no host
  * synchronisation.  The routing outputs are written as in moe_route.
  */
 MOE_API int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
@@ -237,9 +242,10 @@ MOE_API int moe_expert_ffn_combine_noalloc(const moe_shape* s, const uint16_t* x
 
 /*
  * moe_forward with timing hooks (no counterpart on the pages): `events`
- * points to 6 cudaEvent_t handles (any may be NULL; `events` itself may be
+ * points to 7 cudaEvent_t handles (any may be NULL; `events` itself may be
  * NULL), recorded on `stream` before the router kernel and after each of
- * the five kernels: router, dispatch, expert GEMM1, expert GEMM2, combine.
+ * the six kernels: router, dispatch, permute (token rows into dispatch
+ * order), expert GEMM1, expert GEMM2, combine.
  * The events are caller-owned; the library only records them.
  */
 MOE_API int moe_forward_profiled(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,

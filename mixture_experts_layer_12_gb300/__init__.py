@@ -214,15 +214,19 @@ def moe_forward(shape, x, w_router, b_router, w1, w2, y, ids, weights, counts, o
         _stream(stream)))
 
 
-KERNEL_NAMES = ("router", "dispatch", "expert_gemm1", "expert_gemm2", "combine")
+KERNEL_NAMES = ("router", "dispatch", "permute", "expert_gemm1", "expert_gemm2", "combine")
 
 
 def moe_forward_profiled(shape, x, w_router, b_router, w1, w2, y, ids, weights, counts, offsets,
                          perm, slot, ws, events, stream=None):
-    """moe_forward recording ``events`` (6 torch.cuda.Event or None) at the
-    kernel boundaries: before the router, then after each of KERNEL_NAMES."""
+    """moe_forward recording ``events`` (len(KERNEL_NAMES) + 1 torch.cuda.Event
+    or None) at the kernel boundaries: before the router, then after each of
+    KERNEL_NAMES."""
     bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
-    handles = (ctypes.c_void_p * 6)()
+    n = len(KERNEL_NAMES) + 1
+    if len(events) != n:
+        raise ValueError(f"moe_forward_profiled takes {n} events, got {len(events)}")
+    handles = (ctypes.c_void_p * n)()
     for i, ev in enumerate(events):
         if ev is not None:
             if not ev.cuda_event:

@@ -181,8 +181,8 @@ uint16_t* y_ptr(void* ws, const moe_shape* s) {
 // ------------------------------------------------------------------ steps --
 
 // Optional timing hooks: ev[i] (a cudaEvent_t, may be null) is recorded on
-// the stream at kernel boundary i (0 = before the router, 1..5 = after the
-// router, dispatch, GEMM1, GEMM2 and combine).  Recorded as external events
+// the stream at kernel boundary i (0 = before the router, 1..6 = after the
+// router, dispatch, permute, GEMM1, GEMM2 and combine).  Recorded as external events
 // so that, inside a stream capture, they become timed event-record nodes.
 int mark(void* const* ev, int i, cudaStream_t st) {
   if (!ev || !ev[i]) return MOE_OK;
@@ -264,43 +264,53 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   const uint64_t rows = (uint64_t)s->T * s->k;
   uint16_t* h = h_ptr(ws, s);
   uint16_t* Y = y_ptr(ws, s);
-  CUtensorMap tm_w1, tm_h, tm_w2;
+  uint16_t* xp = Y;  // the permuted tokens live where GEMM2 later writes Y
+  CUtensorMap tm_xp, tm_w1, tm_h, tm_w2;
   const bool swiglu = s->expert_act == MOE_EXPERT_SWIGLU;
   const uint64_t w1_cols = (uint64_t)s->F * (swiglu ? 2 : 1);  // SwiGLU: [W_gate | W_up]
+  if ((rc = map_2d(&tm_xp, xp, (uint64_t)s->H, rows, 64, 128, "xp")) != MOE_OK) return rc;
   if ((rc = map_3d(&tm_w1, w1, w1_cols, (uint64_t)s->H, (uint64_t)s->E, 64, 64, "W1")) != MOE_OK) return rc;
   if ((rc = map_2d(&tm_h, h, (uint64_t)s->F, rows, 64, 128, "h")) != MOE_OK) return rc;
   if ((rc = map_3d(&tm_w2, w2, (uint64_t)s->H, (uint64_t)s->F, (uint64_t)s->E, 64, 64, "W2")) != MOE_OK) return rc;
+
+  PermuteArgs pa;
+  pa.x = x;
+  pa.perm = perm;
+  pa.offsets = offsets;
+  pa.T = s->T;
+  pa.H = s->H;
+  pa.k = s->k;
+  pa.E = s->E;
+  pa.xp = xp;
+  cudaError_t e = launch_permute(pa, sms, st);
+  if (e != cudaSuccess) return cuda_fail(e, "permute launch");
+  if ((rc = mark(ev, 3, st)) != MOE_OK) return rc;
 
   // pair tiles are 2*kGemmBM rows: an expert with n rows owns ceil(n / 256)
   const int64_t row_blocks_ub = ((int64_t)rows + 2 * kGemmBM - 1) / (2 * kGemmBM) + s->E;
   GemmArgs g;
   g.offsets = offsets;
-  g.perm = perm;
-  g.k = s->k;
   g.E = s->E;
-  g.T = s->T;
   g.status = status_ptr(ws);
   g.wait_limit_ns = kWaitLimitNs;
 
-  g.a = x;
   g.N = s->F;
   g.K = s->H;
   g.out = h;
   const int out_cols = swiglu ? kGemmBN / 2 : kGemmBN;  // h columns per pair tile
   int64_t ub = row_blocks_ub * ((s->F + out_cols - 1) / out_cols);
-  // GEMM1 gathers its A rows itself; tm_h is passed only to fill the slot
-  cudaError_t e = launch_grouped_gemm(swiglu ? kGemmGatherSwiGLU : kGemmGatherGelu, tm_h, tm_w1, g, (int)(ub < (1 << 30) ? ub : (1 << 30)), st);
+  e = launch_grouped_gemm(swiglu ? kGemmSwiGLU : kGemmGelu, tm_xp, tm_w1, g,
+                          (int)(ub < (1 << 30) ? ub : (1 << 30)), st);
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM1 launch");
-  if ((rc = mark(ev, 3, st)) != MOE_OK) return rc;
+  if ((rc = mark(ev, 4, st)) != MOE_OK) return rc;
 
-  g.a = h;
   g.N = s->H;
   g.K = s->F;
   g.out = Y;
   ub = row_blocks_ub * ((s->H + kGemmBN - 1) / kGemmBN);
   e = launch_grouped_gemm(kGemmPlain, tm_h, tm_w2, g, (int)(ub < (1 << 30) ? ub : (1 << 30)), st);
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM2 launch");
-  if ((rc = mark(ev, 4, st)) != MOE_OK) return rc;
+  if ((rc = mark(ev, 5, st)) != MOE_OK) return rc;
 
   CombineArgs ca;
   ca.Y = Y;
@@ -312,7 +322,7 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   ca.y = y;
   e = launch_combine(ca, st);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-  return mark(ev, 5, st);
+  return mark(ev, 6, st);
 }
 
 int clear_status(void* ws, cudaStream_t st) {

@@ -124,6 +124,38 @@ __global__ void __launch_bounds__(CTHREADS) combine_kernel(const CombineArgs a) 
   *reinterpret_cast<uint4*>(a.y + (size_t)t * a.H + col) = o;
 }
 
+// xp[r] = x[perm[r] / k] for the kept rows r < offsets[E]: the dispatch-
+// ordered ("expanded") copy of the tokens that the expert GEMM reads with
+// TMA.  One warp per row, 16-byte loads, four in flight per lane; the copy
+// is HBM/L2-bandwidth bound (2 H bytes read + 2 H bytes written per row).
+constexpr int PTHREADS = 256;
+__global__ void __launch_bounds__(PTHREADS) permute_kernel(const PermuteArgs a) {
+  const int rows = a.T * a.k;
+  const int kept = min(max(__ldg(a.offsets + a.E), 0), rows);
+  const int vec = a.H / 8;  // 16-byte chunks per row (H % 8 == 0)
+  const int lane = threadIdx.x & 31;
+  const int nw = gridDim.x * (PTHREADS / 32);
+  for (int r = blockIdx.x * (PTHREADS / 32) + (threadIdx.x >> 5); r < kept; r += nw) {
+    // perm is not re-validated by the caller-facing entry point: clamp so a
+    // bad entry cannot address outside x
+    const int tok = min(max(__ldg(a.perm + r) / a.k, 0), a.T - 1);
+    const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)tok * a.H);
+    uint4* dst = reinterpret_cast<uint4*>(a.xp + (size_t)r * a.H);
+    int c = lane;
+    for (; c + 96 < vec; c += 128) {
+      const uint4 v0 = __ldg(src + c);
+      const uint4 v1 = __ldg(src + c + 32);
+      const uint4 v2 = __ldg(src + c + 64);
+      const uint4 v3 = __ldg(src + c + 96);
+      dst[c] = v0;
+      dst[c + 32] = v1;
+      dst[c + 64] = v2;
+      dst[c + 96] = v3;
+    }
+    for (; c < vec; c += 32) dst[c] = __ldg(src + c);
+  }
+}
+
 // One thread waits on an mbarrier that nothing arrives on; the bounded wait
 // gives up after limit_ns, records MOE_DEV_TIMEOUT and the kernel returns.
 __global__ void wait_selftest_kernel(int* status, uint64_t limit_ns) {
@@ -151,6 +183,9 @@ cudaError_t dispatch_combine_set_attributes() {
   cudaError_t e = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess)
     e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
   return e;
@@ -159,6 +194,16 @@ cudaError_t dispatch_combine_set_attributes() {
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st) {
   const int nseg = (a.T + a.seg_tokens - 1) / a.seg_tokens;
   dispatch_kernel<<<nseg, DTHREADS, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const PermuteArgs& a, int sms, cudaStream_t st) {
+  const int64_t rows = (int64_t)a.T * a.k;
+  const int64_t want = (rows + PTHREADS / 32 - 1) / (PTHREADS / 32);  // one row per warp
+  const int64_t cap = (int64_t)(sms > 0 ? sms : 1) * (2048 / PTHREADS);
+  const unsigned grid = (unsigned)(want < cap ? want : cap);
+  if (grid == 0) return cudaSuccess;
+  permute_kernel<<<grid, PTHREADS, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -1,11 +1,12 @@
 // ffn_gemm.cu -- grouped expert GEMM on the 5th-generation tensor cores.
 //
 // Computes, for every expert e and every dispatch row r of e
-// (offsets[e] <= r < offsets[e+1]):
-//   GEMM1 (gather + GELU):  h[r, :] = GELU(x[perm[r] / k, :] · W1[e])
-//   GEMM1 (gather + SwiGLU): h[r, :] = SiLU(x[t] · W_gate[e]) * (x[t] · W_up[e]),
-//                           W1[e] = [W_gate | W_up]  (gated experts)
-//   GEMM2 (plain):          Y[r, :] = h[r, :] · W2[e]
+// (offsets[e] <= r < offsets[e+1]), with xp[r] = x[perm[r] / k] the
+// dispatch-ordered copy of the tokens:
+//   GEMM1 (GELU):   h[r, :] = GELU(xp[r, :] · W1[e])
+//   GEMM1 (SwiGLU): h[r, :] = SiLU(xp[r] · W_gate[e]) * (xp[r] · W_up[e]),
+//                   W1[e] = [W_gate | W_up]  (gated experts)
+//   GEMM2 (plain):  Y[r, :] = h[r, :] · W2[e]
 // which are the two Mmad calls of the expert kernel in "用Ascend C写一个
 // MoE融合算子", section "2. Dispatch + Expert + Combine 流水线" (listing
 // "Expert计算": M = tokens of the expert, N = ffn_hidden_dim, K = hidden_dim,
@@ -21,20 +22,18 @@
 //     through L2 (the pages' expert-block / token-block tiling, made ragged:
 //     an expert owns ceil(n_e / 256) row blocks); the tile list is built on
 //     the device from `offsets`, with no host synchronisation.
-//   * warps 0-3: producers.  Weight tiles (two 64-column TMA boxes of W[e]
-//     per CTA, N contiguous = MN-major operand) and GEMM2's A tile (rows of
-//     h, one box) are TMA loads that signal the leader CTA's stage barrier.
-//     GEMM1's A tile is gathered straight from x by the 128 producer threads
-//     with 16-byte cp.async (8 lanes per 128-byte row slice, 128-byte
-//     swizzle applied by hand), so no permuted copy of x exists; each lane
-//     waits for its own copies and fences them into the async proxy, then
-//     one lane per warp arrives on the leader's stage barrier.
-//   * warp 4: TMEM (two 128x256 fp32 accumulators per CTA, 512 columns);
+//   * warp 0: producer.  One thread per CTA issues the TMA loads of the
+//     stage: the A tile (128 rows of xp or h, one box) and the weight tile
+//     (two 64-column boxes of W[e], N contiguous = MN-major operand); both
+//     CTAs' loads signal the leader CTA's stage barrier.  (Gathering A rows
+//     from x inside the kernel with cp.async cost more tensor-pipe time than
+//     the separate row copy that produces xp.)
+//   * warp 1: TMEM (two 128x256 fp32 accumulators per CTA, 512 columns);
 //     in the leader one thread issues the MMAs from a 6-stage ring (the
 //     load / compute / store overlap of the article's section 2.2
 //     pipeline) and its commits release the stage / publish the
 //     accumulator in both CTAs.
-//   * warps 5-12: epilogue; tcgen05.ld of the CTA's 128 accumulator rows,
+//   * warps 2-9: epilogue; tcgen05.ld of the CTA's 128 accumulator rows,
 //     GELU(erf) for GEMM1, bf16 rounding and 16-byte stores; double-buffered
 //     against the next tile's MMAs.
 // Every mbarrier wait is bounded (MOE_DEV_TIMEOUT on expiry).
@@ -54,22 +53,19 @@ constexpr int A_BYTES = BM * BK * 2;   // 16 KB: 128 rows x 128 B
 constexpr int B_CHUNK = BK * 64 * 2;   // 8 KB: one 64-column box, 64 K rows
 constexpr int B_BYTES = (BN_CTA / 64) * B_CHUNK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int PRODUCER_WARPS = 4;
-constexpr int PRODUCER_THREADS = 32 * PRODUCER_WARPS;
-constexpr int MMA_WARP = PRODUCER_WARPS;
+constexpr int PRODUCER_WARP = 0;
+constexpr int MMA_WARP = 1;
 constexpr int EPI_WARP0 = MMA_WARP + 1;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
 constexpr int TMEM_COLS = ACC * BN;  // 512
-constexpr int GATHER_INFLIGHT = 4;   // cp.async groups a producer keeps open
 constexpr uint16_t PAIR_MASK = 0x3;
 constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, BN, /*a_mn=*/false, /*b_mn=*/true);
 
 static_assert(BK == 64, "one 128-byte swizzle atom of K per stage");
 static_assert(BN_CTA % 64 == 0 && BN <= 256, "UMMA N");
 static_assert(TMEM_COLS <= 512, "TMEM capacity");
-static_assert(PRODUCER_THREADS == BM, "8 lanes per row slice, 4 rows per warp op, 8 ops");
-static_assert(GATHER_INFLIGHT == 4 && GATHER_INFLIGHT < STAGES, "cp.async.wait_group immediate");
+static_assert(EPI_WARPS == 8, "two warps per TMEM lane quadrant (warp % 4), one per column half");
 
 struct Ctrl {
   uint64_t full[STAGES];
@@ -131,24 +127,6 @@ __device__ __forceinline__ float gelu_erf(float z) {
 // SiLU(z) = z * sigmoid(z)
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
-__device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_inflight() {
-  asm volatile("cp.async.wait_group 3;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
@@ -159,8 +137,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
   Ctrl& c = *reinterpret_cast<Ctrl*>(smem + STAGES * STAGE_BYTES);
-  constexpr bool GATHER = MODE != kGemmPlain;  // A rows gathered from x (GEMM1)
-  constexpr bool SWIGLU = MODE == kGemmGatherSwiGLU;
+  constexpr bool SWIGLU = MODE == kGemmSwiGLU;
   // output columns per pair tile: SwiGLU pairs 128 gate with 128 up columns
   constexpr int BN_OUT = SWIGLU ? BN / 2 : BN;
 
@@ -210,11 +187,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (threadIdx.x == 32) {
     // Only the leader's `full`, `tempty` and `drain` are used.  full: one
-    // expect-tx arrival per CTA (+ one arrival per gathering warp of both
-    // CTAs for GEMM1); tempty: every epilogue warp of both CTAs.
-    const uint32_t full_count = GATHER ? 2u + 2u * PRODUCER_WARPS : 2u;
+    // expect-tx arrival per CTA; tempty: every epilogue warp of both CTAs.
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(&c.full[i], full_count);
+      mbar_init(&c.full[i], 2);
       mbar_init(&c.empty[i], 1);
     }
     for (int i = 0; i < ACC; ++i) {
@@ -240,90 +215,37 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem = c.tmem_base;
   const WaitCtl wc{&c.abort_flag, p.status, p.wait_limit_ns};
 
-  if (warp < PRODUCER_WARPS) {
-    // ------------------------------------------------ producer warps
-    const bool b_loader = (warp == 0 && lane == 0);
-    if (b_loader) {
+  if (warp == PRODUCER_WARP) {
+    // ------------------------------------------------ producer (one thread)
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_a);
       tma_prefetch_desc(&tm_b);
-      if constexpr (!GATHER) tma_prefetch_desc(&tm_a);
-    }
-    if (GATHER || warp == 0) {  // GEMM2: warp 0 alone (one TMA thread)
-      const int sub = lane >> 3;     // row within a 4-row group
-      const int chunk = lane & 7;    // 16-byte chunk of the 128-byte row slice
-      const uint32_t a_base = smem_u32(sA);
       const uint32_t full0 = dsmem_map(smem_u32(&c.full[0]), 0);  // leader's barriers
       int stage = 0;
       uint32_t phase = 0;
-      int issued = 0;    // k-blocks issued (all tiles)
-      int signaled = 0;  // k-blocks whose A slice this thread has published
+      int issued = 0;  // k-blocks issued (all tiles)
       int e = 0;
       bool ok = true;
       for (int tile = pair; tile < n_tiles && ok; tile += n_pairs) {
         const Tile t = decode_tile(c, tile, e, rank);
-        const uint16_t* src[8];
-        uint32_t dst[8];
-        uint32_t live = 0;  // bit i: row i of this lane belongs to the expert
-        if constexpr (GATHER) {
-          // this CTA's rows 32*warp + 4*i + sub; rows past the expert's end
-          // are zero-filled without touching memory (computed, never stored)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int row = 32 * warp + 4 * i + sub;
-            int tok = 0;
-            if (row < t.rows_valid) {
-              tok = min(max(__ldg(p.perm + t.row0 + row) / p.k, 0), p.T - 1);
-              live |= 1u << i;
-            }
-            src[i] = p.a + (size_t)tok * (size_t)p.K + chunk * 8;
-            dst[i] = (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
-          }
-        }
+        // B columns of this CTA: its half of the 256-wide tile, or for
+        // SwiGLU the gate (rank 0) / up (rank 1) columns of the same 128
+        // outputs (W1 = [W_gate | W_up], so up starts at column N)
+        const int bcol = SWIGLU ? rank * p.N + t.nb * BN_OUT : t.nb * BN + rank * BN_CTA;
         for (int kb = 0; kb < KB; ++kb) {
-          int got = 1;
-          if (lane == 0) got = mbar_wait(&c.empty[stage], phase ^ 1u, wc);
-          got = __shfl_sync(0xffffffffu, got, 0);
-          if (!got) {
+          if (!mbar_wait(&c.empty[stage], phase ^ 1u, wc)) {
             ok = false;
             break;
           }
           const uint32_t full_cl = full0 + (uint32_t)(stage * sizeof(uint64_t));
-          if (b_loader) {
-            mbar_arrive_expect_tx_cluster(full_cl, GATHER ? B_BYTES : STAGE_BYTES);
-            if constexpr (!GATHER)
-              tma_load_2d_pair(sA + stage * A_BYTES, &tm_a, full_cl, kb * BK, t.row0);
-            // B columns of this CTA: its half of the 256-wide tile, or for
-            // SwiGLU the gate (rank 0) / up (rank 1) columns of the same
-            // 128 outputs (W1 = [W_gate | W_up], so up starts at column N)
-            const int bcol = SWIGLU ? rank * p.N + t.nb * BN_OUT : t.nb * BN + rank * BN_CTA;
+          mbar_arrive_expect_tx_cluster(full_cl, STAGE_BYTES);
+          // rows past the expert's end belong to the next expert (or lie past
+          // the last row: zero-filled); they are computed but never stored
+          tma_load_2d_pair(sA + stage * A_BYTES, &tm_a, full_cl, kb * BK, t.row0);
 #pragma unroll
-            for (int cb = 0; cb < BN_CTA / 64; ++cb)
-              tma_load_3d_pair(sB + stage * B_BYTES + cb * B_CHUNK, &tm_b, full_cl, bcol + cb * 64,
-                               kb * BK, t.e);
-          }
-          if constexpr (GATHER) {
-            // 16-byte chunk (kb*64 + chunk*8 .. +7) of each of this lane's
-            // rows; chunks past K and rows past the expert are zero-filled
-            // (K % 8 == 0)
-            const bool in_k = kb * BK + chunk * 8 < p.K;
-            const uint32_t sbase = a_base + (uint32_t)(stage * A_BYTES);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint32_t nbytes = (in_k && ((live >> i) & 1u)) ? 16u : 0u;
-              cp_async_16(sbase + dst[i],
-                          nbytes ? (const void*)(src[i] + kb * BK) : (const void*)src[i], nbytes);
-            }
-            cp_async_commit();
-            if (issued + 1 - signaled == GATHER_INFLIGHT) {
-              // the oldest open group has landed for every lane: fence each
-              // lane's copies into the async proxy, then one arrival per warp
-              cp_async_wait_inflight();
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0)
-                mbar_arrive_cluster(full0 + (uint32_t)((signaled % STAGES) * sizeof(uint64_t)));
-              ++signaled;
-            }
-          }
+          for (int cb = 0; cb < BN_CTA / 64; ++cb)
+            tma_load_3d_pair(sB + stage * B_BYTES + cb * B_CHUNK, &tm_b, full_cl, bcol + cb * 64,
+                             kb * BK, t.e);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
@@ -331,24 +253,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      if constexpr (GATHER) {
-        cp_async_wait_all();
-        fence_proxy_async_smem();
-        __syncwarp();
-        for (; signaled < issued; ++signaled)
-          if (lane == 0)
-            mbar_arrive_cluster(full0 + (uint32_t)((signaled % STAGES) * sizeof(uint64_t)));
-      }
       // Drain (leader): the TMA bytes of the last STAGES armed stages of both
       // CTAs must have landed before shared memory is released (returns at
       // once on the normal path, where the MMA consumed every stage).
-      if (b_loader && rank == 0) {
+      if (rank == 0) {
         for (int m = max(0, issued - STAGES); m < issued; ++m)
           mbar_wait_drain(&c.full[m % STAGES], (uint32_t)((m / STAGES) & 1), p.wait_limit_ns,
                           p.status);
       }
-      __syncwarp();
     }
+    __syncwarp();
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------ MMA issuer (leader)
     if (rank == 0 && lane == 0) {
@@ -459,7 +373,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 f[i] = __uint_as_float(v[g * 8 + i]);
-                if constexpr (MODE == kGemmGatherGelu) f[i] = gelu_erf(f[i]);
+                if constexpr (MODE == kGemmGelu) f[i] = gelu_erf(f[i]);
               }
               uint4 pk;
               pk.x = pack_bf16x2(f[0], f[1]);
@@ -532,7 +446,7 @@ cudaError_t query_max_pairs(int dev, int* out) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  cudaError_t e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<kGemmGatherGelu>, &cfg);
+  cudaError_t e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<kGemmGelu>, &cfg);
   if (e != cudaSuccess) return e;
   if (n < 1) return cudaErrorInvalidConfiguration;
   if (dev >= 0 && dev < 64) max_pairs_cache[dev] = n;
@@ -553,17 +467,17 @@ cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tm_a, const CUtenso
   if ((e = query_max_pairs(dev, &pairs)) != cudaSuccess) return e;
   if (pairs > max_tiles) pairs = max_tiles;
   switch (mode) {
-    case kGemmGatherGelu: return launch_pair<kGemmGatherGelu>(tm_a, tm_b, a, pairs, st);
-    case kGemmGatherSwiGLU: return launch_pair<kGemmGatherSwiGLU>(tm_a, tm_b, a, pairs, st);
+    case kGemmGelu: return launch_pair<kGemmGelu>(tm_a, tm_b, a, pairs, st);
+    case kGemmSwiGLU: return launch_pair<kGemmSwiGLU>(tm_a, tm_b, a, pairs, st);
     default: return launch_pair<kGemmPlain>(tm_a, tm_b, a, pairs, st);
   }
 }
 
 cudaError_t grouped_gemm_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kGemmGatherGelu>,
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kGemmGelu>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(grouped_gemm_kernel<kGemmGatherSwiGLU>,
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<kGemmSwiGLU>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(grouped_gemm_kernel<kGemmPlain>,

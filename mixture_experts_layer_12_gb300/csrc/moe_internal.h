@@ -79,33 +79,40 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st);
 
 // ---- grouped expert GEMM (tcgen05 + TMA, persistent ragged scheduler).
 struct GemmArgs {
-  const uint16_t* a;       // gather mode: x [T, K] bf16 (rows gathered with cp.async)
   const int32_t* offsets;  // [E+1] dispatch offsets (device)
-  const int32_t* perm;     // gather mode: token row of output row r is perm[r] / k
-  int k;
   int E;
   int N;                   // output columns (SwiGLU: F; W1 then holds 2F columns)
   int K;                   // reduction length
-  int T;                   // rows of the gathered tensor (gather mode)
   uint16_t* out;           // [rows, N] bf16, row r = dispatch row
   int* status;
   uint64_t wait_limit_ns;
 };
-// GEMM1: A rows gathered from x (GemmArgs::a) through perm, GELU epilogue.
-//   tm_a: unused, tm_b: W1 [E, H, F] box {64, 64, 1}.
-// GEMM2: A rows contiguous (dispatch order), no activation.
-//   tm_a: h [T*k, F], box {64, 128}, tm_b: W2 [E, F, H] box {64, 64, 1}.
+// Both GEMMs read A rows in dispatch order through tm_a, box {64, 128}:
+// GEMM1: tm_a = xp [T*k, H] (permuted tokens), tm_b = W1 [E, H, F] (or
+//   [E, H, 2F] for SwiGLU), box {64, 64, 1}; GELU or SiLU(gate) * up.
+// GEMM2: tm_a = h [T*k, F], tm_b = W2 [E, F, H] box {64, 64, 1}; no activation.
 // Launches min(max_tiles, co-resident CTA pairs) persistent pairs
 // (clusters of 2 CTAs); max_tiles bounds the number of 256x256 pair tiles.
-constexpr int kGemmPlain = 0;          // GEMM2: A rows of h, no activation
-constexpr int kGemmGatherGelu = 1;     // GEMM1: gathered x rows, GELU epilogue
-constexpr int kGemmGatherSwiGLU = 2;   // GEMM1: gathered x rows, SiLU(gate) * up epilogue
+constexpr int kGemmPlain = 0;   // GEMM2: no activation
+constexpr int kGemmGelu = 1;    // GEMM1: GELU epilogue
+constexpr int kGemmSwiGLU = 2;  // GEMM1: SiLU(gate) * up epilogue
 cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                 const GemmArgs& a, int max_tiles, cudaStream_t st);
 size_t grouped_gemm_smem_bytes();
 constexpr int kGemmBM = 128;  // rows per CTA; a CTA pair covers 256
 constexpr int kGemmBN = 256;
 constexpr int kGemmBK = 64;
+
+// ---- row permutation (the expanded-x output of the dispatch step):
+// xp[r] = x[perm[r] / k] for r < offsets[E]; rows past offsets[E] untouched.
+struct PermuteArgs {
+  const uint16_t* x;  // [T, H]
+  const int32_t* perm;
+  const int32_t* offsets;  // offsets[E] = number of kept rows (device)
+  int T, H, k, E;
+  uint16_t* xp;  // [T*k, H]
+};
+cudaError_t launch_permute(const PermuteArgs& a, int sms, cudaStream_t st);
 
 // ---- combine: y[t] = sum_j w[t,j] * Y[slot[t,j]] (fp32), bf16 out.
 struct CombineArgs {

@@ -289,14 +289,15 @@ def test_profiled_forward_eager_and_captured():
     layer, y_ref = gpu_forward(cfg, dev_in)
     y_ref = y_ref.clone()
     r = layer.routing
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    nk = len(moe.KERNEL_NAMES)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
     for e in evs:
         e.record()
     args = (layer.shape, dev_in["x"], layer.w_router, layer.bias, layer.w1, layer.w2, layer.y, r.ids,
             r.weights, r.counts, r.offsets, r.perm, r.slot, layer.ws)
     moe.moe_forward_profiled(*args, evs)  # eager
     torch.cuda.synchronize()
-    times = [evs[i].elapsed_time(evs[i + 1]) for i in range(5)]
+    times = [evs[i].elapsed_time(evs[i + 1]) for i in range(nk)]
     assert all(t >= 0 for t in times)
     assert torch.equal(layer.y, y_ref)
     g = torch.cuda.CUDAGraph()  # captured: events become timed graph nodes
@@ -305,7 +306,7 @@ def test_profiled_forward_eager_and_captured():
     layer.y.zero_()
     g.replay()
     torch.cuda.synchronize()
-    assert all(evs[i].elapsed_time(evs[i + 1]) >= 0 for i in range(5))
+    assert all(evs[i].elapsed_time(evs[i + 1]) >= 0 for i in range(nk))
     assert torch.equal(layer.y, y_ref)
 
 
