@@ -31,7 +31,10 @@
  *     slots are all dropped gets y = 0.
  *   - The expert hidden activation h and the expert output are rounded to
  *     bf16 in the workspace; y is bf16 (round to nearest even) from an fp32
- *     combine summed in slot order j = 0..k-1.
+ *     combine summed in slot order j = 0..k-1.  With k = 1 the combine is
+ *     done by the second expert GEMM itself: y[t] = w[t] * (h W2) is formed
+ *     from the fp32 accumulator and rounded to bf16 once (no bf16 rounding
+ *     of the expert output in between).
  *
  * Conventions for every entry point:
  *   - Tensor pointers are DEVICE pointers owned by the caller, row-major and
@@ -198,7 +201,7 @@ MOE_API int moe_expert_ffn_combine(const moe_shape* s, const uint16_t* x, const 
 /*
  * The whole layer (the op "MoEFusion::Compute(x, w_router, expert_weights,
  * y)" of section "3. 完整调用流程"): moe_route followed by
- * moe_expert_ffn_combine, six kernels on `stream` and no host
+ * moe_expert_ffn_combine, six kernels (five when k = 1) on `stream` and no host
  * synchronisation.  The routing outputs are written as in moe_route.
  */
 MOE_API int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
@@ -245,7 +248,8 @@ MOE_API int moe_expert_ffn_combine_noalloc(const moe_shape* s, const uint16_t* x
  * points to 7 cudaEvent_t handles (any may be NULL; `events` itself may be
  * NULL), recorded on `stream` before the router kernel and after each of
  * the six kernels: router, dispatch, permute (token rows into dispatch
- * order), expert GEMM1, expert GEMM2, combine.
+ * order), expert GEMM1, expert GEMM2, combine.  With k = 1 there is no
+ * combine kernel and the last two events are recorded back to back.
  * The events are caller-owned; the library only records them.
  */
 MOE_API int moe_forward_profiled(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,

@@ -282,6 +282,10 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   pa.k = s->k;
   pa.E = s->E;
   pa.xp = xp;
+  // k = 1: GEMM2 writes y itself (fused combine); dropped tokens are zeroed here
+  const bool fuse_combine = s->k == 1;
+  pa.slot = slot;
+  pa.y_zero = fuse_combine ? y : nullptr;
   cudaError_t e = launch_permute(pa, sms, st);
   if (e != cudaSuccess) return cuda_fail(e, "permute launch");
   if ((rc = mark(ev, 3, st)) != MOE_OK) return rc;
@@ -291,6 +295,9 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   GemmArgs g;
   g.offsets = offsets;
   g.E = s->E;
+  g.perm = perm;
+  g.gate_w = weights;
+  g.T = s->T;
   g.status = status_ptr(ws);
   g.wait_limit_ns = kWaitLimitNs;
 
@@ -306,11 +313,13 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
 
   g.N = s->H;
   g.K = s->F;
-  g.out = Y;
+  g.out = fuse_combine ? y : Y;
   ub = row_blocks_ub * ((s->H + kGemmBN - 1) / kGemmBN);
-  e = launch_grouped_gemm(kGemmPlain, tm_h, tm_w2, g, (int)(ub < (1 << 30) ? ub : (1 << 30)), st);
+  e = launch_grouped_gemm(fuse_combine ? kGemmCombineK1 : kGemmPlain, tm_h, tm_w2, g,
+                          (int)(ub < (1 << 30) ? ub : (1 << 30)), st);
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM2 launch");
   if ((rc = mark(ev, 5, st)) != MOE_OK) return rc;
+  if (fuse_combine) return mark(ev, 6, st);  // no combine kernel: the combine window is empty
 
   CombineArgs ca;
   ca.Y = Y;

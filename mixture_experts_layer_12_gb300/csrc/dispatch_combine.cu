@@ -154,6 +154,14 @@ __global__ void __launch_bounds__(PTHREADS) permute_kernel(const PermuteArgs a) 
     }
     for (; c < vec; c += 32) dst[c] = __ldg(src + c);
   }
+  if (a.y_zero) {
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (int t = blockIdx.x * (PTHREADS / 32) + (threadIdx.x >> 5); t < a.T; t += nw) {
+      if (__ldg(a.slot + t) >= 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(a.y_zero + (size_t)t * a.H);
+      for (int c = lane; c < vec; c += 32) dst[c] = z;
+    }
+  }
 }
 
 // One thread waits on an mbarrier that nothing arrives on; the bounded wait

@@ -138,6 +138,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* sB = smem + STAGES * A_BYTES;
   Ctrl& c = *reinterpret_cast<Ctrl*>(smem + STAGES * STAGE_BYTES);
   constexpr bool SWIGLU = MODE == kGemmSwiGLU;
+  constexpr bool COMBINE = MODE == kGemmCombineK1;  // k = 1: scale by the gate, write y[t]
   // output columns per pair tile: SwiGLU pairs 128 gate with 128 up columns
   constexpr int BN_OUT = SWIGLU ? BN / 2 : BN;
 
@@ -325,8 +326,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!got) break;
       tc_fence_after();
       const int row = q * 32 + lane;
-      const bool row_ok = row < t.rows_valid;
+      bool row_ok = row < t.rows_valid;
       uint16_t* orow = p.out + (size_t)(row_ok ? t.row0 + row : 0) * (size_t)p.N;
+      float gw = 1.0f;
+      if constexpr (COMBINE) {
+        // the token's only expert row: y[t] = w[t] * (h W2)[r], no Y round trip
+        const int tok = row_ok ? __ldg(p.perm + t.row0 + row) : -1;
+        row_ok = row_ok && tok >= 0 && tok < p.T;  // perm is not re-validated: never write outside y
+        if (row_ok) {
+          gw = __ldg(p.gate_w + tok);
+          orow = p.out + (size_t)tok * (size_t)p.N;
+        }
+      }
       const uint32_t tbase = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       if constexpr (SWIGLU) {
         // accumulator columns [0,128) = x W_gate, [128,256) = x W_up of the
@@ -374,6 +385,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               for (int i = 0; i < 8; ++i) {
                 f[i] = __uint_as_float(v[g * 8 + i]);
                 if constexpr (MODE == kGemmGelu) f[i] = gelu_erf(f[i]);
+                if constexpr (COMBINE) f[i] *= gw;
               }
               uint4 pk;
               pk.x = pack_bf16x2(f[0], f[1]);
@@ -469,6 +481,7 @@ cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tm_a, const CUtenso
   switch (mode) {
     case kGemmGelu: return launch_pair<kGemmGelu>(tm_a, tm_b, a, pairs, st);
     case kGemmSwiGLU: return launch_pair<kGemmSwiGLU>(tm_a, tm_b, a, pairs, st);
+    case kGemmCombineK1: return launch_pair<kGemmCombineK1>(tm_a, tm_b, a, pairs, st);
     default: return launch_pair<kGemmPlain>(tm_a, tm_b, a, pairs, st);
   }
 }
@@ -478,6 +491,9 @@ cudaError_t grouped_gemm_set_attributes() {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(grouped_gemm_kernel<kGemmSwiGLU>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(grouped_gemm_kernel<kGemmCombineK1>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(grouped_gemm_kernel<kGemmPlain>,

@@ -83,7 +83,10 @@ struct GemmArgs {
   int E;
   int N;                   // output columns (SwiGLU: F; W1 then holds 2F columns)
   int K;                   // reduction length
-  uint16_t* out;           // [rows, N] bf16, row r = dispatch row
+  uint16_t* out;           // [rows, N] bf16, row r = dispatch row (kGemmCombineK1: y [T, N])
+  const int32_t* perm;     // kGemmCombineK1: token of dispatch row r (k = 1: perm[r] = t)
+  const float* gate_w;     // kGemmCombineK1: gate weight of token t
+  int T;                   // kGemmCombineK1: tokens (rows of y)
   int* status;
   uint64_t wait_limit_ns;
 };
@@ -96,6 +99,7 @@ struct GemmArgs {
 constexpr int kGemmPlain = 0;   // GEMM2: no activation
 constexpr int kGemmGelu = 1;    // GEMM1: GELU epilogue
 constexpr int kGemmSwiGLU = 2;  // GEMM1: SiLU(gate) * up epilogue
+constexpr int kGemmCombineK1 = 3;  // GEMM2 + combine for k = 1: y[perm[r]] = w * acc
 cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                 const GemmArgs& a, int max_tiles, cudaStream_t st);
 size_t grouped_gemm_smem_bytes();
@@ -111,6 +115,10 @@ struct PermuteArgs {
   const int32_t* offsets;  // offsets[E] = number of kept rows (device)
   int T, H, k, E;
   uint16_t* xp;  // [T*k, H]
+  // k = 1 with the combine fused into GEMM2: y rows of tokens whose only
+  // slot was dropped (slot[t] < 0) are zeroed here; null otherwise
+  const int32_t* slot;
+  uint16_t* y_zero;
 };
 cudaError_t launch_permute(const PermuteArgs& a, int sms, cudaStream_t st);
 

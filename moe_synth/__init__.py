@@ -60,10 +60,13 @@ DECODE = MoEConfig("decode", T=32, H=4096, F=14336, E=8, k=2, seed=7)
 # Gated (SwiGLU) experts at the same shapes: 3 matrices per expert, so the
 # decode workload streams 2.82 GB of weights.
 PREFILL_SWIGLU = PREFILL.with_(name="prefill_swiglu", act="swiglu")
+# One expert per token (top-1 routing, as in Switch-style layers): the
+# combine is a single scaled row, written by the second GEMM itself.
+PREFILL_K1 = PREFILL.with_(name="prefill_k1", k=1)
 DECODE_SWIGLU = DECODE.with_(name="decode_swiglu", act="swiglu")
 
 ALL = {c.name: c for c in [TINY, PREFILL, *ROUTER.values(), SKEWED, SKEWED_CF, DECODE,
-                           PREFILL_SWIGLU, DECODE_SWIGLU]}
+                           PREFILL_SWIGLU, DECODE_SWIGLU, PREFILL_K1]}
 
 
 def _gen(seed: int, tensor: str, part: int = 0) -> torch.Generator:

@@ -363,3 +363,44 @@ def test_forward_swiglu_decode_all_rows():
 
 def test_forward_swiglu_prefill_sampled():
     forward_parity(moe_synth.PREFILL_SWIGLU, stride=16)
+
+
+# ------------------------------------------- k = 1: combine fused into GEMM2 --
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_forward_k1_drops_zero_rows_written(act):
+    # y starts as NaN everywhere: dropped tokens must be written as 0 and
+    # kept tokens as w * expert output, with no combine kernel
+    cfg = moe_synth.MoEConfig("k1drop", T=300, H=136, F=264, E=8, k=1, seed=60,
+                              capacity_factor=0.5, bias0=2.0, act=act)
+    inputs = moe_synth.make_inputs(cfg)
+    dev_in = to_dev(inputs)
+    layer = moe.MoELayer(dev_in["w_router"], dev_in["w1"], dev_in["w2"], 1, bias=dev_in["bias"],
+                         capacity_factor=cfg.capacity_factor, act=act)
+    layer._ensure(cfg.T, dev_in["x"].device)
+    layer.y.view(torch.int16).fill_(0x7FC0)  # bf16 NaN
+    r = layer.routing
+    moe.moe_forward(layer.shape, dev_in["x"], layer.w_router, layer.bias, layer.w1, layer.w2, layer.y,
+                    r.ids, r.weights, r.counts, r.offsets, r.perm, r.slot, layer.ws)
+    assert moe.moe_get_device_status(layer.ws) == 0
+    y = layer.y
+    assert not torch.isnan(y).any()
+    dead = torch.from_numpy(np_(r.slot)[:, 0] < 0).to(DEV)
+    assert dead.any() and (~dead).any()
+    assert torch.all(y[dead] == 0)
+    logits, rep = routing_parity(cfg, inputs, r)
+    rows = np.arange(cfg.T, dtype=np.int32)
+    y_ref = reference_y(inputs, logits, np_(r.ids), np_(r.slot), rows)
+    check_y(y.float().cpu().numpy(), y_ref)
+
+
+def test_forward_k1_softmax_over_all_experts():
+    # the gate weight of the single expert is below 1 here, so a missing
+    # scale would show
+    cfg = moe_synth.MoEConfig("k1gate", T=200, H=256, F=384, E=16, k=1, seed=61)
+    rep = forward_parity(cfg, gating=moe.MOE_GATE_SOFTMAX_TOPK)
+    assert rep["dropped"] == 0
+
+
+def test_forward_k1_prefill_sampled():
+    forward_parity(moe_synth.PREFILL_K1, stride=16)

@@ -52,7 +52,9 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
     # with a capacity limit, so stale scratch from the first call would show
     cfgs = [moe_synth.DECODE,
             moe_synth.MoEConfig("small", T=96, H=256, F=384, E=16, k=4, seed=31,
-                                capacity_factor=0.8)]
+                                capacity_factor=0.8),
+            moe_synth.MoEConfig("top1", T=200, H=256, F=384, E=8, k=1, seed=32,
+                                capacity_factor=0.6)]
     for cfg in cfgs:
         s, inp, r, ws = _routed(cfg)
         y_ref = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=DEV)
