@@ -398,9 +398,11 @@ def run_ours(args):
     if moe.moe_get_device_status(layer.ws, stream) != 0:
         raise RuntimeError("device status set during warm-up")
 
-    # The timed steps replay a CUDA graph of R consecutive forward steps (the
-    # same six kernels per step, with the library's per-kernel events), so
-    # host launch overhead does not enter the device time.
+    # The timed steps replay a CUDA graph of R consecutive forward steps, so
+    # host launch overhead does not enter the device time.  A second graph of
+    # the same steps with the library's per-kernel events (which sit between
+    # the kernels and so turn off their overlapped launch) gives the
+    # per-kernel split; it is replayed after the timed region.
     R = max(1, min(args.steps, args.graph_steps))
     reps = max(1, args.steps // R)
     K = R * reps
@@ -411,9 +413,13 @@ def run_ours(args):
             e.record(stream)
     torch.cuda.synchronize(device)
     graph = torch.cuda.CUDAGraph()
+    graph_prof = torch.cuda.CUDAGraph()
     cap = torch.cuda.Stream(device)
     cap.wait_stream(stream)
     with torch.cuda.graph(graph, stream=cap):
+        for i in range(R):
+            step()
+    with torch.cuda.graph(graph_prof, stream=cap):
         for i in range(R):
             step(evs[i])
     torch.cuda.synchronize(device)
@@ -445,10 +451,17 @@ def run_ours(args):
     ms_per_step = elapsed_ms / K
     value = whole_job_throughput(cfg.T, world, K, elapsed_ms)
 
-    # per-kernel device time (averaged over the timed steps)
+    # per-kernel device time: mean over the R steps of the profiled graph's
+    # last replay (kernels run back to back, no overlapped launch), after as
+    # many replays as the timed region so both see the same sustained clocks
+    for _ in range(reps):
+        graph_prof.replay()
+    torch.cuda.synchronize(device)
+    if moe.moe_get_device_status(layer.ws, stream) != 0:
+        raise RuntimeError("device status set during the profiled replays")
     names = moe.KERNEL_NAMES
     per_kernel = {n: statistics.fmean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(R))
-                  for j, n in enumerate(names)}  # the last replay's R steps
+                  for j, n in enumerate(names)}
     counts = layer.routing.counts.cpu()
     n_rows = int(counts.sum().item())
     experts_hit = int((counts > 0).sum().item())
@@ -528,7 +541,10 @@ def run_ours(args):
         "config": {"workload": workload_desc(cfg), "tokens_per_gpu": cfg.T,
                    "parallelism": f"replicas x{world} (token data-parallel, no collective)",
                    "kept_rows": n_rows, "experts_hit": experts_hit,
-                   "timing": f"CUDA events around {reps} replays of a CUDA graph of {R} forward steps",
+                   "timing": f"CUDA events around {reps} replays of a CUDA graph of {R} forward steps; "
+                             "per-kernel times from a second graph of the same steps with "
+                             "events between the kernels",
+                   "per_kernel_sum_ms": round(sum(per_kernel.values()), 5),
                    "l2": "inputs larger than L2: every step streams all expert weights "
                          f"({2 * (3 if cfg.act == 'swiglu' else 2) * cfg.E * cfg.H * cfg.F / 1e9:.2f} GB)"},
         "gpu_launches": len(launched) * K,

@@ -251,7 +251,9 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
   da.perm = perm;
   da.slot = slot;
   da.status = status_ptr(ws);
-  e = launch_dispatch(da, st);
+  // the router precedes it on the stream: start early unless timing hooks
+  // sit between the two kernels
+  e = launch_dispatch(da, st, ev == nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "dispatch launch");
   return mark(ev, 2, st);
 }
@@ -259,8 +261,12 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
 int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const uint16_t* w1,
                         const uint16_t* w2, const float* weights, const int32_t* offsets,
                         const int32_t* perm, const int32_t* slot, uint16_t* y, void* ws,
-                        cudaStream_t st, void* const* ev = nullptr) {
+                        cudaStream_t st, void* const* ev = nullptr, bool chained = false) {
   int rc;
+  // Kernels after the first start early (programmatic dependent launch);
+  // the first one only when this library's dispatch kernel precedes it
+  // (`chained`).  With timing hooks, events sit between kernels: no overlap.
+  const bool pdl = ev == nullptr;
   const uint64_t rows = (uint64_t)s->T * s->k;
   uint16_t* h = h_ptr(ws, s);
   uint16_t* Y = y_ptr(ws, s);
@@ -286,7 +292,7 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   const bool fuse_combine = s->k == 1;
   pa.slot = slot;
   pa.y_zero = fuse_combine ? y : nullptr;
-  cudaError_t e = launch_permute(pa, sms, st);
+  cudaError_t e = launch_permute(pa, sms, st, pdl && chained);
   if (e != cudaSuccess) return cuda_fail(e, "permute launch");
   if ((rc = mark(ev, 3, st)) != MOE_OK) return rc;
 
@@ -307,7 +313,7 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   const int out_cols = swiglu ? kGemmBN / 2 : kGemmBN;  // h columns per pair tile
   int64_t ub = row_blocks_ub * ((s->F + out_cols - 1) / out_cols);
   e = launch_grouped_gemm(swiglu ? kGemmSwiGLU : kGemmGelu, tm_xp, tm_w1, g,
-                          (int)(ub < (1 << 30) ? ub : (1 << 30)), st);
+                          (int)(ub < (1 << 30) ? ub : (1 << 30)), st, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM1 launch");
   if ((rc = mark(ev, 4, st)) != MOE_OK) return rc;
 
@@ -316,7 +322,7 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   g.out = fuse_combine ? y : Y;
   ub = row_blocks_ub * ((s->H + kGemmBN - 1) / kGemmBN);
   e = launch_grouped_gemm(fuse_combine ? kGemmCombineK1 : kGemmPlain, tm_h, tm_w2, g,
-                          (int)(ub < (1 << 30) ? ub : (1 << 30)), st);
+                          (int)(ub < (1 << 30) ? ub : (1 << 30)), st, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM2 launch");
   if ((rc = mark(ev, 5, st)) != MOE_OK) return rc;
   if (fuse_combine) return mark(ev, 6, st);  // no combine kernel: the combine window is empty
@@ -329,7 +335,7 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   ca.H = s->H;
   ca.k = s->k;
   ca.y = y;
-  e = launch_combine(ca, st);
+  e = launch_combine(ca, st, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   return mark(ev, 6, st);
 }
@@ -465,7 +471,7 @@ int moe_dispatch(const moe_shape* s, const int32_t* ids, int32_t* counts, int32_
   da.perm = perm;
   da.slot = slot;
   da.status = status_ptr(ws);
-  e = launch_dispatch(da, st);
+  e = launch_dispatch(da, st, /*pdl=*/true);  // follows the histogram kernel
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "dispatch launch");
 }
 
@@ -563,7 +569,8 @@ int moe_forward_profiled(const moe_shape* s, const uint16_t* x, const uint16_t* 
   rc = enqueue_route(s, sms, x, w_router, b_router, ids, weights, counts, offsets, perm, slot, ws, st,
                      events);
   if (rc != MOE_OK) return rc;
-  return enqueue_ffn_combine(s, sms, x, w1, w2, weights, offsets, perm, slot, y, ws, st, events);
+  return enqueue_ffn_combine(s, sms, x, w1, w2, weights, offsets, perm, slot, y, ws, st, events,
+                             /*chained=*/true);
 }
 
 int moe_get_device_status(void* ws, void* stream, int32_t* status) {

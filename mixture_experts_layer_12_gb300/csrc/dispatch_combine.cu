@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(DTHREADS, 1) dispatch_kernel(const DispatchArg
   const int Tk = a.T * a.k;
   const int i0 = seg * a.seg_tokens * a.k;
   const int n = min(a.seg_tokens * a.k, Tk - i0);
+  pdl_launch_dependents();
+  pdl_wait();
 
   for (int e = tid; e < E; e += DTHREADS) {
     s_base[e] = a.base[(size_t)seg * E + e];
@@ -96,6 +98,8 @@ constexpr int CTHREADS = 128;
 // y[t, c..c+7] = sum_j w[t,j] * Y[slot[t,j], c..c+7]; one thread per
 // 8 columns (16-byte loads and stores), grid (T, H / 1024 columns).
 __global__ void __launch_bounds__(CTHREADS) combine_kernel(const CombineArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int t = blockIdx.x;
   const int col = (blockIdx.y * CTHREADS + threadIdx.x) * 8;
   if (col >= a.H) return;
@@ -130,6 +134,8 @@ __global__ void __launch_bounds__(CTHREADS) combine_kernel(const CombineArgs a) 
 // is HBM/L2-bandwidth bound (2 H bytes read + 2 H bytes written per row).
 constexpr int PTHREADS = 256;
 __global__ void __launch_bounds__(PTHREADS) permute_kernel(const PermuteArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int rows = a.T * a.k;
   const int kept = min(max(__ldg(a.offsets + a.E), 0), rows);
   const int vec = a.H / 8;  // 16-byte chunks per row (H % 8 == 0)
@@ -199,27 +205,40 @@ cudaError_t dispatch_combine_set_attributes() {
   return e;
 }
 
-cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st) {
-  const int nseg = (a.T + a.seg_tokens - 1) / a.seg_tokens;
-  dispatch_kernel<<<nseg, DTHREADS, 0, st>>>(a);
-  return cudaGetLastError();
+// Plain 1-D launch, optionally with programmatic serialization (pdl).
+template <typename Kernel, typename Args>
+cudaError_t launch_1d(Kernel k, dim3 grid, int threads, cudaStream_t st, bool pdl, const Args& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    set_pdl_attr(attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, k, a);
 }
 
-cudaError_t launch_permute(const PermuteArgs& a, int sms, cudaStream_t st) {
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st, bool pdl) {
+  const int nseg = (a.T + a.seg_tokens - 1) / a.seg_tokens;
+  return launch_1d(dispatch_kernel, dim3((unsigned)nseg), DTHREADS, st, pdl, a);
+}
+
+cudaError_t launch_permute(const PermuteArgs& a, int sms, cudaStream_t st, bool pdl) {
   const int64_t rows = (int64_t)a.T * a.k;
   const int64_t want = (rows + PTHREADS / 32 - 1) / (PTHREADS / 32);  // one row per warp
   const int64_t cap = (int64_t)(sms > 0 ? sms : 1) * (2048 / PTHREADS);
   const unsigned grid = (unsigned)(want < cap ? want : cap);
   if (grid == 0) return cudaSuccess;
-  permute_kernel<<<grid, PTHREADS, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_1d(permute_kernel, dim3(grid), PTHREADS, st, pdl, a);
 }
 
-cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st) {
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st, bool pdl) {
   const int cols_per_block = CTHREADS * 8;
   dim3 grid((unsigned)a.T, (unsigned)((a.H + cols_per_block - 1) / cols_per_block), 1);
-  combine_kernel<<<grid, CTHREADS, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_1d(combine_kernel, grid, CTHREADS, st, pdl, a);
 }
 
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st) {

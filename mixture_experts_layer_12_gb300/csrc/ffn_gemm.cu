@@ -149,6 +149,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_pairs = gridDim.x >> 1;
   const int NB = (p.N + BN_OUT - 1) / BN_OUT;
   const int KB = (p.K + BK - 1) / BK;
+  pdl_launch_dependents();
+  pdl_wait();  // offsets, A rows and the output buffers belong to earlier kernels
 
   // ---- tile schedule from the dispatch offsets (warp 0), barriers (warp 1)
   if (warp == 0) {
@@ -422,19 +424,20 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 template <int MODE>
 cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const GemmArgs& a,
-                        int pairs, cudaStream_t st) {
+                        int pairs, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  if (pdl) set_pdl_attr(attr[1]);
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, tm_a, tm_b, a);
 }
 
@@ -471,7 +474,7 @@ cudaError_t query_max_pairs(int dev, int* out) {
 size_t grouped_gemm_smem_bytes() { return SMEM_BYTES; }
 
 cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
-                                const GemmArgs& a, int max_tiles, cudaStream_t st) {
+                                const GemmArgs& a, int max_tiles, cudaStream_t st, bool pdl) {
   if (max_tiles <= 0) return cudaSuccess;
   int dev = 0, pairs = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -479,10 +482,10 @@ cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tm_a, const CUtenso
   if ((e = query_max_pairs(dev, &pairs)) != cudaSuccess) return e;
   if (pairs > max_tiles) pairs = max_tiles;
   switch (mode) {
-    case kGemmGelu: return launch_pair<kGemmGelu>(tm_a, tm_b, a, pairs, st);
-    case kGemmSwiGLU: return launch_pair<kGemmSwiGLU>(tm_a, tm_b, a, pairs, st);
-    case kGemmCombineK1: return launch_pair<kGemmCombineK1>(tm_a, tm_b, a, pairs, st);
-    default: return launch_pair<kGemmPlain>(tm_a, tm_b, a, pairs, st);
+    case kGemmGelu: return launch_pair<kGemmGelu>(tm_a, tm_b, a, pairs, st, pdl);
+    case kGemmSwiGLU: return launch_pair<kGemmSwiGLU>(tm_a, tm_b, a, pairs, st, pdl);
+    case kGemmCombineK1: return launch_pair<kGemmCombineK1>(tm_a, tm_b, a, pairs, st, pdl);
+    default: return launch_pair<kGemmPlain>(tm_a, tm_b, a, pairs, st, pdl);
   }
 }
 

@@ -75,7 +75,7 @@ struct DispatchArgs {
   int32_t *perm, *slot;
   int* status;
 };
-cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st);
+cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st, bool pdl);
 
 // ---- grouped expert GEMM (tcgen05 + TMA, persistent ragged scheduler).
 struct GemmArgs {
@@ -100,8 +100,10 @@ constexpr int kGemmPlain = 0;   // GEMM2: no activation
 constexpr int kGemmGelu = 1;    // GEMM1: GELU epilogue
 constexpr int kGemmSwiGLU = 2;  // GEMM1: SiLU(gate) * up epilogue
 constexpr int kGemmCombineK1 = 3;  // GEMM2 + combine for k = 1: y[perm[r]] = w * acc
+// pdl: launched with programmatic serialization (the predecessor on the
+// stream is this library's kernel of the same call)
 cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
-                                const GemmArgs& a, int max_tiles, cudaStream_t st);
+                                const GemmArgs& a, int max_tiles, cudaStream_t st, bool pdl);
 size_t grouped_gemm_smem_bytes();
 constexpr int kGemmBM = 128;  // rows per CTA; a CTA pair covers 256
 constexpr int kGemmBN = 256;
@@ -120,7 +122,7 @@ struct PermuteArgs {
   const int32_t* slot;
   uint16_t* y_zero;
 };
-cudaError_t launch_permute(const PermuteArgs& a, int sms, cudaStream_t st);
+cudaError_t launch_permute(const PermuteArgs& a, int sms, cudaStream_t st, bool pdl);
 
 // ---- combine: y[t] = sum_j w[t,j] * Y[slot[t,j]] (fp32), bf16 out.
 struct CombineArgs {
@@ -130,7 +132,7 @@ struct CombineArgs {
   int T, H, k;
   uint16_t* y;
 };
-cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st, bool pdl);
 
 // ---- bounded-wait self test.
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st);

@@ -213,6 +213,8 @@ __global__ void __launch_bounds__(RTHREADS)
   const int KB = (a.H + RBK - 1) / RBK;
   const int kb0 = (int)(((long long)KB * s) / S);
   const int kb1 = (int)(((long long)KB * (s + 1)) / S);
+  pdl_launch_dependents();  // the dispatch kernel may be scheduled now; it waits for us
+  pdl_wait();               // no-op: launched with full serialization
   const int nkb = kb1 - kb0;
 
   if (threadIdx.x == 0) {
@@ -521,6 +523,8 @@ __global__ void __launch_bounds__(HTHREADS) histogram_kernel(const HistArgs a) {
   __shared__ int s_part[HTHREADS];
   __shared__ int s_tot[kMaxExperts];
   __shared__ int s_last;
+  pdl_launch_dependents();
+  pdl_wait();  // no-op: launched with full serialization
   for (int e = threadIdx.x; e < a.E; e += HTHREADS) s_hist[e] = 0;
   __syncthreads();
   const int n = min(a.seg_tokens, a.T - (int)blockIdx.x * a.seg_tokens) * a.k;

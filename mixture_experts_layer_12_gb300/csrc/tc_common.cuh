@@ -37,6 +37,24 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 }
 
 // Makes mbarrier initialisation visible to the async proxy and the cluster.
+// Programmatic dependent launch.  launch_dependents lets the next kernel on
+// the stream (if it was launched with programmatic serialization) start its
+// CTAs early; wait blocks until every prerequisite grid has completed and
+// its memory is visible.  Every kernel here calls both before its first
+// global-memory access, so an early start only hides launch latency.  Both
+// are no-ops when there is no such dependency.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch attribute for a kernel whose predecessor on the stream is one of
+// this library's kernels of the same call (never the caller's work).
+inline void set_pdl_attr(cudaLaunchAttribute& at) {
+  at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at.val.programmaticStreamSerializationAllowed = 1;
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

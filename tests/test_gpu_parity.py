@@ -283,6 +283,38 @@ def test_split_entry_points_match_forward():
         assert torch.equal(a, b)
 
 
+def test_back_to_back_steps_with_overlapped_launch():
+    # consecutive forwards share the routing buffers and the workspace; the
+    # kernels after the first of each call start early (programmatic
+    # dependent launch), so alternate two inputs into two outputs inside one
+    # graph and compare each with a lone eager call
+    cfg = moe_synth.MoEConfig("chain", T=384, H=256, F=512, E=16, k=2, seed=26)
+    dev_in = to_dev(moe_synth.make_inputs(cfg))
+    xb = torch.roll(dev_in["x"], 7, dims=0) * -0.5
+    layer, _ = gpu_forward(cfg, dev_in)
+    r = layer.routing
+    ys = [torch.empty_like(layer.y) for _ in range(2)]
+    refs = []
+    for x in (dev_in["x"], xb):
+        moe.moe_forward(layer.shape, x, layer.w_router, layer.bias, layer.w1, layer.w2, layer.y,
+                        r.ids, r.weights, r.counts, r.offsets, r.perm, r.slot, layer.ws)
+        refs.append(layer.y.clone())
+    assert not torch.equal(refs[0], refs[1])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream()):
+        for i in range(12):
+            moe.moe_forward(layer.shape, (dev_in["x"], xb)[i % 2], layer.w_router, layer.bias,
+                            layer.w1, layer.w2, ys[i % 2], r.ids, r.weights, r.counts, r.offsets,
+                            r.perm, r.slot, layer.ws)
+    for _ in range(3):
+        ys[0].zero_()
+        ys[1].zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert moe.moe_get_device_status(layer.ws) == 0
+        assert torch.equal(ys[0], refs[0]) and torch.equal(ys[1], refs[1])
+
+
 def test_profiled_forward_eager_and_captured():
     cfg = moe_synth.MoEConfig("prof", T=256, H=128, F=256, E=8, k=2, seed=25)
     dev_in = to_dev(moe_synth.make_inputs(cfg))
