@@ -39,10 +39,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # one ncu capture, keyed by workload/kernel and by the sha256 of the kernel
 # source it was taken on; reported as null once the source changes.
 NCU_TRAFFIC = {
-    # prefill workload, `ncu --set full` (profiles/expert_gemm_prefill.md, profiles/router_prefill.md)
-    "prefill/expert_gemm1": {"bytes": 1025576e3 + 222542592, "src": "ffn_gemm.cu", "src_sha": "7c00d930c3d66624"},
-    "prefill/expert_gemm2": {"bytes": 1434461e3 + 66115328, "src": "ffn_gemm.cu", "src_sha": "7c00d930c3d66624"},
-    "prefill/router": {"bytes": 33683200, "src": "router.cu", "src_sha": "cbbe0469d985a570"},
+    # prefill workload, `ncu --set full` (profiles/expert_gemm_prefill.md, profiles/router_prefill.md):
+    # dram__bytes_read.sum + dram__bytes_write.sum of one launch
+    "prefill/expert_gemm1": {"bytes": 1037565e3 + 221870336, "src": "ffn_gemm.cu", "src_sha": "59cca3f2c56b3306"},
+    "prefill/expert_gemm2": {"bytes": 1592799e3 + 66000640, "src": "ffn_gemm.cu", "src_sha": "59cca3f2c56b3306"},
+    "prefill/router": {"bytes": 33692416, "src": "router.cu", "src_sha": "0fe9ac7818d6ca7e"},
 }
 
 
@@ -331,6 +332,31 @@ def run_route_only(args, cfg, device):
         raise RuntimeError("device status set during the timed region")
     elapsed = ev[0].elapsed_time(ev[1])
     ms = elapsed / K
+    # end to end through the public API with host buffers: H2D of x, the
+    # routing, D2H of ids and gate weights, every step, inside the timed region
+    E2E = max(1, min(args.e2e_steps, K))
+    x_host = inputs["x"].pin_memory()
+    ids_host = torch.empty(cfg.T, cfg.k, dtype=torch.int32).pin_memory()
+    w_host = torch.empty(cfg.T, cfg.k, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty_like(x0)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    for i in range(3 + E2E):
+        if i == 3:
+            torch.cuda.synchronize(device)
+            e0.record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        moe.moe_route(s, x_dev, wr, None, r.ids, r.weights, r.counts, r.offsets, r.perm, r.slot,
+                      ws, stream)
+        ids_host.copy_(r.ids, non_blocking=True)
+        w_host.copy_(r.weights, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = e0.elapsed_time(e1)
+    e2e = {"value": cfg.T * E2E / (e2e_ms * 1e-3), "unit": UNIT,
+           "h2d_bytes_per_step": cfg.T * cfg.H * 2, "d2h_bytes_per_step": cfg.T * cfg.k * 8,
+           "steps": E2E}
+
     peaks, src = load_peaks()
     w = kernel_work(cfg, cfg.T * cfg.k, 0)
     route_bytes = w["router"]["bytes"] + w["dispatch"]["bytes"]
@@ -347,6 +373,7 @@ def run_route_only(args, cfg, device):
                      "peak_kind": f"HBM copy ({src})", "kernel": "router+dispatch",
                      "bytes_per_launch": route_bytes, "traffic": None},
         "clocks": clk,
+        "e2e": e2e,
     }
     print(json.dumps(line), flush=True)
     return 0

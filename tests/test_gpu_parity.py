@@ -147,6 +147,18 @@ def test_router_sweep_full_size(k):
     print(cfg.name, rep)
 
 
+@pytest.mark.parametrize("cf", [None, 0.9])
+def test_router_more_tiles_than_one_wave(cf):
+    # 313 tiles of 128 tokens: more router clusters than fit on the GPU at
+    # once, and 313 segments for the scan of the per-tile counts
+    cfg = moe_synth.MoEConfig("wide", T=40000, H=256, F=0, E=8, k=2, seed=27, capacity_factor=cf)
+    inputs = moe_synth.make_inputs(cfg, with_ffn=False)
+    r = gpu_route(cfg, to_dev(inputs))
+    _, rep = routing_parity(cfg, inputs, r)
+    if cf is not None:
+        assert rep["dropped"] > 0
+
+
 @pytest.mark.parametrize("T,H,E,k,bias", [(1, 64, 8, 1, None), (130, 200, 16, 3, 0.5),
                                           (257, 520, 256, 8, None), (64, 4096, 40, 5, 2.0),
                                           (300, 72, 192, 2, None)])
