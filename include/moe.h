@@ -139,7 +139,8 @@ MOE_API int64_t moe_expert_capacity(const moe_shape* s);
  * enough for every other entry point): a 1 KB status block, per-128-token
  * expert counts [ceil(T/128), E] int32, h [T*k, F] bf16 and a [T*k, H]
  * bf16 region that holds first the token rows in dispatch order, then the
- * expert outputs.  Returns 0 for an invalid shape. */
+ * expert outputs.  Returns 0 for an invalid shape (E may be any 1..256
+ * here, as moe_expert_ffn allows). */
 MOE_API size_t moe_workspace_size(const moe_shape* s);
 
 /* Workspace bytes needed by moe_route and moe_dispatch (status block and
@@ -197,6 +198,53 @@ MOE_API int moe_expert_ffn_combine(const moe_shape* s, const uint16_t* x, const 
                            const uint16_t* w2, const float* weights, const int32_t* offsets,
                            const int32_t* perm, const int32_t* slot, uint16_t* y, void* ws,
                            size_t ws_bytes, void* stream);
+
+/*
+ * The steps of moe_expert_ffn_combine one at a time, for callers that move
+ * rows between the steps themselves -- e.g. expert parallelism, where each
+ * GPU holds some of the experts and the dispatched rows travel to their
+ * expert's GPU and back (the article's section 3 all-to-all).
+ *
+ * moe_dispatch_rows: the dispatch step's regrouped tokens x_i of section
+ * "MoE的计算流程" (step 3): xp[r] = x[perm[r] / k] for r < offsets[E], in
+ * dispatch order (expert-major); rows of xp past offsets[E] are not written.
+ *   x [T, H] bf16, perm / offsets as produced by moe_route, xp [T*k, H] bf16.
+ * Uses no workspace; perm entries outside [0, T*k) are clamped, never
+ * dereferenced.
+ */
+MOE_API int moe_dispatch_rows(const moe_shape* s, const uint16_t* x, const int32_t* perm,
+                              const int32_t* offsets, uint16_t* xp, void* stream);
+
+/*
+ * moe_expert_ffn: step 4 (listing "Expert计算") on rows already grouped:
+ * rows [seg_offsets[i], seg_offsets[i+1]) of xp form segment i, computed by
+ * expert i % E:  Y[r] = act(xp[r] · W1[e]) · W2[e]  (GELU, or SwiGLU with
+ * W1 = [W_gate | W_up]), h and Y rounded to bf16.
+ *   s: H, F, E (the experts whose weights W1 / W2 hold; any 1..256, the
+ *     router's E % 8 rule does not apply), expert_act; T*k is the row
+ *     capacity of xp and Y (e.g. T = rows, k = 1); gating is ignored.
+ *   n_segments: 1..256; seg_offsets [n_segments+1] int32 (device), non-
+ *     decreasing, seg_offsets[n_segments] <= T*k (not re-validated).
+ *   xp [T*k, H] bf16, W1 [E, H, F] (or [E, H, 2F]), W2 [E, F, H], Y [T*k, H]
+ *   bf16 (rows outside every segment are not written).
+ * With E experts per GPU and rows received from G sources, each source's
+ * rows grouped by expert, n_segments = G * E and segment i = (source i / E,
+ * expert i % E): the received buffer is used as it arrives.
+ * ws as for moe_expert_ffn_combine (moe_workspace_size of the same s).
+ */
+MOE_API int moe_expert_ffn(const moe_shape* s, int32_t n_segments, const uint16_t* xp,
+                           const uint16_t* w1, const uint16_t* w2, const int32_t* seg_offsets,
+                           uint16_t* Y, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_combine: step 5 (listing "Scatter + 加权", written as a gather):
+ * y[t] = sum over j with slot[t,j] >= 0 of weights[t,j] * Y[slot[t,j]],
+ * fp32 in slot order, rounded to bf16; 0 when every slot was dropped.
+ *   Y [T*k, H] bf16 in dispatch order, weights [T, k] fp32, slot [T, k]
+ *   int32 as produced by moe_route, y [T, H] bf16.  No workspace.
+ */
+MOE_API int moe_combine(const moe_shape* s, const uint16_t* Y, const float* weights,
+                        const int32_t* slot, uint16_t* y, void* stream);
 
 /*
  * The whole layer (the op "MoEFusion::Compute(x, w_router, expert_weights,

@@ -38,7 +38,8 @@ MOE_WS_MIN_BYTES = 256
 EXPORTS = ("moe_version", "moe_last_error_string", "moe_expert_capacity", "moe_workspace_size",
            "moe_route", "moe_dispatch", "moe_expert_ffn_combine", "moe_forward",
            "moe_get_device_status", "moe_selftest_wait_timeout", "moe_forward_profiled",
-           "moe_expert_ffn_combine_noalloc", "moe_route_workspace_size")
+           "moe_expert_ffn_combine_noalloc", "moe_route_workspace_size", "moe_dispatch_rows",
+           "moe_expert_ffn", "moe_combine")
 MOE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -101,6 +102,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "moe_forward_profiled": ([S, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P],
                                      ctypes.c_int),
             "moe_expert_ffn_combine_noalloc": ([S, P, P, P, P, P, P, P, P, P], ctypes.c_int),
+            "moe_dispatch_rows": ([S, P, P, P, P, P], ctypes.c_int),
+            "moe_expert_ffn": ([S, ctypes.c_int32, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
+            "moe_combine": ([S, P, P, P, P, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -188,6 +192,31 @@ def moe_expert_ffn_combine(shape, x, w1, w2, weights, offsets, perm, slot, y, ws
         _ptr(weights, f32, "weights"), _ptr(offsets, i32, "offsets"), _ptr(perm, i32, "perm"),
         _ptr(slot, i32, "slot"), _ptr(y, bf, "y"), _ptr(ws, None, "ws"),
         ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_dispatch_rows(shape, x, perm, offsets, xp, stream=None):
+    """xp[r] = x[perm[r] // k] for the kept rows, in dispatch order."""
+    bf, i32 = torch.bfloat16, torch.int32
+    _check(load_library().moe_dispatch_rows(
+        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(perm, i32, "perm"),
+        _ptr(offsets, i32, "offsets"), _ptr(xp, bf, "xp"), _stream(stream)))
+
+
+def moe_expert_ffn(shape, n_segments, xp, w1, w2, seg_offsets, Y, ws, stream=None):
+    """Expert FFN on rows grouped in segments; segment i uses expert i % E."""
+    bf, i32 = torch.bfloat16, torch.int32
+    _check(load_library().moe_expert_ffn(
+        ctypes.byref(shape), int(n_segments), _ptr(xp, bf, "xp"), _ptr(w1, bf, "w1"),
+        _ptr(w2, bf, "w2"), _ptr(seg_offsets, i32, "seg_offsets"), _ptr(Y, bf, "Y"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_combine(shape, Y, weights, slot, y, stream=None):
+    """y[t] = sum_j weights[t, j] * Y[slot[t, j]] over the kept slots."""
+    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+    _check(load_library().moe_combine(
+        ctypes.byref(shape), _ptr(Y, bf, "Y"), _ptr(weights, f32, "weights"),
+        _ptr(slot, i32, "slot"), _ptr(y, bf, "y"), _stream(stream)))
 
 
 def moe_expert_ffn_combine_noalloc(shape, x, w1, w2, weights, offsets, perm, slot, y, stream=None):

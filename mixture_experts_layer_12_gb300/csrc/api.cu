@@ -112,10 +112,14 @@ int map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int check_shape(const moe_shape* s, bool need_ffn) {
+// experts_only: the shape describes only experts' weights (moe_expert_ffn),
+// so the router's E % 8 == 0 does not apply.
+int check_shape(const moe_shape* s, bool need_ffn, bool experts_only = false) {
   if (!s) return fail(MOE_ERR_INVALID_ARG, "shape is null");
   if (s->T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d < 0", s->T);
-  if (s->E < 1 || s->E > kMaxExperts || s->E % 8 != 0)
+  if (experts_only && (s->E < 1 || s->E > kMaxExperts))
+    return fail(MOE_ERR_UNSUPPORTED, "E = %d: need 1 <= E <= %d", s->E, kMaxExperts);
+  if (!experts_only && (s->E < 1 || s->E > kMaxExperts || s->E % 8 != 0))
     return fail(MOE_ERR_UNSUPPORTED, "E = %d: need 8 <= E <= %d and E %% 8 == 0", s->E, kMaxExperts);
   if (s->k < 1 || s->k > kMaxTopK || s->k > s->E)
     return fail(MOE_ERR_UNSUPPORTED, "k = %d: need 1 <= k <= min(8, E)", s->k);
@@ -258,6 +262,57 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
   return mark(ev, 2, st);
 }
 
+// GEMM1 (+ activation) into h, then GEMM2 into `out`, over T*k rows grouped
+// in n_seg segments: segment i (rows [seg_offsets[i], seg_offsets[i+1]))
+// uses expert i % s->E.  combine_k1: GEMM2 writes y[perm[r]] = w * acc.
+// pdl_first: GEMM1 follows this library's kernel of the same call.
+int enqueue_expert_gemms(const moe_shape* s, int n_seg, const uint16_t* xp, const uint16_t* w1,
+                         const uint16_t* w2, const int32_t* seg_offsets, uint16_t* h,
+                         uint16_t* out, bool combine_k1, const int32_t* perm,
+                         const float* weights, int* status, cudaStream_t st, bool pdl_first,
+                         bool pdl, void* const* ev, int ev_gemm1, int ev_gemm2) {
+  int rc;
+  const uint64_t rows = (uint64_t)s->T * s->k;
+  CUtensorMap tm_xp, tm_w1, tm_h, tm_w2;
+  const bool swiglu = s->expert_act == MOE_EXPERT_SWIGLU;
+  const uint64_t w1_cols = (uint64_t)s->F * (swiglu ? 2 : 1);  // SwiGLU: [W_gate | W_up]
+  if ((rc = map_2d(&tm_xp, xp, (uint64_t)s->H, rows, 64, 128, "xp")) != MOE_OK) return rc;
+  if ((rc = map_3d(&tm_w1, w1, w1_cols, (uint64_t)s->H, (uint64_t)s->E, 64, 64, "W1")) != MOE_OK) return rc;
+  if ((rc = map_2d(&tm_h, h, (uint64_t)s->F, rows, 64, 128, "h")) != MOE_OK) return rc;
+  if ((rc = map_3d(&tm_w2, w2, (uint64_t)s->H, (uint64_t)s->F, (uint64_t)s->E, 64, 64, "W2")) != MOE_OK) return rc;
+
+  // pair tiles are 2*kGemmBM rows: a segment with n rows owns ceil(n / 256)
+  const int64_t row_blocks_ub = ((int64_t)rows + 2 * kGemmBM - 1) / (2 * kGemmBM) + n_seg;
+  GemmArgs g;
+  g.offsets = seg_offsets;
+  g.E = n_seg;
+  g.E_w = s->E;
+  g.perm = perm;
+  g.gate_w = weights;
+  g.T = s->T;
+  g.status = status;
+  g.wait_limit_ns = kWaitLimitNs;
+
+  g.N = s->F;
+  g.K = s->H;
+  g.out = h;
+  const int out_cols = swiglu ? kGemmBN / 2 : kGemmBN;  // h columns per pair tile
+  int64_t ub = row_blocks_ub * ((s->F + out_cols - 1) / out_cols);
+  cudaError_t e = launch_grouped_gemm(swiglu ? kGemmSwiGLU : kGemmGelu, tm_xp, tm_w1, g,
+                                      (int)(ub < (1 << 30) ? ub : (1 << 30)), st, pdl_first);
+  if (e != cudaSuccess) return cuda_fail(e, "expert GEMM1 launch");
+  if ((rc = mark(ev, ev_gemm1, st)) != MOE_OK) return rc;
+
+  g.N = s->H;
+  g.K = s->F;
+  g.out = out;
+  ub = row_blocks_ub * ((s->H + kGemmBN - 1) / kGemmBN);
+  e = launch_grouped_gemm(combine_k1 ? kGemmCombineK1 : kGemmPlain, tm_h, tm_w2, g,
+                          (int)(ub < (1 << 30) ? ub : (1 << 30)), st, pdl);
+  if (e != cudaSuccess) return cuda_fail(e, "expert GEMM2 launch");
+  return mark(ev, ev_gemm2, st);
+}
+
 int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const uint16_t* w1,
                         const uint16_t* w2, const float* weights, const int32_t* offsets,
                         const int32_t* perm, const int32_t* slot, uint16_t* y, void* ws,
@@ -267,17 +322,9 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   // the first one only when this library's dispatch kernel precedes it
   // (`chained`).  With timing hooks, events sit between kernels: no overlap.
   const bool pdl = ev == nullptr;
-  const uint64_t rows = (uint64_t)s->T * s->k;
   uint16_t* h = h_ptr(ws, s);
   uint16_t* Y = y_ptr(ws, s);
   uint16_t* xp = Y;  // the permuted tokens live where GEMM2 later writes Y
-  CUtensorMap tm_xp, tm_w1, tm_h, tm_w2;
-  const bool swiglu = s->expert_act == MOE_EXPERT_SWIGLU;
-  const uint64_t w1_cols = (uint64_t)s->F * (swiglu ? 2 : 1);  // SwiGLU: [W_gate | W_up]
-  if ((rc = map_2d(&tm_xp, xp, (uint64_t)s->H, rows, 64, 128, "xp")) != MOE_OK) return rc;
-  if ((rc = map_3d(&tm_w1, w1, w1_cols, (uint64_t)s->H, (uint64_t)s->E, 64, 64, "W1")) != MOE_OK) return rc;
-  if ((rc = map_2d(&tm_h, h, (uint64_t)s->F, rows, 64, 128, "h")) != MOE_OK) return rc;
-  if ((rc = map_3d(&tm_w2, w2, (uint64_t)s->H, (uint64_t)s->F, (uint64_t)s->E, 64, 64, "W2")) != MOE_OK) return rc;
 
   PermuteArgs pa;
   pa.x = x;
@@ -296,35 +343,10 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   if (e != cudaSuccess) return cuda_fail(e, "permute launch");
   if ((rc = mark(ev, 3, st)) != MOE_OK) return rc;
 
-  // pair tiles are 2*kGemmBM rows: an expert with n rows owns ceil(n / 256)
-  const int64_t row_blocks_ub = ((int64_t)rows + 2 * kGemmBM - 1) / (2 * kGemmBM) + s->E;
-  GemmArgs g;
-  g.offsets = offsets;
-  g.E = s->E;
-  g.perm = perm;
-  g.gate_w = weights;
-  g.T = s->T;
-  g.status = status_ptr(ws);
-  g.wait_limit_ns = kWaitLimitNs;
-
-  g.N = s->F;
-  g.K = s->H;
-  g.out = h;
-  const int out_cols = swiglu ? kGemmBN / 2 : kGemmBN;  // h columns per pair tile
-  int64_t ub = row_blocks_ub * ((s->F + out_cols - 1) / out_cols);
-  e = launch_grouped_gemm(swiglu ? kGemmSwiGLU : kGemmGelu, tm_xp, tm_w1, g,
-                          (int)(ub < (1 << 30) ? ub : (1 << 30)), st, pdl);
-  if (e != cudaSuccess) return cuda_fail(e, "expert GEMM1 launch");
-  if ((rc = mark(ev, 4, st)) != MOE_OK) return rc;
-
-  g.N = s->H;
-  g.K = s->F;
-  g.out = fuse_combine ? y : Y;
-  ub = row_blocks_ub * ((s->H + kGemmBN - 1) / kGemmBN);
-  e = launch_grouped_gemm(fuse_combine ? kGemmCombineK1 : kGemmPlain, tm_h, tm_w2, g,
-                          (int)(ub < (1 << 30) ? ub : (1 << 30)), st, pdl);
-  if (e != cudaSuccess) return cuda_fail(e, "expert GEMM2 launch");
-  if ((rc = mark(ev, 5, st)) != MOE_OK) return rc;
+  if ((rc = enqueue_expert_gemms(s, s->E, xp, w1, w2, offsets, h, fuse_combine ? y : Y,
+                                 fuse_combine, perm, weights, status_ptr(ws), st, pdl, pdl, ev, 4,
+                                 5)) != MOE_OK)
+    return rc;
   if (fuse_combine) return mark(ev, 6, st);  // no combine kernel: the combine window is empty
 
   CombineArgs ca;
@@ -391,7 +413,7 @@ int64_t moe_expert_capacity(const moe_shape* s) {
 }
 
 size_t moe_workspace_size(const moe_shape* s) {
-  if (check_shape(s, true) != MOE_OK) return 0;
+  if (check_shape(s, true, /*experts_only=*/true) != MOE_OK) return 0;
   return ws_bytes_for(s);
 }
 
@@ -498,6 +520,81 @@ int moe_expert_ffn_combine(const moe_shape* s, const uint16_t* x, const uint16_t
   REQUIRE_PTR(slot);
   REQUIRE_PTR(y);
   return enqueue_ffn_combine(s, sms, x, w1, w2, weights, offsets, perm, slot, y, ws, st);
+}
+
+int moe_dispatch_rows(const moe_shape* s, const uint16_t* x, const int32_t* perm,
+                      const int32_t* offsets, uint16_t* xp, void* stream) {
+  int rc = check_shape(s, false);
+  if (rc != MOE_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int sms = 0;
+  if ((rc = device_setup(&sms)) != MOE_OK) return rc;
+  if (s->T == 0) return MOE_OK;
+  REQUIRE_PTR(x);
+  REQUIRE_PTR(perm);
+  REQUIRE_PTR(offsets);
+  REQUIRE_PTR(xp);
+  PermuteArgs pa;
+  pa.x = x;
+  pa.perm = perm;
+  pa.offsets = offsets;
+  pa.T = s->T;
+  pa.H = s->H;
+  pa.k = s->k;
+  pa.E = s->E;
+  pa.xp = xp;
+  pa.slot = nullptr;
+  pa.y_zero = nullptr;
+  cudaError_t e = launch_permute(pa, sms, st, /*pdl=*/false);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "permute launch");
+}
+
+int moe_expert_ffn(const moe_shape* s, int32_t n_segments, const uint16_t* xp, const uint16_t* w1,
+                   const uint16_t* w2, const int32_t* seg_offsets, uint16_t* Y, void* ws,
+                   size_t ws_bytes, void* stream) {
+  int rc = check_shape(s, true, /*experts_only=*/true);
+  if (rc != MOE_OK) return rc;
+  if (n_segments < 1 || n_segments > kMaxExperts)
+    return fail(MOE_ERR_INVALID_ARG, "n_segments = %d, must be 1..%d", n_segments, kMaxExperts);
+  REQUIRE_PTR(ws);
+  if (ws_bytes < ws_bytes_for(s))
+    return fail(MOE_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed", ws_bytes, ws_bytes_for(s));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int sms = 0;
+  if ((rc = device_setup(&sms)) != MOE_OK) return rc;
+  if ((rc = clear_status(ws, st)) != MOE_OK) return rc;
+  if (s->T == 0) return MOE_OK;
+  REQUIRE_PTR(xp);
+  REQUIRE_PTR(w1);
+  REQUIRE_PTR(w2);
+  REQUIRE_PTR(seg_offsets);
+  REQUIRE_PTR(Y);
+  return enqueue_expert_gemms(s, n_segments, xp, w1, w2, seg_offsets, h_ptr(ws, s), Y, false,
+                              nullptr, nullptr, status_ptr(ws), st, false, true, nullptr, 0, 0);
+}
+
+int moe_combine(const moe_shape* s, const uint16_t* Y, const float* weights, const int32_t* slot,
+                uint16_t* y, void* stream) {
+  int rc = check_shape(s, false);
+  if (rc != MOE_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int sms = 0;
+  if ((rc = device_setup(&sms)) != MOE_OK) return rc;
+  if (s->T == 0) return MOE_OK;
+  REQUIRE_PTR(Y);
+  REQUIRE_PTR(weights);
+  REQUIRE_PTR(slot);
+  REQUIRE_PTR(y);
+  CombineArgs ca;
+  ca.Y = Y;
+  ca.w = weights;
+  ca.slot = slot;
+  ca.T = s->T;
+  ca.H = s->H;
+  ca.k = s->k;
+  ca.y = y;
+  cudaError_t e = launch_combine(ca, st, /*pdl=*/false);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine launch");
 }
 
 int moe_expert_ffn_combine_noalloc(const moe_shape* s, const uint16_t* x, const uint16_t* w1,

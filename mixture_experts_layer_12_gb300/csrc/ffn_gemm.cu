@@ -235,6 +235,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // SwiGLU the gate (rank 0) / up (rank 1) columns of the same 128
         // outputs (W1 = [W_gate | W_up], so up starts at column N)
         const int bcol = SWIGLU ? rank * p.N + t.nb * BN_OUT : t.nb * BN + rank * BN_CTA;
+        const int we = t.e % p.E_w;  // the segment's expert weights
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&c.empty[stage], phase ^ 1u, wc)) {
             ok = false;
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int cb = 0; cb < BN_CTA / 64; ++cb)
             tma_load_3d_pair(sB + stage * B_BYTES + cb * B_CHUNK, &tm_b, full_cl, bcol + cb * 64,
-                             kb * BK, t.e);
+                             kb * BK, we);
           ++issued;
           if (++stage == STAGES) {
             stage = 0;

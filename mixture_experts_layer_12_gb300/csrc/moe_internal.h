@@ -79,8 +79,9 @@ cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st, bool pdl);
 
 // ---- grouped expert GEMM (tcgen05 + TMA, persistent ragged scheduler).
 struct GemmArgs {
-  const int32_t* offsets;  // [E+1] dispatch offsets (device)
-  int E;
+  const int32_t* offsets;  // [E+1] row offsets of the E segments (device)
+  int E;                   // row segments
+  int E_w;                 // weight matrices: segment e uses W[e % E_w]
   int N;                   // output columns (SwiGLU: F; W1 then holds 2F columns)
   int K;                   // reduction length
   uint16_t* out;           // [rows, N] bf16, row r = dispatch row (kGemmCombineK1: y [T, N])

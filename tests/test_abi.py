@@ -34,7 +34,7 @@ def exported_symbols(path):
 
 def test_exports_match_header(lib):
     decl = declared_symbols()
-    assert len(decl) == 13
+    assert len(decl) == 16
     assert decl == set(moe.EXPORTS)
     exported = {s for s in exported_symbols(moe.LIB_PATH) if s.startswith("moe_")}
     assert exported == decl
@@ -76,7 +76,10 @@ def test_bad_shapes_rejected_before_launch(lib, kw, code):
     base = dict(T=64, H=128, F=256, E=8, k=2)
     base.update(kw)
     s = moe.make_shape(**base)
-    assert lib.moe_workspace_size(ctypes.byref(s)) == 0
+    if kw == dict(E=7):  # a valid expert count for moe_expert_ffn, not for the router
+        assert lib.moe_workspace_size(ctypes.byref(s)) > 0
+    else:
+        assert lib.moe_workspace_size(ctypes.byref(s)) == 0
     rc = lib.moe_forward(ctypes.byref(s), *([None] * 13), 0, None)
     assert rc == code
     assert lib.moe_last_error_string()
@@ -121,3 +124,14 @@ def test_unknown_expert_act_rejected(lib):
     s.expert_act = 7
     assert lib.moe_workspace_size(ctypes.byref(s)) == 0
     assert lib.moe_forward(ctypes.byref(s), *([None] * 13), 0, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_step_entry_points_validate_before_touching_the_device(lib):
+    s = moe.make_shape(64, 128, 256, 8, 1)
+    ws = ctypes.c_void_p(16)
+    for n in (0, 257, -3):
+        assert lib.moe_expert_ffn(ctypes.byref(s), n, None, None, None, None, None, ws, 1 << 30,
+                                  None) == moe.MOE_ERR_INVALID_ARG
+    bad = moe.make_shape(64, 128, 256, 7, 1)  # E not a multiple of 8
+    assert lib.moe_dispatch_rows(ctypes.byref(bad), None, None, None, None, None) != moe.MOE_OK
+    assert lib.moe_combine(ctypes.byref(bad), None, None, None, None, None) != moe.MOE_OK

@@ -448,3 +448,57 @@ def test_forward_k1_softmax_over_all_experts():
 
 def test_forward_k1_prefill_sampled():
     forward_parity(moe_synth.PREFILL_K1, stride=16)
+
+
+# ------------------------------------------- expert parallelism (simulated) --
+
+def _exchange_locally(layers, routed):
+    """The two all-to-alls of an expert-parallel step for G ranks held in
+    one process: slices of the senders' rows, concatenated per receiver."""
+    G = len(layers)
+    starts = [np.concatenate([[0], np.cumsum(r.send_split)]).tolist() for r in routed]
+    Ys = []
+    for d in range(G):
+        counts = torch.stack([routed[s].send_counts[d] for s in range(G)])
+        rows = torch.cat([routed[s].rows[starts[s][d]:starts[s][d + 1]] for s in range(G)])
+        Ys.append((layers[d].compute(rows, counts), counts.sum(dim=1).tolist()))
+    backs = []
+    for s in range(G):
+        parts = []
+        for d in range(G):
+            Y, recv = Ys[d]
+            off = int(sum(recv[:s]))
+            parts.append(Y[off:off + recv[s]])
+        backs.append(torch.cat(parts))
+    return backs
+
+
+@pytest.mark.parametrize("G,T,H,F,E,k,cf,bias,act", [
+    (2, 512, 256, 512, 8, 2, None, None, "gelu"),
+    (4, 700, 256, 384, 8, 4, 0.8, 2.0, "gelu"),      # drops, skew, ragged
+    (2, 300, 128, 256, 16, 2, None, None, "swiglu"),
+    (2, 256, 128, 256, 8, 1, 0.7, 1.0, "gelu"),      # k = 1 (the whole layer fuses its combine)
+])
+def test_expert_parallel_ranks_match_whole_layer(G, T, H, F, E, k, cf, bias, act):
+    from mixture_experts_layer_12_gb300.expert_parallel import CudaOps, ExpertParallelMoE
+    cfg = moe_synth.MoEConfig("ep", T=T, H=H, F=F, E=E, k=k, seed=80, capacity_factor=cf,
+                              bias0=bias, act=act)
+    full = to_dev(moe_synth.make_inputs(cfg))
+    xs = [to_dev(moe_synth.make_inputs(cfg.with_(seed=90 + r), with_ffn=False))["x"]
+          for r in range(G)]
+    El = E // G
+    layers = [ExpertParallelMoE(CudaOps(full["w_router"], full["w1"][r * El:(r + 1) * El],
+                                        full["w2"][r * El:(r + 1) * El], k, E, bias=full["bias"],
+                                        capacity_factor=cf, act=act), r, G) for r in range(G)]
+    routed = [layers[r].send(xs[r]) for r in range(G)]
+    backs = _exchange_locally(layers, routed)
+    whole = moe.MoELayer(full["w_router"], full["w1"], full["w2"], k, bias=full["bias"],
+                         capacity_factor=cf, act=act)
+    for r in range(G):
+        y = layers[r].finish(routed[r], backs[r])
+        y_ref = whole(xs[r]).clone()
+        assert moe.moe_get_device_status(whole.ws) == 0
+        if k > 1:
+            assert torch.equal(y, y_ref), f"rank {r}"
+        else:  # the whole layer rounds w * acc once; here Y is rounded first
+            check_y(y.float().cpu().numpy(), y_ref.double().cpu().numpy())
