@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(CTHREADS) combine_kernel(const CombineArgs a) 
 
 // xp[r] = x[perm[r] / k] for the kept rows r < offsets[E]: the dispatch-
 // ordered ("expanded") copy of the tokens that the expert GEMM reads with
-// TMA.  One warp per row, 16-byte loads, four in flight per lane; the copy
+// TMA.  One warp per row, 16-byte loads, eight in flight per lane; the copy
 // is HBM/L2-bandwidth bound (2 H bytes read + 2 H bytes written per row).
 constexpr int PTHREADS = 256;
 __global__ void __launch_bounds__(PTHREADS) permute_kernel(const PermuteArgs a) {
@@ -148,15 +148,12 @@ __global__ void __launch_bounds__(PTHREADS) permute_kernel(const PermuteArgs a) 
     const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)tok * a.H);
     uint4* dst = reinterpret_cast<uint4*>(a.xp + (size_t)r * a.H);
     int c = lane;
-    for (; c + 96 < vec; c += 128) {
-      const uint4 v0 = __ldg(src + c);
-      const uint4 v1 = __ldg(src + c + 32);
-      const uint4 v2 = __ldg(src + c + 64);
-      const uint4 v3 = __ldg(src + c + 96);
-      dst[c] = v0;
-      dst[c + 32] = v1;
-      dst[c + 64] = v2;
-      dst[c + 96] = v3;
+    for (; c + 224 < vec; c += 256) {
+      uint4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldg(src + c + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) dst[c + 32 * u] = v[u];
     }
     for (; c < vec; c += 32) dst[c] = __ldg(src + c);
   }
