@@ -502,3 +502,22 @@ def test_expert_parallel_ranks_match_whole_layer(G, T, H, F, E, k, cf, bias, act
             assert torch.equal(y, y_ref), f"rank {r}"
         else:  # the whole layer rounds w * acc once; here Y is rounded first
             check_y(y.float().cpu().numpy(), y_ref.double().cpu().numpy())
+
+
+# ---------------------------------------------- host batches, copies overlapped --
+
+def test_host_pipeline_matches_one_call_at_a_time():
+    from mixture_experts_layer_12_gb300.host_pipeline import HostPipeline
+    cfg = moe_synth.MoEConfig("pipe", T=256, H=256, F=512, E=8, k=2, seed=28)
+    dev_in = to_dev(moe_synth.make_inputs(cfg))
+    layer = moe.MoELayer(dev_in["w_router"], dev_in["w1"], dev_in["w2"], cfg.k)
+    xs = [moe_synth.make_inputs(cfg.with_(seed=100 + i), with_ffn=False)["x"].pin_memory()
+          for i in range(5)]
+    refs = [layer(x.to(DEV)).cpu() for x in xs]
+    ys = [torch.full((cfg.T, cfg.H), float("nan"), dtype=torch.bfloat16).pin_memory()
+          for _ in range(5)]
+    HostPipeline(layer, cfg.T, DEV).run(xs, ys)
+    torch.cuda.synchronize()
+    assert moe.moe_get_device_status(layer.ws) == 0
+    for y, ref in zip(ys, refs):
+        assert torch.equal(y, ref)
