@@ -521,3 +521,33 @@ def test_host_pipeline_matches_one_call_at_a_time():
     assert moe.moe_get_device_status(layer.ws) == 0
     for y, ref in zip(ys, refs):
         assert torch.equal(y, ref)
+
+
+# ------------------------------------------------- the GEMM1 epilogue's GELU --
+
+def test_gelu_epilogue_elementwise_against_fp64():
+    # W1 = W2 = I (one expert, H = F = 64): Y = h = bf16(GELU(x)) element by
+    # element, so the epilogue's GELU is seen directly for z in [-10, 10]
+    import math
+    T, H = 1024, 64
+    eye = torch.eye(H, dtype=torch.bfloat16, device=DEV).reshape(1, H, H).contiguous()
+    z = torch.linspace(-10.0, 10.0, T * H, dtype=torch.float64)
+    z[T * H // 2] = 0.0
+    x = z.to(torch.bfloat16).reshape(T, H).to(DEV)
+    s = moe.make_shape(T, H, H, 1, 1)
+    ws = moe.alloc_workspace(s, DEV)
+    Y = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
+    seg = torch.tensor([0, T], dtype=torch.int32, device=DEV)
+    moe.moe_expert_ffn(s, 1, x, eye, eye, seg, Y, ws)
+    assert moe.moe_get_device_status(ws) == 0
+    zz = x.double().cpu().reshape(-1).numpy()
+    ref = np.array([0.5 * v * math.erfc(-v / math.sqrt(2.0)) for v in zz])
+    got = Y.double().cpu().reshape(-1).numpy()
+    err = np.abs(got - ref)
+    near = zz >= -5.0  # |GELU| > 1.4e-6: within one bf16 step of the exact value
+    assert np.all(err[near] <= 2.0 ** -7 * np.abs(ref[near]))
+    # z < -5 (|GELU| < 1.4e-6): Abramowitz & Stegun 7.1.26's relative error
+    # grows to 2.0% at z = -10 (|GELU| ~ 1e-18), plus half a bf16 step
+    assert np.all(err[~near] <= 0.03 * np.abs(ref[~near]))
+    assert np.all(np.sign(got) == np.sign(ref))
+    assert got[T * H // 2] == 0.0
