@@ -41,8 +41,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # prefill workload, `ncu --set full` (profiles/expert_gemm_prefill.md, profiles/router_prefill.md):
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch
-    "prefill/expert_gemm1": {"bytes": 1037565e3 + 221870336, "src": "ffn_gemm.cu", "src_sha": "59cca3f2c56b3306"},
-    "prefill/expert_gemm2": {"bytes": 1592799e3 + 66000640, "src": "ffn_gemm.cu", "src_sha": "59cca3f2c56b3306"},
+    "prefill/expert_gemm1": {"bytes": 1027084e3 + 221348352, "src": "ffn_gemm.cu", "src_sha": "b025e2a1c26843e7"},
+    "prefill/expert_gemm2": {"bytes": 1432670e3 + 65446912, "src": "ffn_gemm.cu", "src_sha": "b025e2a1c26843e7"},
     "prefill/router": {"bytes": 33692416, "src": "router.cu", "src_sha": "0fe9ac7818d6ca7e"},
 }
 

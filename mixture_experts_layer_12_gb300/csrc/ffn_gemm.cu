@@ -141,8 +141,10 @@ __device__ __forceinline__ float gelu_erf(float z) {
   return 0.5f * z * (z >= 0.0f ? 2.0f - c : c);
 }
 
-// SiLU(z) = z * sigmoid(z)
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+// SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z)); the fast exponential and
+// division are far inside the bf16 rounding of h, and for z < -88 the
+// denominator overflows to +inf and the quotient to 0 (the limit).
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
