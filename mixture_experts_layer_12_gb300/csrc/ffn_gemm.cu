@@ -243,6 +243,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_prefetch_desc(&tm_a);
       tma_prefetch_desc(&tm_b);
       const uint32_t full0 = dsmem_map(smem_u32(&c.full[0]), 0);  // leader's barriers
+      // An expert with a single row block reads each weight tile once: those
+      // tiles go to L2 as evict-first and its A rows as evict-last (the
+      // weight stream of a decode step).  With several row blocks the pairs
+      // on the other blocks read the same weight tile a little later, so
+      // the loads keep the default policy.
+      const uint64_t pol_first = l2_evict_first_policy();
+      const uint64_t pol_last = l2_evict_last_policy();
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;  // k-blocks issued (all tiles)
@@ -255,6 +262,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // outputs (W1 = [W_gate | W_up], so up starts at column N)
         const int bcol = SWIGLU ? rank * p.N + t.nb * BN_OUT : t.nb * BN + rank * BN_CTA;
         const int we = t.e % p.E_w;  // the segment's expert weights
+        const bool once = c.mblocks[t.e] == 1;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&c.empty[stage], phase ^ 1u, wc)) {
             ok = false;
@@ -264,11 +272,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive_expect_tx_cluster(full_cl, STAGE_BYTES);
           // rows past the expert's end belong to the next expert (or lie past
           // the last row: zero-filled); they are computed but never stored
-          tma_load_2d_pair(sA + stage * A_BYTES, &tm_a, full_cl, kb * BK, t.row0);
+          if (once) {
+            tma_load_2d_pair_hint(sA + stage * A_BYTES, &tm_a, full_cl, kb * BK, t.row0, pol_last);
 #pragma unroll
-          for (int cb = 0; cb < BN_CTA / 64; ++cb)
-            tma_load_3d_pair(sB + stage * B_BYTES + cb * B_CHUNK, &tm_b, full_cl, bcol + cb * 64,
-                             kb * BK, we);
+            for (int cb = 0; cb < BN_CTA / 64; ++cb)
+              tma_load_3d_pair_hint(sB + stage * B_BYTES + cb * B_CHUNK, &tm_b, full_cl,
+                                    bcol + cb * 64, kb * BK, we, pol_first);
+          } else {
+            tma_load_2d_pair(sA + stage * A_BYTES, &tm_a, full_cl, kb * BK, t.row0);
+#pragma unroll
+            for (int cb = 0; cb < BN_CTA / 64; ++cb)
+              tma_load_3d_pair(sB + stage * B_BYTES + cb * B_CHUNK, &tm_b, full_cl, bcol + cb * 64,
+                               kb * BK, we);
+          }
           ++issued;
           if (++stage == STAGES) {
             stage = 0;
