@@ -189,12 +189,17 @@ def whole_job_throughput(tokens_per_rank: int, world: int, steps: int, max_elaps
 
 # --------------------------------------------------------- work per kernel --
 
-def launched_kernels(cfg):
-    """The library's kernels per forward step (with k = 1 the combine is part
-    of the second expert GEMM)."""
+def launched_kernels(shape):
+    """The library's kernels per forward step: small batches route and
+    dispatch in one launch, and with k = 1 the combine runs inside the second
+    expert GEMM, as the library reports for the shape."""
     import mixture_experts_layer_12_gb300 as moe
-    names = moe.KERNEL_NAMES
-    return tuple(n for n in names if not (cfg.k == 1 and n == "combine"))
+    in_router, in_gemm = moe.moe_forward_plan(shape)
+    return tuple(n for n in moe.KERNEL_NAMES
+                 if not (in_router and n == "dispatch") and not (in_gemm and n == "combine"))
+
+
+FUSED_INTO = {"dispatch": "router", "combine": "expert_gemm2"}
 
 
 def kernel_work(cfg, n_rows, experts_hit):
@@ -367,7 +372,7 @@ def run_route_only(args, cfg, device):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "step": "moe_route (router + dispatch)",
                    "l2": f"{copies} rotating copies of x ({copies * x0.numel() * 2 / 1e6:.0f} MB > L2)"},
-        "gpu_launches": 2 * K,
+        "gpu_launches": (1 if moe.moe_forward_plan(s)[0] else 2) * K,  # router (+ dispatch)
         "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks.get("hbm_gbs"),
                      "unit": "GB/s", "frac": round(ach / peaks.get("hbm_gbs", 6800.0), 4),
                      "peak_kind": f"HBM copy ({src})", "kernel": "router+dispatch",
@@ -497,11 +502,11 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     dominant = max(per_kernel, key=per_kernel.get)
     kernels = {}
-    launched = launched_kernels(cfg)
+    launched = launched_kernels(layer.shape)
     for n in names:
         ms = per_kernel[n]
-        if n not in launched:  # k = 1: the combine runs inside GEMM2's epilogue
-            kernels[n] = {"ms": round(ms, 5), "fused_into": "expert_gemm2"}
+        if n not in launched:  # this step runs inside another kernel
+            kernels[n] = {"ms": round(ms, 5), "fused_into": FUSED_INTO[n]}
             continue
         kernels[n] = {"ms": round(ms, 5), "share": round(ms / sum(per_kernel.values()), 4),
                       "tflops": round(work[n]["flops"] / (ms * 1e-3) / 1e12, 2),

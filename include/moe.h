@@ -149,6 +149,21 @@ MOE_API size_t moe_workspace_size(const moe_shape* s);
 MOE_API size_t moe_route_workspace_size(const moe_shape* s);
 
 /*
+ * Which kernels moe_forward (and moe_route) launch for this shape; no
+ * counterpart on the pages, for callers that count or profile kernels.
+ * Host only: depends on the shape alone.
+ *   *dispatch_in_router = 1 for small batches (T <= 128 and E <= 64): the
+ *     logits are computed on the CUDA cores and the dispatch (step 3) runs
+ *     in the same launch; 0: the tensor-core router, then a dispatch kernel.
+ *   *combine_in_gemm = 1 for k = 1: the combine runs inside the second
+ *     expert GEMM; 0: a separate combine kernel.
+ * Returns MOE_OK, or MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for a bad
+ * shape or a null output.
+ */
+MOE_API int moe_forward_plan(const moe_shape* s, int32_t* dispatch_in_router,
+                             int32_t* combine_in_gemm);
+
+/*
  * Steps 1-3 (the router kernel "MoERouterKernel::Process": x × W_router on
  * the tensor cores, per-token TopK, Softmax over the k scores; then the
  * dispatch of GatherTokensByExpert) for all T tokens.

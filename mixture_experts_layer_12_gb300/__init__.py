@@ -39,7 +39,7 @@ EXPORTS = ("moe_version", "moe_last_error_string", "moe_expert_capacity", "moe_w
            "moe_route", "moe_dispatch", "moe_expert_ffn_combine", "moe_forward",
            "moe_get_device_status", "moe_selftest_wait_timeout", "moe_forward_profiled",
            "moe_expert_ffn_combine_noalloc", "moe_route_workspace_size", "moe_dispatch_rows",
-           "moe_expert_ffn", "moe_combine")
+           "moe_expert_ffn", "moe_combine", "moe_forward_plan")
 MOE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -105,6 +105,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "moe_dispatch_rows": ([S, P, P, P, P, P], ctypes.c_int),
             "moe_expert_ffn": ([S, ctypes.c_int32, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "moe_combine": ([S, P, P, P, P, P], ctypes.c_int),
+            "moe_forward_plan": ([S, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
+                                 ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -157,6 +159,14 @@ def moe_workspace_size(shape: moe_shape) -> int:
     if n == 0:
         _check(MOE_ERR_UNSUPPORTED)
     return n
+
+
+def moe_forward_plan(shape: moe_shape) -> tuple[bool, bool]:
+    """(dispatch runs inside the router launch, combine runs inside the
+    second expert GEMM) for this shape."""
+    d, c = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(load_library().moe_forward_plan(ctypes.byref(shape), ctypes.byref(d), ctypes.byref(c)))
+    return bool(d.value), bool(c.value)
 
 
 def moe_route_workspace_size(shape: moe_shape) -> int:

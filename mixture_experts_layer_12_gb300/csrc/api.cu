@@ -204,6 +204,33 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
                   int32_t* offsets, int32_t* perm, int32_t* slot, void* ws, cudaStream_t st,
                   void* const* ev = nullptr) {
   int rc;
+  if (s->T <= kSmallRouteTokens && s->E <= kSmallRouteExperts) {
+    // small batch: logits on the CUDA cores and the dispatch by the last
+    // CTA, one launch (a 32-token decode step routes in well under half the
+    // time of the tensor-core router followed by the dispatch kernel)
+    SmallRouteArgs sa;
+    sa.x = x;
+    sa.w = w_router;
+    sa.bias = b_router;
+    sa.T = s->T;
+    sa.H = s->H;
+    sa.E = s->E;
+    sa.k = s->k;
+    sa.capacity = (int)capacity_of(s);
+    sa.gating = s->gating;
+    sa.ids = ids;
+    sa.weights = weights;
+    sa.counts = counts;
+    sa.offsets = offsets;
+    sa.perm = perm;
+    sa.slot = slot;
+    sa.ticket = ticket_ptr(ws);
+    if ((rc = mark(ev, 0, st)) != MOE_OK) return rc;
+    cudaError_t e = launch_router_small(sa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "router launch");
+    if ((rc = mark(ev, 1, st)) != MOE_OK) return rc;
+    return mark(ev, 2, st);  // no separate dispatch kernel
+  }
   CUtensorMap tm_x, tm_w;
   if ((rc = map_2d(&tm_x, x, (uint64_t)s->H, (uint64_t)s->T, 64, 128, "x (router)")) != MOE_OK) return rc;
   if ((rc = map_2d(&tm_w, w_router, (uint64_t)s->E, (uint64_t)s->H, 64, 64, "w_router")) != MOE_OK) return rc;
@@ -420,6 +447,16 @@ size_t moe_workspace_size(const moe_shape* s) {
 size_t moe_route_workspace_size(const moe_shape* s) {
   if (check_shape(s, false) != MOE_OK) return 0;
   return route_ws_bytes(s);
+}
+
+int moe_forward_plan(const moe_shape* s, int32_t* dispatch_in_router, int32_t* combine_in_gemm) {
+  int rc = check_shape(s, true);
+  if (rc != MOE_OK) return rc;
+  if (!dispatch_in_router || !combine_in_gemm)
+    return fail(MOE_ERR_INVALID_ARG, "dispatch_in_router / combine_in_gemm is null");
+  *dispatch_in_router = s->T <= kSmallRouteTokens && s->E <= kSmallRouteExperts ? 1 : 0;
+  *combine_in_gemm = s->k == 1 ? 1 : 0;
+  return MOE_OK;
 }
 
 int moe_route(const moe_shape* s, const uint16_t* x, const uint16_t* w_router, const float* b_router,

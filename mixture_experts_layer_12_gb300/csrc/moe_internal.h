@@ -46,6 +46,27 @@ struct RouterArgs {
 cudaError_t launch_router(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterArgs& a,
                           cudaStream_t st);
 size_t router_smem_bytes(int E);
+
+// ---- small-batch route (router + dispatch in one launch, CUDA cores):
+// for T <= kSmallRouteTokens and E <= kSmallRouteExperts.
+constexpr int kSmallRouteTokens = 128;
+constexpr int kSmallRouteExperts = 64;
+struct SmallRouteArgs {
+  const uint16_t* x;  // [T, H] bf16
+  const uint16_t* w;  // [H, E] bf16
+  const float* bias;  // [E] or null
+  int T, H, E, k;
+  int capacity;       // -1: unlimited
+  int gating;         // MOE_GATE_*
+  int32_t* ids;
+  float* weights;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* slot;
+  unsigned int* ticket;  // zero before the launch
+};
+cudaError_t launch_router_small(const SmallRouteArgs& a, cudaStream_t st);
 // Clusters of `splits` router CTAs that can be resident at once.
 cudaError_t router_max_clusters(int E, int splits, int* out);
 

@@ -551,6 +551,174 @@ __global__ void __launch_bounds__(HTHREADS) histogram_kernel(const HistArgs a) {
   }
 }
 
+// ---- small batches (T <= kSmallRouteTokens, E <= 64): the whole route in
+// one launch on the CUDA cores.  One CTA per token: each thread keeps
+// partial logits for every expert over a strided slice of H (16-byte loads
+// of x and of W_router's E-contiguous rows), then warps reduce by shuffle
+// and the CTA sums the warps in order (a fixed order: deterministic).  The
+// token's TopK and gate weights follow the tensor-core router exactly (same
+// insertion list, gating modes, bias, NaN -> -inf).  The last CTA to finish
+// (atomic ticket, nobody waits) then dispatches all T*k assignments: rank
+// within the expert in (token, slot) order -- the serial scan of
+// "Gather操作" -- the capacity clip, counts, offsets, slot and perm.
+constexpr int SR_THREADS = 256;
+constexpr int SR_WARPS = SR_THREADS / 32;
+constexpr int SR_MAX_ASSIGN = kSmallRouteTokens * kMaxTopK;
+
+template <int NE>  // experts rounded up to 8, 16, 32 or 64
+__global__ void __launch_bounds__(SR_THREADS) router_small_kernel(const SmallRouteArgs a) {
+  __shared__ float s_part[SR_WARPS][NE];
+  __shared__ float s_logit[NE];
+  __shared__ int s_last;
+  __shared__ int s_pos[SR_MAX_ASSIGN];
+  __shared__ int s_wc[SR_WARPS][NE];
+  __shared__ int s_run[NE];
+  __shared__ int s_off[NE + 1];
+  pdl_launch_dependents();
+  pdl_wait();  // no-op: launched with full serialization
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int t = blockIdx.x;
+  const int E = a.E;
+  const int Q = E / 8;  // 16-byte groups of experts in a W_router row
+
+  // ---- logits of token t
+  float acc[NE];
+#pragma unroll
+  for (int e = 0; e < NE; ++e) acc[e] = 0.f;
+  const uint16_t* xr = a.x + (size_t)t * a.H;
+  for (int h0 = tid * 8; h0 < a.H; h0 += SR_THREADS * 8) {
+    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr + h0));
+    const float xf[8] = {bf16_lo(xv.x), bf16_hi(xv.x), bf16_lo(xv.y), bf16_hi(xv.y),
+                         bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      const uint4* wrow = reinterpret_cast<const uint4*>(a.w + (size_t)(h0 + r) * E);
+#pragma unroll
+      for (int q = 0; q < NE / 8; ++q) {
+        if (q < Q) {
+          const uint4 wv = __ldg(wrow + q);
+          acc[q * 8 + 0] = fmaf(xf[r], bf16_lo(wv.x), acc[q * 8 + 0]);
+          acc[q * 8 + 1] = fmaf(xf[r], bf16_hi(wv.x), acc[q * 8 + 1]);
+          acc[q * 8 + 2] = fmaf(xf[r], bf16_lo(wv.y), acc[q * 8 + 2]);
+          acc[q * 8 + 3] = fmaf(xf[r], bf16_hi(wv.y), acc[q * 8 + 3]);
+          acc[q * 8 + 4] = fmaf(xf[r], bf16_lo(wv.z), acc[q * 8 + 4]);
+          acc[q * 8 + 5] = fmaf(xf[r], bf16_hi(wv.z), acc[q * 8 + 5]);
+          acc[q * 8 + 6] = fmaf(xf[r], bf16_lo(wv.w), acc[q * 8 + 6]);
+          acc[q * 8 + 7] = fmaf(xf[r], bf16_hi(wv.w), acc[q * 8 + 7]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < NE; ++e) {
+    float v = acc[e];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) s_part[warp][e] = v;
+  }
+  __syncthreads();
+  if (tid < E) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < SR_WARPS; ++w) v += s_part[w][tid];
+    if (a.bias) v += __ldg(a.bias + tid);
+    s_logit[tid] = isnan(v) ? -INFINITY : v;
+  }
+  __syncthreads();
+
+  // ---- TopK and gate weights (thread 0)
+  if (tid == 0) {
+    TopK8 tk;
+    tk.init();
+    for (int e = 0; e < E; ++e) tk.push(s_logit[e], e, a.k);
+    const float mx = tk.v[0];
+    float ex[kMaxTopK];
+    float z = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      ex[j] = j < a.k ? expf(tk.v[j] - mx) : 0.f;
+      z += ex[j];
+    }
+    if (a.gating != MOE_GATE_TOPK_SOFTMAX) {
+      float zall = 0.f;
+      for (int e = 0; e < E; ++e) zall += expf(s_logit[e] - mx);
+      float zsel = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j) {
+        ex[j] = ex[j] / zall;
+        zsel += ex[j];
+      }
+      z = a.gating == MOE_GATE_SOFTMAX_TOPK ? 1.f : zsel;
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+      if (j < a.k) {
+        a.ids[(size_t)t * a.k + j] = tk.id[j];
+        a.weights[(size_t)t * a.k + j] = ex[j] / z;
+      }
+    }
+    __threadfence();
+    s_last = atomicAdd(a.ticket, 1u) == gridDim.x - 1 ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+
+  // ---- the last CTA: dispatch of all T*k assignments
+  __threadfence();
+  const int n = a.T * a.k;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int e = tid; e < E; e += SR_THREADS) s_run[e] = 0;
+  for (int c0 = 0; c0 < n; c0 += SR_THREADS) {
+    for (int idx = tid; idx < SR_WARPS * NE; idx += SR_THREADS) (&s_wc[0][0])[idx] = 0;
+    __syncthreads();
+    const int i = c0 + tid;
+    int e = i < n ? __ldcg(a.ids + i) : -1;
+    if (e < 0 || e >= E) e = -1;
+    const unsigned m = __match_any_sync(0xffffffffu, e);
+    const int below = __popc(m & lt);  // same expert, earlier lane
+    if (e >= 0 && below == 0) s_wc[warp][e] = __popc(m);
+    __syncthreads();
+    for (int ee = tid; ee < E; ee += SR_THREADS) {  // exclusive scan over warps
+      int run = s_run[ee];
+      for (int w = 0; w < SR_WARPS; ++w) {
+        const int v = s_wc[w][ee];
+        s_wc[w][ee] = run;
+        run += v;
+      }
+      s_run[ee] = run;
+    }
+    __syncthreads();
+    if (i < n) s_pos[i] = e >= 0 ? s_wc[warp][e] + below : -1;
+    __syncthreads();
+  }
+  if (tid == 0) {  // counts after the capacity clip and their exclusive scan
+    int run = 0;
+    for (int e = 0; e < E; ++e) {
+      const int kept = a.capacity >= 0 ? min(s_run[e], a.capacity) : s_run[e];
+      a.counts[e] = kept;
+      a.offsets[e] = run;
+      s_off[e] = run;
+      run += kept;
+    }
+    a.offsets[E] = run;
+    s_off[E] = run;
+  }
+  __syncthreads();
+  for (int i = tid; i < n; i += SR_THREADS) {
+    const int e = __ldcg(a.ids + i);
+    const int pos = s_pos[i];
+    if (pos >= 0 && (a.capacity < 0 || pos < a.capacity)) {
+      a.slot[i] = s_off[e] + pos;
+      a.perm[s_off[e] + pos] = i;
+    } else {
+      a.slot[i] = -1;
+    }
+  }
+  for (int i = s_off[E] + tid; i < n; i += SR_THREADS) a.perm[i] = -1;
+}
+
 }  // namespace
 
 size_t router_smem_bytes(int E) {
@@ -571,6 +739,15 @@ cudaError_t router_set_attributes() {
   if ((e = set_attr_nb<2>()) != cudaSuccess) return e;
   if ((e = set_attr_nb<3>()) != cudaSuccess) return e;
   return set_attr_nb<4>();
+}
+
+cudaError_t launch_router_small(const SmallRouteArgs& a, cudaStream_t st) {
+  const dim3 grid((unsigned)a.T);
+  if (a.E <= 8) router_small_kernel<8><<<grid, SR_THREADS, 0, st>>>(a);
+  else if (a.E <= 16) router_small_kernel<16><<<grid, SR_THREADS, 0, st>>>(a);
+  else if (a.E <= 32) router_small_kernel<32><<<grid, SR_THREADS, 0, st>>>(a);
+  else router_small_kernel<64><<<grid, SR_THREADS, 0, st>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_router(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterArgs& a,

@@ -34,7 +34,7 @@ def exported_symbols(path):
 
 def test_exports_match_header(lib):
     decl = declared_symbols()
-    assert len(decl) == 16
+    assert len(decl) == 17
     assert decl == set(moe.EXPORTS)
     exported = {s for s in exported_symbols(moe.LIB_PATH) if s.startswith("moe_")}
     assert exported == decl
@@ -135,3 +135,18 @@ def test_step_entry_points_validate_before_touching_the_device(lib):
     bad = moe.make_shape(64, 128, 256, 7, 1)  # E not a multiple of 8
     assert lib.moe_dispatch_rows(ctypes.byref(bad), None, None, None, None, None) != moe.MOE_OK
     assert lib.moe_combine(ctypes.byref(bad), None, None, None, None, None) != moe.MOE_OK
+
+
+def test_forward_plan_is_a_host_only_shape_rule(lib):
+    import moe_synth
+    for cfg, want in [(moe_synth.DECODE, (True, False)), (moe_synth.TINY, (True, False)),
+                      (moe_synth.PREFILL, (False, False)), (moe_synth.PREFILL_K1, (False, True)),
+                      (moe_synth.SKEWED, (False, False))]:
+        s = moe.make_shape(cfg.T, cfg.H, cfg.F, cfg.E, cfg.k, cfg.capacity_factor)
+        assert moe.moe_forward_plan(s) == want, cfg.name
+    assert moe.moe_forward_plan(moe.make_shape(128, 64, 64, 64, 2)) == (True, False)
+    assert moe.moe_forward_plan(moe.make_shape(129, 64, 64, 64, 2)) == (False, False)
+    assert moe.moe_forward_plan(moe.make_shape(128, 64, 64, 72, 2)) == (False, False)
+    c = ctypes.c_int32(0)
+    good = moe.make_shape(64, 128, 256, 8, 2)
+    assert lib.moe_forward_plan(ctypes.byref(good), None, ctypes.byref(c)) == moe.MOE_ERR_INVALID_ARG

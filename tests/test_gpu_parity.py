@@ -159,6 +159,25 @@ def test_router_more_tiles_than_one_wave(cf):
         assert rep["dropped"] > 0
 
 
+@pytest.mark.parametrize("T,E,k,cf,gating,bias", [
+    (128, 64, 8, 0.5, 0, None),      # the largest small batch, 64 experts, drops
+    (100, 16, 3, None, 1, 0.5),      # softmax over all experts
+    (37, 32, 4, 1.0, 2, None),       # renormalised
+    (1, 8, 2, None, 0, None),        # one token
+    (128, 8, 2, 0.3, 0, 3.0),        # skewed, heavy drops
+])
+def test_small_batch_route_in_one_launch(T, E, k, cf, gating, bias):
+    # T <= 128 and E <= 64: logits on the CUDA cores, dispatch by the last CTA
+    cfg = moe_synth.MoEConfig("small", T=T, H=264, F=0, E=E, k=k, seed=29, capacity_factor=cf,
+                              bias0=bias)
+    assert moe.moe_forward_plan(moe.make_shape(T, cfg.H, 8, E, k, cf, gating))[0]
+    inputs = moe_synth.make_inputs(cfg, with_ffn=False)
+    r = gpu_route(cfg, to_dev(inputs), gating)
+    _, rep = routing_parity(cfg, inputs, r, gating=gating)
+    if cf == 0.3:
+        assert rep["dropped"] > 0
+
+
 @pytest.mark.parametrize("T,H,E,k,bias", [(1, 64, 8, 1, None), (130, 200, 16, 3, 0.5),
                                           (257, 520, 256, 8, None), (64, 4096, 40, 5, 2.0),
                                           (300, 72, 192, 2, None)])
