@@ -94,38 +94,64 @@ __global__ void __launch_bounds__(DTHREADS, 1) dispatch_kernel(const DispatchArg
 }
 
 constexpr int CTHREADS = 128;
+constexpr int CCPT = 2;  // 16-byte column chunks per thread
 
-// y[t, c..c+7] = sum_j w[t,j] * Y[slot[t,j], c..c+7]; one thread per
-// 8 columns (16-byte loads and stores), grid (T, H / 1024 columns).
+// y[t, c..c+7] = sum_j w[t,j] * Y[slot[t,j], c..c+7] (fp32, j ascending).
+// Grid (T, H / (CTHREADS * 8 * CCPT)): each thread takes CCPT 16-byte column
+// chunks of one token (chunks CTHREADS * 8 columns apart, so every warp
+// access is coalesced) and issues all k * CCPT loads before the sums: the
+// kernel is latency-bound, so loads in flight per thread set its speed.
+// KMAX >= k (1, 2, 4 or 8) sizes the per-thread arrays.
+template <int KMAX>
 __global__ void __launch_bounds__(CTHREADS) combine_kernel(const CombineArgs a) {
   pdl_launch_dependents();
   pdl_wait();
   const int t = blockIdx.x;
-  const int col = (blockIdx.y * CTHREADS + threadIdx.x) * 8;
-  if (col >= a.H) return;
-  float acc[8];
+  const int col0 = (blockIdx.y * CTHREADS * CCPT + threadIdx.x) * 8;
+  if (col0 >= a.H) return;
+  int r[KMAX];
+  float w[KMAX];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  for (int j = 0; j < a.k; ++j) {
-    const int r = __ldg(a.slot + (size_t)t * a.k + j);
-    if (r < 0) continue;
-    const float wt = __ldg(a.w + (size_t)t * a.k + j);
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.Y + (size_t)r * a.H + col));
-    acc[0] = fmaf(wt, bf16_lo(v.x), acc[0]);
-    acc[1] = fmaf(wt, bf16_hi(v.x), acc[1]);
-    acc[2] = fmaf(wt, bf16_lo(v.y), acc[2]);
-    acc[3] = fmaf(wt, bf16_hi(v.y), acc[3]);
-    acc[4] = fmaf(wt, bf16_lo(v.z), acc[4]);
-    acc[5] = fmaf(wt, bf16_hi(v.z), acc[5]);
-    acc[6] = fmaf(wt, bf16_lo(v.w), acc[6]);
-    acc[7] = fmaf(wt, bf16_hi(v.w), acc[7]);
+  for (int j = 0; j < KMAX; ++j) {
+    r[j] = j < a.k ? __ldg(a.slot + (size_t)t * a.k + j) : -1;
+    w[j] = r[j] >= 0 ? __ldg(a.w + (size_t)t * a.k + j) : 0.f;
   }
-  uint4 o;
-  o.x = pack_bf16x2(acc[0], acc[1]);
-  o.y = pack_bf16x2(acc[2], acc[3]);
-  o.z = pack_bf16x2(acc[4], acc[5]);
-  o.w = pack_bf16x2(acc[6], acc[7]);
-  *reinterpret_cast<uint4*>(a.y + (size_t)t * a.H + col) = o;
+  uint4 v[KMAX][CCPT];
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j)
+#pragma unroll
+    for (int c = 0; c < CCPT; ++c) {
+      const int col = col0 + c * CTHREADS * 8;
+      if (r[j] >= 0 && col < a.H)
+        v[j][c] = __ldg(reinterpret_cast<const uint4*>(a.Y + (size_t)r[j] * a.H + col));
+    }
+#pragma unroll
+  for (int c = 0; c < CCPT; ++c) {
+    const int col = col0 + c * CTHREADS * 8;
+    if (col >= a.H) break;
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (r[j] < 0) continue;
+      const float wt = w[j];
+      acc[0] = fmaf(wt, bf16_lo(v[j][c].x), acc[0]);
+      acc[1] = fmaf(wt, bf16_hi(v[j][c].x), acc[1]);
+      acc[2] = fmaf(wt, bf16_lo(v[j][c].y), acc[2]);
+      acc[3] = fmaf(wt, bf16_hi(v[j][c].y), acc[3]);
+      acc[4] = fmaf(wt, bf16_lo(v[j][c].z), acc[4]);
+      acc[5] = fmaf(wt, bf16_hi(v[j][c].z), acc[5]);
+      acc[6] = fmaf(wt, bf16_lo(v[j][c].w), acc[6]);
+      acc[7] = fmaf(wt, bf16_hi(v[j][c].w), acc[7]);
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(a.y + (size_t)t * a.H + col) = o;
+  }
 }
 
 // xp[r] = x[perm[r] / k] for the kept rows r < offsets[E]: the dispatch-
@@ -196,9 +222,12 @@ cudaError_t dispatch_combine_set_attributes() {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
+  const void* combines[] = {(const void*)combine_kernel<1>, (const void*)combine_kernel<2>,
+                           (const void*)combine_kernel<4>, (const void*)combine_kernel<8>};
+  for (const void* f : combines)
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
   return e;
 }
 
@@ -233,9 +262,12 @@ cudaError_t launch_permute(const PermuteArgs& a, int sms, cudaStream_t st, bool 
 }
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st, bool pdl) {
-  const int cols_per_block = CTHREADS * 8;
+  const int cols_per_block = CTHREADS * 8 * CCPT;
   dim3 grid((unsigned)a.T, (unsigned)((a.H + cols_per_block - 1) / cols_per_block), 1);
-  return launch_1d(combine_kernel, grid, CTHREADS, st, pdl, a);
+  if (a.k <= 1) return launch_1d(combine_kernel<1>, grid, CTHREADS, st, pdl, a);
+  if (a.k <= 2) return launch_1d(combine_kernel<2>, grid, CTHREADS, st, pdl, a);
+  if (a.k <= 4) return launch_1d(combine_kernel<4>, grid, CTHREADS, st, pdl, a);
+  return launch_1d(combine_kernel<8>, grid, CTHREADS, st, pdl, a);
 }
 
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st) {
