@@ -14,6 +14,7 @@
 
 namespace moe {
 cudaError_t grouped_gemm_set_attributes();
+cudaError_t small_gemm_set_attributes();
 cudaError_t router_set_attributes();
 cudaError_t dispatch_combine_set_attributes();
 }  // namespace moe
@@ -63,6 +64,7 @@ int device_setup(int* sms) {
       return fail(MOE_ERR_UNSUPPORTED, "built for sm_103a; device %d is sm_%d%d", dev, major, minor);
     if ((e = router_set_attributes()) != cudaSuccess) return cuda_fail(e, "router attributes");
     if ((e = grouped_gemm_set_attributes()) != cudaSuccess) return cuda_fail(e, "gemm attributes");
+    if ((e = small_gemm_set_attributes()) != cudaSuccess) return cuda_fail(e, "gemm attributes");
     if ((e = dispatch_combine_set_attributes()) != cudaSuccess)
       return cuda_fail(e, "dispatch/combine attributes");
     if (!g_encode) {
@@ -302,6 +304,58 @@ int enqueue_expert_gemms(const moe_shape* s, int n_seg, const uint16_t* xp, cons
   const uint64_t rows = (uint64_t)s->T * s->k;
   CUtensorMap tm_xp, tm_w1, tm_h, tm_w2;
   const bool swiglu = s->expert_act == MOE_EXPERT_SWIGLU;
+  // Small batch: every segment fits one 64-token tile and the weights can
+  // stream as the MMA's M operand (ffn_gemm_small.cu), which keeps more
+  // weight bytes in flight.  Measured on a decode step it wins when it has
+  // at least two full waves of tiles (GEMM1: 448 tiles, 0.155 -> 0.142 ms)
+  // and loses slightly below that (GEMM2: 128 tiles, 0.154 -> 0.156 ms), so
+  // each GEMM takes it only with at least 2 * co-resident-pairs tiles.
+  int small_pairs = 0;
+  if (rows <= (uint64_t)kSmallGemmRows && !swiglu) {
+    cudaError_t ce = small_gemm_max_pairs(&small_pairs);
+    if (ce != cudaSuccess) return cuda_fail(ce, "cudaOccupancyMaxActiveClusters(small gemm)");
+  }
+  const int64_t small_tiles1 = (int64_t)n_seg * ((s->F + 255) / 256);
+  const int64_t small_tiles2 = (int64_t)n_seg * ((s->H + 255) / 256);
+  const bool small1 = small_pairs > 0 && small_tiles1 >= 2 * (int64_t)small_pairs;
+  const bool small2 = small_pairs > 0 && small_tiles2 >= 2 * (int64_t)small_pairs;
+  if (small1 || small2) {
+    // token-row boxes: 32 rows for the small kernel, 128 for the main one
+    if ((rc = map_2d(&tm_xp, xp, (uint64_t)s->H, rows, 64, small1 ? 32 : 128, "xp")) != MOE_OK) return rc;
+    if ((rc = map_3d(&tm_w1, w1, (uint64_t)s->F, (uint64_t)s->H, (uint64_t)s->E, 64, 64, "W1")) != MOE_OK) return rc;
+    if ((rc = map_2d(&tm_h, h, (uint64_t)s->F, rows, 64, small2 ? 32 : 128, "h")) != MOE_OK) return rc;
+    if ((rc = map_3d(&tm_w2, w2, (uint64_t)s->H, (uint64_t)s->F, (uint64_t)s->E, 64, 64, "W2")) != MOE_OK) return rc;
+    const int64_t row_blocks_ub = ((int64_t)rows + 2 * kGemmBM - 1) / (2 * kGemmBM) + n_seg;
+    GemmArgs g;
+    g.offsets = seg_offsets;
+    g.E = n_seg;
+    g.E_w = s->E;
+    g.perm = perm;
+    g.gate_w = weights;
+    g.T = s->T;
+    g.status = status;
+    g.wait_limit_ns = kWaitLimitNs;
+    g.N = s->F;
+    g.K = s->H;
+    g.out = h;
+    cudaError_t e =
+        small1 ? launch_small_gemm(kGemmGelu, tm_w1, tm_xp, g, (int)small_tiles1, st, pdl_first)
+               : launch_grouped_gemm(kGemmGelu, tm_xp, tm_w1, g,
+                                     (int)(row_blocks_ub * ((s->F + kGemmBN - 1) / kGemmBN)), st,
+                                     pdl_first);
+    if (e != cudaSuccess) return cuda_fail(e, "expert GEMM1 launch");
+    if ((rc = mark(ev, ev_gemm1, st)) != MOE_OK) return rc;
+    g.N = s->H;
+    g.K = s->F;
+    g.out = out;
+    const int mode2 = combine_k1 ? kGemmCombineK1 : kGemmPlain;
+    e = small2 ? launch_small_gemm(mode2, tm_w2, tm_h, g, (int)small_tiles2, st, pdl)
+               : launch_grouped_gemm(mode2, tm_h, tm_w2, g,
+                                     (int)(row_blocks_ub * ((s->H + kGemmBN - 1) / kGemmBN)), st,
+                                     pdl);
+    if (e != cudaSuccess) return cuda_fail(e, "expert GEMM2 launch");
+    return mark(ev, ev_gemm2, st);
+  }
   const uint64_t w1_cols = (uint64_t)s->F * (swiglu ? 2 : 1);  // SwiGLU: [W_gate | W_up]
   if ((rc = map_2d(&tm_xp, xp, (uint64_t)s->H, rows, 64, 128, "xp")) != MOE_OK) return rc;
   if ((rc = map_3d(&tm_w1, w1, w1_cols, (uint64_t)s->H, (uint64_t)s->E, 64, 64, "W1")) != MOE_OK) return rc;

@@ -131,6 +131,16 @@ constexpr int kGemmBM = 128;  // rows per CTA; a CTA pair covers 256
 constexpr int kGemmBN = 256;
 constexpr int kGemmBK = 64;
 
+// Small batches (at most kSmallGemmRows dispatch rows in all): the same
+// GEMMs with the weights as the MMA's M operand and the tokens as its N
+// (ffn_gemm_small.cu), modes kGemmGelu, kGemmPlain and kGemmCombineK1.
+// tm_w: W [E, K, N] box {64, 64, 1}; tm_x: rows [T*k, K] box {64, 32}.
+constexpr int kSmallGemmRows = 64;
+cudaError_t launch_small_gemm(int mode, const CUtensorMap& tm_w, const CUtensorMap& tm_x,
+                              const GemmArgs& a, int max_tiles, cudaStream_t st, bool pdl);
+// CTA pairs of the small kernel that are resident at once.
+cudaError_t small_gemm_max_pairs(int* out);
+
 // ---- row permutation (the expanded-x output of the dispatch step):
 // xp[r] = x[perm[r] / k] for r < offsets[E]; rows past offsets[E] untouched.
 struct PermuteArgs {

@@ -544,10 +544,24 @@ def test_host_pipeline_matches_one_call_at_a_time():
 
 # ------------------------------------------------- the GEMM1 epilogue's GELU --
 
+def _gelu_reference_check(x, Y):
+    import math
+    zz = x.double().cpu().reshape(-1).numpy()
+    ref = np.array([0.5 * v * math.erfc(-v / math.sqrt(2.0)) for v in zz])
+    got = Y.double().cpu().reshape(-1).numpy()
+    err = np.abs(got - ref)
+    near = zz >= -5.0  # |GELU| > 1.4e-6: within one bf16 step of the exact value
+    assert np.all(err[near] <= 2.0 ** -7 * np.abs(ref[near]))
+    # z < -5 (|GELU| < 1.4e-6): Abramowitz & Stegun 7.1.26's relative error
+    # grows to 2.0% at z = -10 (|GELU| ~ 1e-18), plus half a bf16 step
+    assert np.all(err[~near] <= 0.03 * np.abs(ref[~near]))
+    assert np.all(np.sign(got) == np.sign(ref))
+    return zz, got
+
+
 def test_gelu_epilogue_elementwise_against_fp64():
     # W1 = W2 = I (one expert, H = F = 64): Y = h = bf16(GELU(x)) element by
     # element, so the epilogue's GELU is seen directly for z in [-10, 10]
-    import math
     T, H = 1024, 64
     eye = torch.eye(H, dtype=torch.bfloat16, device=DEV).reshape(1, H, H).contiguous()
     z = torch.linspace(-10.0, 10.0, T * H, dtype=torch.float64)
@@ -559,14 +573,42 @@ def test_gelu_epilogue_elementwise_against_fp64():
     seg = torch.tensor([0, T], dtype=torch.int32, device=DEV)
     moe.moe_expert_ffn(s, 1, x, eye, eye, seg, Y, ws)
     assert moe.moe_get_device_status(ws) == 0
-    zz = x.double().cpu().reshape(-1).numpy()
-    ref = np.array([0.5 * v * math.erfc(-v / math.sqrt(2.0)) for v in zz])
-    got = Y.double().cpu().reshape(-1).numpy()
-    err = np.abs(got - ref)
-    near = zz >= -5.0  # |GELU| > 1.4e-6: within one bf16 step of the exact value
-    assert np.all(err[near] <= 2.0 ** -7 * np.abs(ref[near]))
-    # z < -5 (|GELU| < 1.4e-6): Abramowitz & Stegun 7.1.26's relative error
-    # grows to 2.0% at z = -10 (|GELU| ~ 1e-18), plus half a bf16 step
-    assert np.all(err[~near] <= 0.03 * np.abs(ref[~near]))
-    assert np.all(np.sign(got) == np.sign(ref))
+    _, got = _gelu_reference_check(x, Y)
     assert got[T * H // 2] == 0.0
+
+
+def test_gelu_epilogue_small_batch_kernel():
+    # 64 rows in 64 one-row segments of one expert, F = 10240: 2560 column
+    # tiles, so GEMM1 runs on the small-batch kernel (weights as the MMA's M
+    # operand); W1 = [I | 0] and W2 = [I ; 0] expose h[:, :64] = GELU(x)
+    T, H, F = 64, 64, 10240
+    w1 = torch.zeros(1, H, F, dtype=torch.bfloat16, device=DEV)
+    w1[0, :, :H] = torch.eye(H, dtype=torch.bfloat16, device=DEV)
+    w2 = torch.zeros(1, F, H, dtype=torch.bfloat16, device=DEV)
+    w2[0, :H, :] = torch.eye(H, dtype=torch.bfloat16, device=DEV)
+    z = torch.linspace(-10.0, 10.0, T * H, dtype=torch.float64)
+    x = z.to(torch.bfloat16).reshape(T, H).to(DEV)
+    s = moe.make_shape(T, H, F, 1, 1)
+    ws = moe.alloc_workspace(s, DEV)
+    Y = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
+    seg = torch.arange(T + 1, dtype=torch.int32, device=DEV)
+    moe.moe_expert_ffn(s, T, x, w1, w2, seg, Y, ws)
+    assert moe.moe_get_device_status(ws) == 0
+    _gelu_reference_check(x, Y)
+
+
+# ----------------------------------------------- small batches (T*k <= 64 rows) --
+
+# The small-batch kernel runs a GEMM when it has at least two waves of column
+# tiles (2 x 76 pairs on a GB300): F = 5120 over 8 experts gives GEMM1 160
+# tiles, H = 5120 gives GEMM2 160; the other shapes stay on the main kernel.
+@pytest.mark.parametrize("T,H,F,E,k,cf,bias", [
+    (16, 256, 5120, 8, 4, None, None),   # GEMM1 small: 64 rows over 8 experts
+    (40, 5120, 512, 8, 1, 0.5, None),    # GEMM2 small with the k = 1 combine; drops
+    (21, 264, 1408, 16, 3, 0.7, None),   # ragged H and F, drops (main kernel)
+    (64, 256, 296, 8, 1, None, 50.0),    # every row on one expert (main kernel)
+])
+def test_forward_small_batch_weights_as_m_operand(T, H, F, E, k, cf, bias):
+    cfg = moe_synth.MoEConfig("smallgemm", T=T, H=H, F=F, E=E, k=k, seed=33, capacity_factor=cf,
+                              bias0=bias)
+    forward_parity(cfg)
