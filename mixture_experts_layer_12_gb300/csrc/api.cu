@@ -168,7 +168,14 @@ size_t hist_bytes(const moe_shape* s) {
 size_t h_bytes(const moe_shape* s) { return align_up((size_t)s->T * s->k * s->F * 2, 1024); }
 size_t y_bytes(const moe_shape* s) { return align_up((size_t)s->T * s->k * s->H * 2, 1024); }
 size_t route_ws_bytes(const moe_shape* s) { return kStatusBytes + hist_bytes(s); }
-size_t ws_bytes_for(const moe_shape* s) { return route_ws_bytes(s) + h_bytes(s) + y_bytes(s); }
+// small batches: fp32 partial expert outputs of a K-split second GEMM
+size_t part_bytes(const moe_shape* s) {
+  const size_t rows = (size_t)s->T * s->k;
+  return rows <= (size_t)kSmallGemmRows ? align_up((size_t)kMaxKSplits * rows * s->H * 4, 1024) : 0;
+}
+size_t ws_bytes_for(const moe_shape* s) {
+  return route_ws_bytes(s) + h_bytes(s) + y_bytes(s) + part_bytes(s);
+}
 
 int* status_ptr(void* ws) { return reinterpret_cast<int*>(ws); }
 unsigned int* ticket_ptr(void* ws) {
@@ -179,6 +186,11 @@ int32_t* hist_ptr(void* ws) {
 }
 uint16_t* h_ptr(void* ws, const moe_shape* s) {
   return reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + route_ws_bytes(s));
+}
+float* part_ptr(void* ws, const moe_shape* s) {
+  if (part_bytes(s) == 0) return nullptr;
+  return reinterpret_cast<float*>(static_cast<char*>(ws) + route_ws_bytes(s) + h_bytes(s) +
+                                  y_bytes(s));
 }
 uint16_t* y_ptr(void* ws, const moe_shape* s) {
   return reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + route_ws_bytes(s) + h_bytes(s));
@@ -299,70 +311,62 @@ int enqueue_expert_gemms(const moe_shape* s, int n_seg, const uint16_t* xp, cons
                          const uint16_t* w2, const int32_t* seg_offsets, uint16_t* h,
                          uint16_t* out, bool combine_k1, const int32_t* perm,
                          const float* weights, int* status, cudaStream_t st, bool pdl_first,
-                         bool pdl, void* const* ev, int ev_gemm1, int ev_gemm2) {
+                         bool pdl, void* const* ev, int ev_gemm1, int ev_gemm2,
+                         float* part = nullptr, int* splits_used = nullptr) {
   int rc;
   const uint64_t rows = (uint64_t)s->T * s->k;
-  CUtensorMap tm_xp, tm_w1, tm_h, tm_w2;
   const bool swiglu = s->expert_act == MOE_EXPERT_SWIGLU;
-  // Small batch: every segment fits one 64-token tile and the weights can
-  // stream as the MMA's M operand (ffn_gemm_small.cu), which keeps more
-  // weight bytes in flight.  Measured on a decode step it wins when it has
-  // at least two full waves of tiles (GEMM1: 448 tiles, 0.155 -> 0.142 ms)
-  // and loses slightly below that (GEMM2: 128 tiles, 0.154 -> 0.156 ms), so
-  // each GEMM takes it only with at least 2 * co-resident-pairs tiles.
+  if (splits_used) *splits_used = 1;
+
+  // Small batch (every segment fits one 64-token tile): a GEMM may run on
+  // the kernel that streams the weights as the MMA's M operand
+  // (ffn_gemm_small.cu), which keeps more weight bytes in flight.  Measured
+  // on a decode step it wins with at least two waves of column tiles
+  // (GEMM1: 448 tiles, 0.155 -> 0.142 ms) and loses slightly below (GEMM2:
+  // 128 tiles, 0.154 -> 0.156 ms), so a GEMM takes it only with at least
+  // 2 * co-resident-pairs tiles.  When its fp32 partials can go to `part`
+  // (the combine sums them), GEMM2 may split K in S <= kMaxKSplits parts to
+  // reach that and fill its last wave best: decode GEMM2's 128 column tiles
+  // are 1.7 waves on 76 pairs, with S = 4 its 512 tiles are 6.7.  Gated
+  // experts keep GEMM1 on the main kernel.
   int small_pairs = 0;
-  if (rows <= (uint64_t)kSmallGemmRows && !swiglu) {
+  if (rows <= (uint64_t)kSmallGemmRows) {
     cudaError_t ce = small_gemm_max_pairs(&small_pairs);
     if (ce != cudaSuccess) return cuda_fail(ce, "cudaOccupancyMaxActiveClusters(small gemm)");
   }
   const int64_t small_tiles1 = (int64_t)n_seg * ((s->F + 255) / 256);
   const int64_t small_tiles2 = (int64_t)n_seg * ((s->H + 255) / 256);
-  const bool small1 = small_pairs > 0 && small_tiles1 >= 2 * (int64_t)small_pairs;
-  const bool small2 = small_pairs > 0 && small_tiles2 >= 2 * (int64_t)small_pairs;
-  if (small1 || small2) {
-    // token-row boxes: 32 rows for the small kernel, 128 for the main one
-    if ((rc = map_2d(&tm_xp, xp, (uint64_t)s->H, rows, 64, small1 ? 32 : 128, "xp")) != MOE_OK) return rc;
-    if ((rc = map_3d(&tm_w1, w1, (uint64_t)s->F, (uint64_t)s->H, (uint64_t)s->E, 64, 64, "W1")) != MOE_OK) return rc;
-    if ((rc = map_2d(&tm_h, h, (uint64_t)s->F, rows, 64, small2 ? 32 : 128, "h")) != MOE_OK) return rc;
-    if ((rc = map_3d(&tm_w2, w2, (uint64_t)s->H, (uint64_t)s->F, (uint64_t)s->E, 64, 64, "W2")) != MOE_OK) return rc;
-    const int64_t row_blocks_ub = ((int64_t)rows + 2 * kGemmBM - 1) / (2 * kGemmBM) + n_seg;
-    GemmArgs g;
-    g.offsets = seg_offsets;
-    g.E = n_seg;
-    g.E_w = s->E;
-    g.perm = perm;
-    g.gate_w = weights;
-    g.T = s->T;
-    g.status = status;
-    g.wait_limit_ns = kWaitLimitNs;
-    g.N = s->F;
-    g.K = s->H;
-    g.out = h;
-    cudaError_t e =
-        small1 ? launch_small_gemm(kGemmGelu, tm_w1, tm_xp, g, (int)small_tiles1, st, pdl_first)
-               : launch_grouped_gemm(kGemmGelu, tm_xp, tm_w1, g,
-                                     (int)(row_blocks_ub * ((s->F + kGemmBN - 1) / kGemmBN)), st,
-                                     pdl_first);
-    if (e != cudaSuccess) return cuda_fail(e, "expert GEMM1 launch");
-    if ((rc = mark(ev, ev_gemm1, st)) != MOE_OK) return rc;
-    g.N = s->H;
-    g.K = s->F;
-    g.out = out;
-    const int mode2 = combine_k1 ? kGemmCombineK1 : kGemmPlain;
-    e = small2 ? launch_small_gemm(mode2, tm_w2, tm_h, g, (int)small_tiles2, st, pdl)
-               : launch_grouped_gemm(mode2, tm_h, tm_w2, g,
-                                     (int)(row_blocks_ub * ((s->H + kGemmBN - 1) / kGemmBN)), st,
-                                     pdl);
-    if (e != cudaSuccess) return cuda_fail(e, "expert GEMM2 launch");
-    return mark(ev, ev_gemm2, st);
+  const bool small1 = small_pairs > 0 && !swiglu && small_tiles1 >= 2 * (int64_t)small_pairs;
+  int S2 = 0;  // 0: GEMM2 on the main kernel
+  if (small_pairs > 0 && part && !combine_k1) {
+    const int kb2 = (s->F + 63) / 64;
+    double best = 0.0;
+    for (int S = 1; S <= kMaxKSplits && S <= kb2; ++S) {
+      const int64_t n = small_tiles2 * S;
+      if (n < 2 * (int64_t)small_pairs) continue;
+      const double waves = (double)n / small_pairs;
+      const double eff = waves / ceil(waves);
+      if (eff > best + 1e-9) {
+        best = eff;
+        S2 = S;
+      }
+    }
+  } else if (small_pairs > 0 && small_tiles2 >= 2 * (int64_t)small_pairs) {
+    S2 = 1;
   }
+  const bool small2 = S2 > 0;
+
+  // token-row boxes: 32 rows for the small kernel, 128 (a CTA's half of a
+  // 256-row pair tile) for the main one
+  CUtensorMap tm_xp, tm_w1, tm_h, tm_w2;
   const uint64_t w1_cols = (uint64_t)s->F * (swiglu ? 2 : 1);  // SwiGLU: [W_gate | W_up]
-  if ((rc = map_2d(&tm_xp, xp, (uint64_t)s->H, rows, 64, 128, "xp")) != MOE_OK) return rc;
+  if ((rc = map_2d(&tm_xp, xp, (uint64_t)s->H, rows, 64, small1 ? 32 : 128, "xp")) != MOE_OK) return rc;
   if ((rc = map_3d(&tm_w1, w1, w1_cols, (uint64_t)s->H, (uint64_t)s->E, 64, 64, "W1")) != MOE_OK) return rc;
-  if ((rc = map_2d(&tm_h, h, (uint64_t)s->F, rows, 64, 128, "h")) != MOE_OK) return rc;
+  if ((rc = map_2d(&tm_h, h, (uint64_t)s->F, rows, 64, small2 ? 32 : 128, "h")) != MOE_OK) return rc;
   if ((rc = map_3d(&tm_w2, w2, (uint64_t)s->H, (uint64_t)s->F, (uint64_t)s->E, 64, 64, "W2")) != MOE_OK) return rc;
 
-  // pair tiles are 2*kGemmBM rows: a segment with n rows owns ceil(n / 256)
+  // pair tiles of the main kernel are 2*kGemmBM rows: a segment with n rows
+  // owns ceil(n / 256)
   const int64_t row_blocks_ub = ((int64_t)rows + 2 * kGemmBM - 1) / (2 * kGemmBM) + n_seg;
   GemmArgs g;
   g.offsets = seg_offsets;
@@ -371,25 +375,42 @@ int enqueue_expert_gemms(const moe_shape* s, int n_seg, const uint16_t* xp, cons
   g.perm = perm;
   g.gate_w = weights;
   g.T = s->T;
+  g.splits = 1;
+  g.part = nullptr;
+  g.part_stride = 0;
   g.status = status;
   g.wait_limit_ns = kWaitLimitNs;
 
   g.N = s->F;
   g.K = s->H;
   g.out = h;
-  const int out_cols = swiglu ? kGemmBN / 2 : kGemmBN;  // h columns per pair tile
-  int64_t ub = row_blocks_ub * ((s->F + out_cols - 1) / out_cols);
-  cudaError_t e = launch_grouped_gemm(swiglu ? kGemmSwiGLU : kGemmGelu, tm_xp, tm_w1, g,
-                                      (int)(ub < (1 << 30) ? ub : (1 << 30)), st, pdl_first);
+  cudaError_t e;
+  if (small1) {
+    e = launch_small_gemm(kGemmGelu, tm_w1, tm_xp, g, (int)small_tiles1, st, pdl_first);
+  } else {
+    const int out_cols = swiglu ? kGemmBN / 2 : kGemmBN;  // h columns per pair tile
+    const int64_t ub = row_blocks_ub * ((s->F + out_cols - 1) / out_cols);
+    e = launch_grouped_gemm(swiglu ? kGemmSwiGLU : kGemmGelu, tm_xp, tm_w1, g,
+                            (int)(ub < (1 << 30) ? ub : (1 << 30)), st, pdl_first);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM1 launch");
   if ((rc = mark(ev, ev_gemm1, st)) != MOE_OK) return rc;
 
   g.N = s->H;
   g.K = s->F;
   g.out = out;
-  ub = row_blocks_ub * ((s->H + kGemmBN - 1) / kGemmBN);
-  e = launch_grouped_gemm(combine_k1 ? kGemmCombineK1 : kGemmPlain, tm_h, tm_w2, g,
-                          (int)(ub < (1 << 30) ? ub : (1 << 30)), st, pdl);
+  if (small2) {
+    const int mode2 = combine_k1 ? kGemmCombineK1 : S2 > 1 ? kGemmPartial : kGemmPlain;
+    g.splits = S2;
+    g.part = part;
+    g.part_stride = (size_t)rows * s->H;
+    e = launch_small_gemm(mode2, tm_w2, tm_h, g, (int)(small_tiles2 * S2), st, pdl);
+    if (e == cudaSuccess && splits_used) *splits_used = S2;
+  } else {
+    const int64_t ub = row_blocks_ub * ((s->H + kGemmBN - 1) / kGemmBN);
+    e = launch_grouped_gemm(combine_k1 ? kGemmCombineK1 : kGemmPlain, tm_h, tm_w2, g,
+                            (int)(ub < (1 << 30) ? ub : (1 << 30)), st, pdl);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM2 launch");
   return mark(ev, ev_gemm2, st);
 }
@@ -424,9 +445,11 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   if (e != cudaSuccess) return cuda_fail(e, "permute launch");
   if ((rc = mark(ev, 3, st)) != MOE_OK) return rc;
 
+  float* part = part_ptr(ws, s);
+  int splits = 1;
   if ((rc = enqueue_expert_gemms(s, s->E, xp, w1, w2, offsets, h, fuse_combine ? y : Y,
                                  fuse_combine, perm, weights, status_ptr(ws), st, pdl, pdl, ev, 4,
-                                 5)) != MOE_OK)
+                                 5, part, &splits)) != MOE_OK)
     return rc;
   if (fuse_combine) return mark(ev, 6, st);  // no combine kernel: the combine window is empty
 
@@ -438,6 +461,9 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   ca.H = s->H;
   ca.k = s->k;
   ca.y = y;
+  ca.part = splits > 1 ? part : nullptr;  // GEMM2 left fp32 partials per K split
+  ca.splits = splits;
+  ca.part_stride = (size_t)s->T * s->k * s->H;
   e = launch_combine(ca, st, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   return mark(ev, 6, st);
@@ -684,6 +710,9 @@ int moe_combine(const moe_shape* s, const uint16_t* Y, const float* weights, con
   ca.H = s->H;
   ca.k = s->k;
   ca.y = y;
+  ca.part = nullptr;
+  ca.splits = 1;
+  ca.part_stride = 0;
   cudaError_t e = launch_combine(ca, st, /*pdl=*/false);
   return e == cudaSuccess ? MOE_OK : cuda_fail(e, "combine launch");
 }

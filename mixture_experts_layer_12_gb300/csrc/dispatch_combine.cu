@@ -154,6 +154,55 @@ __global__ void __launch_bounds__(CTHREADS) combine_kernel(const CombineArgs a) 
   }
 }
 
+// The combine when the second expert GEMM ran split along K (small batches):
+// a kept row's expert output is the sum of the splits' fp32 partials in
+// split order, rounded to bf16 (as the unsplit GEMM rounds it), then
+// weighted and summed over the token's slots in fp32 exactly as above.
+__global__ void __launch_bounds__(CTHREADS) combine_partial_kernel(const CombineArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int t = blockIdx.x;
+  const int col = (blockIdx.y * CTHREADS + threadIdx.x) * 8;
+  if (col >= a.H) return;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  for (int j = 0; j < a.k; ++j) {
+    const int r = __ldg(a.slot + (size_t)t * a.k + j);
+    if (r < 0) continue;
+    const float wt = __ldg(a.w + (size_t)t * a.k + j);
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    for (int sp = 0; sp < a.splits; ++sp) {
+      const float4* src =
+          reinterpret_cast<const float4*>(a.part + sp * a.part_stride + (size_t)r * a.H + col);
+      const float4 p0 = __ldg(src);
+      const float4 p1 = __ldg(src + 1);
+      v[0] += p0.x;
+      v[1] += p0.y;
+      v[2] += p0.z;
+      v[3] += p0.w;
+      v[4] += p1.x;
+      v[5] += p1.y;
+      v[6] += p1.z;
+      v[7] += p1.w;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      const uint32_t b = pack_bf16x2(v[i], v[i + 1]);  // the expert output in bf16
+      acc[i] = fmaf(wt, bf16_lo(b), acc[i]);
+      acc[i + 1] = fmaf(wt, bf16_hi(b), acc[i + 1]);
+    }
+  }
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  *reinterpret_cast<uint4*>(a.y + (size_t)t * a.H + col) = o;
+}
+
 // xp[r] = x[perm[r] / k] for the kept rows r < offsets[E]: the dispatch-
 // ordered ("expanded") copy of the tokens that the expert GEMM reads with
 // TMA.  One warp per row, 16-byte loads, eight in flight per lane; the copy
@@ -223,7 +272,8 @@ cudaError_t dispatch_combine_set_attributes() {
     e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
   const void* combines[] = {(const void*)combine_kernel<1>, (const void*)combine_kernel<2>,
-                           (const void*)combine_kernel<4>, (const void*)combine_kernel<8>};
+                           (const void*)combine_kernel<4>, (const void*)combine_kernel<8>,
+                           (const void*)combine_partial_kernel};
   for (const void* f : combines)
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -262,6 +312,10 @@ cudaError_t launch_permute(const PermuteArgs& a, int sms, cudaStream_t st, bool 
 }
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st, bool pdl) {
+  if (a.part) {
+    dim3 grid((unsigned)a.T, (unsigned)((a.H + CTHREADS * 8 - 1) / (CTHREADS * 8)), 1);
+    return launch_1d(combine_partial_kernel, grid, CTHREADS, st, pdl, a);
+  }
   const int cols_per_block = CTHREADS * 8 * CCPT;
   dim3 grid((unsigned)a.T, (unsigned)((a.H + cols_per_block - 1) / cols_per_block), 1);
   if (a.k <= 1) return launch_1d(combine_kernel<1>, grid, CTHREADS, st, pdl, a);

@@ -91,10 +91,17 @@ __device__ __forceinline__ float s_gelu(float z) {
 }
 
 // Tiles of one pair increase monotonically: the segment cursor only moves
-// forward.  Each segment with rows owns ceil(N / 256) column tiles.
-__device__ __forceinline__ int s_decode(const SCtrl& c, int tile, int& e) {
+// forward.  Each segment with rows owns ceil(N / 256) column tiles, each in
+// S K-splits (split fastest; the host keeps S <= KB so no range is empty);
+// returns the column block, sets the split and its K range.
+__device__ __forceinline__ int s_decode(const SCtrl& c, int tile, int& e, int S, int KB, int& sp,
+                                        int& kb0, int& kb1) {
   while (tile >= c.tile_start[e + 1]) ++e;
-  return tile - c.tile_start[e];  // column block
+  const int local = tile - c.tile_start[e];
+  sp = local % S;
+  kb0 = (int)(((long long)KB * sp) / S);
+  kb1 = (int)(((long long)KB * (sp + 1)) / S);
+  return local / S;
 }
 
 template <int MODE>
@@ -108,6 +115,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
   uint8_t* sB = smem + S_STAGES * SA_BYTES;  // token tiles
   SCtrl& c = *reinterpret_cast<SCtrl*>(smem + S_STAGES * S_STAGE);
   constexpr bool COMBINE = MODE == kGemmCombineK1;
+  constexpr bool PARTIAL = MODE == kGemmPartial;  // split-K: fp32 partial per split
+  const int S = PARTIAL ? p.splits : 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -131,7 +140,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
         const int n = max(__ldg(p.offsets + e + 1) - o0, 0);
         c.row_off[e] = o0;
         c.rows[e] = min(n, SN);  // the host keeps every segment within SN rows
-        cnt[u] = n > 0 ? NB : 0;
+        cnt[u] = n > 0 ? NB * S : 0;
       }
       sum += cnt[u];
     }
@@ -192,11 +201,12 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       int e = 0;
       bool ok = true;
       for (int tile = pair; tile < n_tiles && ok; tile += n_pairs) {
-        const int nb = s_decode(c, tile, e);
+        int sp, kb0, kb1;
+        const int nb = s_decode(c, tile, e, S, KB, sp, kb0, kb1);
         const int we = e % p.E_w;
         const int wcol = nb * SP_M + rank * SM_CTA;      // this CTA's 128 output columns
         const int trow = c.row_off[e] + rank * SN_CTA;   // this CTA's 32 token rows
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&c.empty[stage], phase ^ 1u, wc)) {
             ok = false;
             break;
@@ -230,12 +240,15 @@ __global__ void __launch_bounds__(S_THREADS, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
+      int e = 0;
       bool ok = true;
       for (int tile = pair; tile < n_tiles && ok; tile += n_pairs) {
+        int sp, kb0, kb1;
+        s_decode(c, tile, e, S, KB, sp, kb0, kb1);
         if (!mbar_wait(&c.tempty[acc], acc_phase ^ 1u, wc)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * SN);
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&c.full[stage], phase, wc)) {
             ok = false;
             break;
@@ -249,7 +262,7 @@ __global__ void __launch_bounds__(S_THREADS, 1)
             // tokens: K-major, 16 elements = 32 bytes into the swizzle row
             const uint64_t ad = sdesc_sw128(a0 + j * 2048, SA_CHUNK, 1024);
             const uint64_t bd = sdesc_sw128(b0 + j * 32, 16, 1024);
-            umma_bf16_pair(d, ad, bd, S_IDESC, (kb | j) != 0 ? 1u : 0u);
+            umma_bf16_pair(d, ad, bd, S_IDESC, (kb != kb0 || j != 0) ? 1u : 0u);
           }
           umma_commit_pair_mc(&c.empty[stage], S_PAIR_MASK);
           if (++stage == S_STAGES) {
@@ -276,7 +289,8 @@ __global__ void __launch_bounds__(S_THREADS, 1)
     uint32_t acc_phase = 0;
     int e = 0;
     for (int tile = pair; tile < n_tiles; tile += n_pairs) {
-      const int nb = s_decode(c, tile, e);
+      int sp, kb0, kb1;
+      const int nb = s_decode(c, tile, e, S, KB, sp, kb0, kb1);
       int got = 1;
       if (lane == 0) got = mbar_wait(&c.tfull[acc], acc_phase, wc);
       got = __shfl_sync(0xffffffffu, got, 0);
@@ -299,6 +313,10 @@ __global__ void __launch_bounds__(S_THREADS, 1)
               float f = __uint_as_float(v[i]);
               if constexpr (MODE == kGemmGelu) f = s_gelu(f);
               size_t orow = (size_t)(row0 + n);
+              if constexpr (PARTIAL) {
+                p.part[(size_t)sp * p.part_stride + orow * (size_t)p.N + col] = f;
+                continue;
+              }
               if constexpr (COMBINE) {
                 // k = 1: the token's only expert row, scaled by its gate
                 const int tok = __ldg(p.perm + row0 + n);
@@ -397,6 +415,7 @@ cudaError_t launch_small_gemm(int mode, const CUtensorMap& tm_w, const CUtensorM
   switch (mode) {
     case kGemmGelu: return s_launch<kGemmGelu>(tm_w, tm_x, a, pairs, st, pdl);
     case kGemmCombineK1: return s_launch<kGemmCombineK1>(tm_w, tm_x, a, pairs, st, pdl);
+    case kGemmPartial: return s_launch<kGemmPartial>(tm_w, tm_x, a, pairs, st, pdl);
     default: return s_launch<kGemmPlain>(tm_w, tm_x, a, pairs, st, pdl);
   }
 }
@@ -406,6 +425,9 @@ cudaError_t small_gemm_set_attributes() {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(small_gemm_kernel<kGemmCombineK1>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(small_gemm_kernel<kGemmPartial>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S_SMEM);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(small_gemm_kernel<kGemmPlain>,

@@ -109,6 +109,9 @@ struct GemmArgs {
   const int32_t* perm;     // kGemmCombineK1: token of dispatch row r (k = 1: perm[r] = t)
   const float* gate_w;     // kGemmCombineK1: gate weight of token t
   int T;                   // kGemmCombineK1: tokens (rows of y)
+  int splits;              // kGemmPartial: K splits (small kernel); 1 otherwise
+  float* part;             // kGemmPartial: fp32 partial outputs, split-major
+  size_t part_stride;      // kGemmPartial: elements between splits
   int* status;
   uint64_t wait_limit_ns;
 };
@@ -122,6 +125,8 @@ constexpr int kGemmPlain = 0;   // GEMM2: no activation
 constexpr int kGemmGelu = 1;    // GEMM1: GELU epilogue
 constexpr int kGemmSwiGLU = 2;  // GEMM1: SiLU(gate) * up epilogue
 constexpr int kGemmCombineK1 = 3;  // GEMM2 + combine for k = 1: y[perm[r]] = w * acc
+constexpr int kGemmPartial = 4;    // small kernel only: split-K, fp32 part[split][r][:]
+constexpr int kMaxKSplits = 4;
 // pdl: launched with programmatic serialization (the predecessor on the
 // stream is this library's kernel of the same call)
 cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
@@ -163,6 +168,11 @@ struct CombineArgs {
   const int32_t* slot;
   int T, H, k;
   uint16_t* y;
+  // when set: the expert outputs are the sum of `splits` fp32 partials
+  // (part[s * part_stride + r * H + c]), rounded to bf16 before weighting
+  const float* part;
+  int splits;
+  size_t part_stride;
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st, bool pdl);
 
