@@ -44,9 +44,6 @@ NCU_TRAFFIC = {
     "prefill/expert_gemm1": {"bytes": 1030029e3 + 222244352, "src": "ffn_gemm.cu", "src_sha": "43fdc202f8c9fbc7"},
     "prefill/expert_gemm2": {"bytes": 1443140e3 + 65493504, "src": "ffn_gemm.cu", "src_sha": "43fdc202f8c9fbc7"},
     "prefill/router": {"bytes": 33692416, "src": "router.cu", "src_sha": "0fe9ac7818d6ca7e"},
-    # decode workload (profiles/decode_weight_stream.md)
-    "decode/expert_gemm1": {"bytes": 940114944 + 4197376, "src": "ffn_gemm.cu", "src_sha": "43fdc202f8c9fbc7"},
-    "decode/expert_gemm2": {"bytes": 941415680 + 3444224, "src": "ffn_gemm.cu", "src_sha": "43fdc202f8c9fbc7"},
 }
 
 
