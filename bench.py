@@ -43,7 +43,10 @@ NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch
     "prefill/expert_gemm1": {"bytes": 1030029e3 + 222244352, "src": "ffn_gemm.cu", "src_sha": "43fdc202f8c9fbc7"},
     "prefill/expert_gemm2": {"bytes": 1443140e3 + 65493504, "src": "ffn_gemm.cu", "src_sha": "43fdc202f8c9fbc7"},
-    "prefill/router": {"bytes": 33692416, "src": "router.cu", "src_sha": "0fe9ac7818d6ca7e"},
+    "prefill/router": {"bytes": 33687808, "src": "router.cu", "src_sha": "b38c2e7e655d8eba"},
+    # decode workload (profiles/decode_weight_stream.md): both GEMMs on the small-batch kernel
+    "decode/expert_gemm1": {"bytes": 940161024 + 3989760, "src": "ffn_gemm_small.cu", "src_sha": "ff59fa4c79617713"},
+    "decode/expert_gemm2": {"bytes": 941419776 + 5054208, "src": "ffn_gemm_small.cu", "src_sha": "ff59fa4c79617713"},
 }
 
 
