@@ -240,7 +240,7 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
     sa.slot = slot;
     sa.ticket = ticket_ptr(ws);
     if ((rc = mark(ev, 0, st)) != MOE_OK) return rc;
-    cudaError_t e = launch_router_small(sa, st);
+    cudaError_t e = launch_router_small(sa, st, ev == nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "router launch");
     if ((rc = mark(ev, 1, st)) != MOE_OK) return rc;
     return mark(ev, 2, st);  // no separate dispatch kernel
@@ -277,10 +277,11 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
   ra.counts = counts;
   ra.offsets = offsets;
   ra.ticket = ticket_ptr(ws);
+  ra.scan_in_dispatch = dispatch_scans(mtiles, s->E) ? 1 : 0;
   ra.status = status_ptr(ws);
   ra.wait_limit_ns = kWaitLimitNs;
   if ((rc = mark(ev, 0, st)) != MOE_OK) return rc;
-  cudaError_t e = launch_router(tm_x, tm_w, ra, st);
+  cudaError_t e = launch_router(tm_x, tm_w, ra, st, ev == nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "router launch");
   if ((rc = mark(ev, 1, st)) != MOE_OK) return rc;
 
@@ -291,7 +292,9 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
   da.E = s->E;
   da.capacity = ra.capacity;
   da.seg_tokens = kSegTokens;
+  da.scan = ra.scan_in_dispatch;
   da.base = hist_ptr(ws);
+  da.counts = counts;
   da.offsets = offsets;
   da.perm = perm;
   da.slot = slot;
@@ -306,7 +309,8 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
 // GEMM1 (+ activation) into h, then GEMM2 into `out`, over T*k rows grouped
 // in n_seg segments: segment i (rows [seg_offsets[i], seg_offsets[i+1]))
 // uses expert i % s->E.  combine_k1: GEMM2 writes y[perm[r]] = w * acc.
-// pdl_first: GEMM1 follows this library's kernel of the same call.
+// pdl_first: GEMM1 starts early (programmatic dependent launch); false only
+// when a timing event sits before it.
 int enqueue_expert_gemms(const moe_shape* s, int n_seg, const uint16_t* xp, const uint16_t* w1,
                          const uint16_t* w2, const int32_t* seg_offsets, uint16_t* h,
                          uint16_t* out, bool combine_k1, const int32_t* perm,
@@ -418,11 +422,10 @@ int enqueue_expert_gemms(const moe_shape* s, int n_seg, const uint16_t* xp, cons
 int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const uint16_t* w1,
                         const uint16_t* w2, const float* weights, const int32_t* offsets,
                         const int32_t* perm, const int32_t* slot, uint16_t* y, void* ws,
-                        cudaStream_t st, void* const* ev = nullptr, bool chained = false) {
+                        cudaStream_t st, void* const* ev = nullptr) {
   int rc;
-  // Kernels after the first start early (programmatic dependent launch);
-  // the first one only when this library's dispatch kernel precedes it
-  // (`chained`).  With timing hooks, events sit between kernels: no overlap.
+  // Every kernel starts early (programmatic dependent launch) unless timing
+  // hooks sit between the kernels.
   const bool pdl = ev == nullptr;
   uint16_t* h = h_ptr(ws, s);
   uint16_t* Y = y_ptr(ws, s);
@@ -441,7 +444,7 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   const bool fuse_combine = s->k == 1;
   pa.slot = slot;
   pa.y_zero = fuse_combine ? y : nullptr;
-  cudaError_t e = launch_permute(pa, sms, st, pdl && chained);
+  cudaError_t e = launch_permute(pa, sms, st, pdl);
   if (e != cudaSuccess) return cuda_fail(e, "permute launch");
   if ((rc = mark(ev, 3, st)) != MOE_OK) return rc;
 
@@ -469,9 +472,11 @@ int enqueue_ffn_combine(const moe_shape* s, int sms, const uint16_t* x, const ui
   return mark(ev, 6, st);
 }
 
-int clear_status(void* ws, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(ws, 0, 128, st);  // status word and ticket
-  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "cudaMemsetAsync(status)");
+// Status word and ticket to zero (a one-warp kernel; with pdl it starts
+// early, like the kernels after it).
+int clear_status(void* ws, cudaStream_t st, bool pdl = true) {
+  cudaError_t e = launch_clear_status(static_cast<int*>(ws), st, pdl);
+  return e == cudaSuccess ? MOE_OK : cuda_fail(e, "status clear launch");
 }
 
 int empty_routing(const moe_shape* s, int32_t* counts, int32_t* offsets, cudaStream_t st) {
@@ -595,8 +600,9 @@ int moe_dispatch(const moe_shape* s, const int32_t* ids, int32_t* counts, int32_
   ha.counts = counts;
   ha.offsets = offsets;
   ha.ticket = ticket_ptr(ws);
+  ha.scan_in_dispatch = dispatch_scans((s->T + kSegTokens - 1) / kSegTokens, s->E) ? 1 : 0;
   ha.status = status_ptr(ws);
-  cudaError_t e = launch_histogram(ha, st);
+  cudaError_t e = launch_histogram(ha, st, /*pdl=*/true);
   if (e != cudaSuccess) return cuda_fail(e, "histogram launch");
   DispatchArgs da;
   da.ids = ids;
@@ -605,7 +611,9 @@ int moe_dispatch(const moe_shape* s, const int32_t* ids, int32_t* counts, int32_
   da.E = s->E;
   da.capacity = cap;
   da.seg_tokens = kSegTokens;
+  da.scan = ha.scan_in_dispatch;
   da.base = hist_ptr(ws);
+  da.counts = counts;
   da.offsets = offsets;
   da.perm = perm;
   da.slot = slot;
@@ -687,7 +695,7 @@ int moe_expert_ffn(const moe_shape* s, int32_t n_segments, const uint16_t* xp, c
   REQUIRE_PTR(seg_offsets);
   REQUIRE_PTR(Y);
   return enqueue_expert_gemms(s, n_segments, xp, w1, w2, seg_offsets, h_ptr(ws, s), Y, false,
-                              nullptr, nullptr, status_ptr(ws), st, false, true, nullptr, 0, 0);
+                              nullptr, nullptr, status_ptr(ws), st, true, true, nullptr, 0, 0);
 }
 
 int moe_combine(const moe_shape* s, const uint16_t* Y, const float* weights, const int32_t* slot,
@@ -772,7 +780,7 @@ int moe_forward_profiled(const moe_shape* s, const uint16_t* x, const uint16_t* 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int sms = 0;
   if ((rc = device_setup(&sms)) != MOE_OK) return rc;
-  if ((rc = clear_status(ws, st)) != MOE_OK) return rc;
+  if ((rc = clear_status(ws, st, events == nullptr)) != MOE_OK) return rc;
   if (s->T == 0) return empty_routing(s, counts, offsets, st);
   REQUIRE_PTR(x);
   REQUIRE_PTR(w_router);
@@ -786,8 +794,7 @@ int moe_forward_profiled(const moe_shape* s, const uint16_t* x, const uint16_t* 
   rc = enqueue_route(s, sms, x, w_router, b_router, ids, weights, counts, offsets, perm, slot, ws, st,
                      events);
   if (rc != MOE_OK) return rc;
-  return enqueue_ffn_combine(s, sms, x, w1, w2, weights, offsets, perm, slot, y, ws, st, events,
-                             /*chained=*/true);
+  return enqueue_ffn_combine(s, sms, x, w1, w2, weights, offsets, perm, slot, y, ws, st, events);
 }
 
 int moe_get_device_status(void* ws, void* stream, int32_t* status) {

@@ -35,7 +35,9 @@ constexpr int DWARPS = DTHREADS / 32;
 __global__ void __launch_bounds__(DTHREADS, 1) dispatch_kernel(const DispatchArgs a) {
   __shared__ int s_base[kMaxExperts];
   __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_tot[kMaxExperts];
   __shared__ int s_wc[DWARPS * kMaxExperts];  // [warp][expert]
+  extern __shared__ int s_cnt[];              // scan: [nseg][E] raw counts
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -48,12 +50,82 @@ __global__ void __launch_bounds__(DTHREADS, 1) dispatch_kernel(const DispatchArg
   pdl_launch_dependents();
   pdl_wait();
 
-  for (int e = tid; e < E; e += DTHREADS) {
-    s_base[e] = a.base[(size_t)seg * E + e];
-    s_off[e] = a.offsets[e];
+  if (a.scan) {
+    // this segment's bases (earlier segments' counts per expert) and the
+    // totals, from all nseg x E counts: G lanes per expert (G | 32) split
+    // the segments, then a butterfly sums them (integers: order-free)
+    const int nseg = (int)gridDim.x;
+    for (int i = tid; i < nseg * E; i += DTHREADS) s_cnt[i] = __ldcg(a.base + i);
+    for (int idx = tid; idx < DWARPS * E; idx += DTHREADS) s_wc[idx] = 0;
+    __syncthreads();
+    int G = 32;
+    while (G > 1 && G * E > DTHREADS) G >>= 1;
+    const int ee = tid / G;
+    const int part = tid % G;
+    int pre = 0, tot = 0;
+    if (ee < E)
+      for (int sg = part; sg < nseg; sg += G) {
+        const int v = s_cnt[sg * E + ee];
+        tot += v;
+        if (sg < seg) pre += v;
+      }
+    for (int off = G / 2; off > 0; off >>= 1) {
+      pre += __shfl_xor_sync(0xffffffffu, pre, off);
+      tot += __shfl_xor_sync(0xffffffffu, tot, off);
+    }
+    if (ee < E && part == 0) {
+      s_base[ee] = pre;
+      s_tot[ee] = tot;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // kept counts (capacity clip) and their exclusive scan: lane l holds
+      // experts 8l .. 8l+7 (E <= 256)
+      int loc[8];
+      int sum = 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int e2 = lane * 8 + u;
+        int n2 = 0;
+        if (e2 < E) {
+          n2 = s_tot[e2];
+          if (a.capacity >= 0) n2 = min(n2, a.capacity);
+        }
+        loc[u] = n2;
+        sum += n2;
+      }
+      int incl = sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      int run = incl - sum;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int e2 = lane * 8 + u;
+        if (e2 < E) {
+          s_off[e2] = run;
+          if (seg == 0) {
+            a.offsets[e2] = run;
+            a.counts[e2] = loc[u];
+          }
+        }
+        run += loc[u];
+      }
+      if (lane == 31) {
+        s_off[E] = incl;
+        if (seg == 0) a.offsets[E] = incl;
+      }
+    }
+  } else {
+    for (int e = tid; e < E; e += DTHREADS) {
+      s_base[e] = a.base[(size_t)seg * E + e];
+      s_off[e] = a.offsets[e];
+    }
+    if (tid == 0) s_off[E] = a.offsets[E];
+    for (int idx = tid; idx < DWARPS * E; idx += DTHREADS) s_wc[idx] = 0;
   }
-  if (tid == 0) s_off[E] = a.offsets[E];
-  for (int idx = tid; idx < DWARPS * E; idx += DTHREADS) s_wc[idx] = 0;
   __syncthreads();
 
   int e = -1;
@@ -269,6 +341,9 @@ cudaError_t dispatch_combine_set_attributes() {
   cudaError_t e = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(kDispatchScanMaxCounts * sizeof(int)));
+  if (e == cudaSuccess)
     e = cudaFuncSetAttribute(permute_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
   const void* combines[] = {(const void*)combine_kernel<1>, (const void*)combine_kernel<2>,
@@ -283,10 +358,12 @@ cudaError_t dispatch_combine_set_attributes() {
 
 // Plain 1-D launch, optionally with programmatic serialization (pdl).
 template <typename Kernel, typename Args>
-cudaError_t launch_1d(Kernel k, dim3 grid, int threads, cudaStream_t st, bool pdl, const Args& a) {
+cudaError_t launch_1d(Kernel k, dim3 grid, int threads, cudaStream_t st, bool pdl, const Args& a,
+                      size_t smem = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   if (pdl) {
@@ -297,9 +374,24 @@ cudaError_t launch_1d(Kernel k, dim3 grid, int threads, cudaStream_t st, bool pd
   return cudaLaunchKernelEx(&cfg, k, a);
 }
 
+// Zeroes a call's status block (status word and ticket, 32 ints) as a
+// kernel: a memset node between two kernels costs several microseconds of
+// serialisation, and a kernel can start early under programmatic dependent
+// launch like every other kernel of the call.
+__global__ void clear_status_kernel(int* p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  p[threadIdx.x] = 0;
+}
+
+cudaError_t launch_clear_status(int* p, cudaStream_t st, bool pdl) {
+  return launch_1d(clear_status_kernel, dim3(1), 32, st, pdl, p);
+}
+
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st, bool pdl) {
   const int nseg = (a.T + a.seg_tokens - 1) / a.seg_tokens;
-  return launch_1d(dispatch_kernel, dim3((unsigned)nseg), DTHREADS, st, pdl, a);
+  const size_t smem = a.scan ? (size_t)nseg * a.E * sizeof(int) : 0;
+  return launch_1d(dispatch_kernel, dim3((unsigned)nseg), DTHREADS, st, pdl, a, smem);
 }
 
 cudaError_t launch_permute(const PermuteArgs& a, int sms, cudaStream_t st, bool pdl) {

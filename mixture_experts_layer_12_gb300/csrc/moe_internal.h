@@ -37,6 +37,7 @@ struct RouterArgs {
   int32_t* counts;    // [E]
   int32_t* offsets;   // [E+1]
   unsigned int* ticket;  // zero before the launch
+  int scan_in_dispatch;  // 1: publish raw per-tile counts only (see dispatch_scans)
   int* status;
   uint64_t wait_limit_ns;
 };
@@ -44,7 +45,7 @@ struct RouterArgs {
 // tm_x: x [T, H] bf16, box {64, 128}, 128B swizzle.
 // tm_w: w_router [H, E] bf16, box {64, 64}, 128B swizzle.
 cudaError_t launch_router(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterArgs& a,
-                          cudaStream_t st);
+                          cudaStream_t st, bool pdl);
 size_t router_smem_bytes(int E);
 
 // ---- small-batch route (router + dispatch in one launch, CUDA cores):
@@ -66,7 +67,7 @@ struct SmallRouteArgs {
   int32_t* slot;
   unsigned int* ticket;  // zero before the launch
 };
-cudaError_t launch_router_small(const SmallRouteArgs& a, cudaStream_t st);
+cudaError_t launch_router_small(const SmallRouteArgs& a, cudaStream_t st, bool pdl);
 // Clusters of `splits` router CTAs that can be resident at once.
 cudaError_t router_max_clusters(int E, int splits, int* out);
 
@@ -80,23 +81,40 @@ struct HistArgs {
   int32_t* counts;
   int32_t* offsets;
   unsigned int* ticket;  // zero before the launch
+  int scan_in_dispatch;  // 1: publish raw per-segment counts only (see dispatch_scans)
   int* status;
 };
-cudaError_t launch_histogram(const HistArgs& a, cudaStream_t st);
+cudaError_t launch_histogram(const HistArgs& a, cudaStream_t st, bool pdl);
 
 // ---- dispatch: one CTA per segment ranks its assignments within each
 //      expert and scatters perm / slot (capacity clip applied).
+// With scan = 1 (dispatch_scans: few segments) `base` holds the raw
+// per-segment counts and every CTA derives its own bases and the expert
+// offsets from them (CTA 0 also writes counts / offsets): the producer's
+// last-CTA scan, a serial step between the two kernels, disappears.  With
+// scan = 0 the producer's last CTA has already turned `base` into exclusive
+// bases and written counts / offsets.
+constexpr int kDispatchScanMaxCounts = 16384;  // nseg * E ints held in shared memory
+inline bool dispatch_scans(int nseg, int E) {
+  // every CTA reads all counts: nseg^2 * E reads in all, kept to 16 MB
+  return (long long)nseg * E <= kDispatchScanMaxCounts &&
+         (long long)nseg * nseg * E <= (1LL << 22);
+}
 struct DispatchArgs {
   const int32_t* ids;
   int T, k, E;
   int capacity;  // -1: unlimited
   int seg_tokens;
-  const int32_t* base;     // [nseg][E] exclusive bases from the scan
-  const int32_t* offsets;  // [E+1]
+  int scan;
+  const int32_t* base;  // [nseg][E]: raw counts (scan) or exclusive bases
+  int32_t* counts;      // [E] (written when scan)
+  int32_t* offsets;     // [E+1] (read, or written when scan)
   int32_t *perm, *slot;
   int* status;
 };
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st, bool pdl);
+// The status block (32 ints at p) set to zero by a one-warp kernel.
+cudaError_t launch_clear_status(int* p, cudaStream_t st, bool pdl);
 
 // ---- grouped expert GEMM (tcgen05 + TMA, persistent ragged scheduler).
 struct GemmArgs {
@@ -127,8 +145,11 @@ constexpr int kGemmSwiGLU = 2;  // GEMM1: SiLU(gate) * up epilogue
 constexpr int kGemmCombineK1 = 3;  // GEMM2 + combine for k = 1: y[perm[r]] = w * acc
 constexpr int kGemmPartial = 4;    // small kernel only: split-K, fp32 part[split][r][:]
 constexpr int kMaxKSplits = 4;
-// pdl: launched with programmatic serialization (the predecessor on the
-// stream is this library's kernel of the same call)
+// pdl: launched with programmatic stream serialization.  Every kernel of
+// this library executes griddepcontrol.wait before its first global-memory
+// access, which waits for the whole predecessor grid (this library's or the
+// caller's) to complete and its writes to become visible; the early launch
+// overlaps only launch latency and shared-memory setup.
 cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
                                 const GemmArgs& a, int max_tiles, cudaStream_t st, bool pdl);
 size_t grouped_gemm_smem_bytes();

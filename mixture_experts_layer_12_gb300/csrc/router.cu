@@ -21,17 +21,18 @@
 //     into rank r's shared memory with DSMEM stores; after one cluster
 //     barrier every rank sums its rows' S partials locally in rank order
 //     (deterministic);
-//   * TopK: for E <= 64 one thread per token streams the E logits through a
-//     k-entry insertion list; for larger E one warp per token (lane l holds
-//     experts l, l+32, ...) runs k rounds of a shuffle argmax over (value,
-//     index) pairs.  Larger value first, equal values -> lower index.  Gate
+//   * TopK: 8 lanes per token, each holding its share of the E logits
+//     (4-expert chunks) in registers; k rounds of a local scan plus a
+//     shuffle argmax over the 8 lanes.  Larger value first, equal values ->
+//     lower index.  Gate
 //     weights (fp32 expf): softmax over the k logits, or (the article's
 //     section 2.1 order) softmax over all E then the k probabilities, with
 //     or without renormalisation;
 //   * per-tile expert counts go to the workspace (summed through DSMEM
-//     atomics into rank 0); the last tile to finish (an atomic ticket, no
-//     waiting) scans them into counts / offsets (with the capacity clip) and
-//     per-tile exclusive bases for the dispatch kernel.
+//     atomics into rank 0).  For few tiles the dispatch kernel scans them;
+//     otherwise the last tile to finish (an atomic ticket, no waiting) scans
+//     them into counts / offsets (with the capacity clip) and per-tile
+//     exclusive bases for the dispatch kernel.
 #include <math.h>
 
 #include "tc_common.cuh"
@@ -214,7 +215,6 @@ __global__ void __launch_bounds__(RTHREADS)
   const int kb0 = (int)(((long long)KB * s) / S);
   const int kb1 = (int)(((long long)KB * (s + 1)) / S);
   pdl_launch_dependents();  // the dispatch kernel may be scheduled now; it waits for us
-  pdl_wait();               // no-op: launched with full serialization
   const int nkb = kb1 - kb0;
 
   if (threadIdx.x == 0) {
@@ -234,6 +234,9 @@ __global__ void __launch_bounds__(RTHREADS)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The setup above touched only shared memory and TMEM; from here on
+  // global memory (x, the outputs) may belong to the predecessor grid.
+  pdl_wait();
   const uint32_t tmem = c.tmem_base;
   const WaitCtl wc{&c.abort_flag, a.status, a.wait_limit_ns};
 
@@ -296,25 +299,38 @@ __global__ void __launch_bounds__(RTHREADS)
   const bool have = ok && nkb > 0 && c.abort_flag == 0;
   cluster_sync_all();  // no rank still reads its pipeline buffers (now receive buffers)
 
-  // ---- push this rank's partial of row `row` to the rank that owns it
-  // (warps 0-3: warp w may read TMEM lanes 32w .. 32w+31)
-  if (warp < 4) {
-    const int row = warp * 32 + lane;
+  // ---- push this rank's partial of row `row` to the rank that owns it.
+  // Warps w and w+4 read TMEM lanes 32(w%4) .. +31 (a warp's own lane
+  // quadrant) and take alternate 16-column chunks, up to four loads in
+  // flight per wait.
+  {
+    const int q = warp & 3;
+    const int h = warp >> 2;
+    const int row = q * 32 + lane;
     const int owner = row / rpc;
     const uint32_t dst =
         dsmem_map(smem_u32(recv + (size_t)(s * rpc + row % rpc) * C::PITCH), (uint32_t)owner);
-    const uint32_t tb = tmem + ((uint32_t)(warp * 32) << 16);
-    for (int col = 0; col < a.npad; col += 16) {
-      uint32_t v[16];
-      tmem_ld_x16(tb + (uint32_t)col, v);
+    const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16);
+    const int nch = a.npad / 16;
+    for (int c0 = h; c0 < nch; c0 += 8) {  // chunks c0, c0+2, c0+4, c0+6
+      uint32_t v[4][16];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c0 + 2 * u < nch) tmem_ld_x16(tb + (uint32_t)((c0 + 2 * u) * 16), v[u]);
       tmem_ld_wait();
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const float f0 = have ? __uint_as_float(v[4 * g + 0]) : 0.f;
-        const float f1 = have ? __uint_as_float(v[4 * g + 1]) : 0.f;
-        const float f2 = have ? __uint_as_float(v[4 * g + 2]) : 0.f;
-        const float f3 = have ? __uint_as_float(v[4 * g + 3]) : 0.f;
-        dsmem_st_v4(dst + (uint32_t)((col + 4 * g) * 4), f0, f1, f2, f3);
+      for (int u = 0; u < 4; ++u) {
+        if (c0 + 2 * u < nch) {
+          const int col = (c0 + 2 * u) * 16;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const float f0 = have ? __uint_as_float(v[u][4 * g + 0]) : 0.f;
+            const float f1 = have ? __uint_as_float(v[u][4 * g + 1]) : 0.f;
+            const float f2 = have ? __uint_as_float(v[u][4 * g + 2]) : 0.f;
+            const float f3 = have ? __uint_as_float(v[u][4 * g + 3]) : 0.f;
+            dsmem_st_v4(dst + (uint32_t)((col + 4 * g) * 4), f0, f1, f2, f3);
+          }
+        }
       }
     }
   }
@@ -326,37 +342,104 @@ __global__ void __launch_bounds__(RTHREADS)
   }
   cluster_sync_all();  // every partial of this rank's rows has arrived
 
-  // ---- reduce the S partials of each owned row in place (slot 0): sum over
-  // ranks ascending, then + bias; all threads, one (row, expert) each
-  for (int idx = threadIdx.x; idx < rpc * a.E; idx += RTHREADS) {
-    const int li = idx / a.E;
-    const int e = idx - li * a.E;
-    float sum = recv[(size_t)li * C::PITCH + e];
-    for (int r = 1; r < S; ++r) sum += recv[(size_t)(r * rpc + li) * C::PITCH + e];
-    if (a.bias) sum += __ldg(a.bias + e);
-    recv[(size_t)li * C::PITCH + e] = isnan(sum) ? -INFINITY : sum;
-  }
-  __syncthreads();
-  auto logit = [&](int li, int e) -> float { return recv[(size_t)li * C::PITCH + e]; };
-  if (a.E <= 64) {
-    for (int li = threadIdx.x; li < rpc; li += RTHREADS) {
+  // ---- per owned token: sum its S partial rows (ranks ascending, then +
+  // bias; NaN -> -inf), TopK and the gate weights.  A group of 8 lanes takes
+  // one token: lane g holds the 4-expert chunks g, g+8, g+16, ... in
+  // registers.  Each of the k rounds scans the lane's untaken logits in
+  // ascending expert order (strict '>' keeps the lower index on ties), a
+  // 3-step shuffle argmax over the 8 lanes picks the round's expert (larger
+  // value, then lower index) and its owner marks it taken.  All tokens of
+  // the CTA are in flight at once.
+  {
+    constexpr int GS = 8;
+    constexpr int NCH = 2 * NB64;  // chunks per lane when E = 64 * NB64
+    constexpr int NV = NCH * 4;    // logits per lane
+    static_assert(kMaxTopK <= GS, "lane g writes choice g");
+    static_assert(NV <= 32, "taken mask");
+    const int g = lane & (GS - 1);
+    const unsigned gmask = 0xffu << (lane & ~(GS - 1));
+    for (int li0 = 0; li0 < rpc; li0 += RTHREADS / GS) {
+      const int li = li0 + (int)threadIdx.x / GS;
       const int t = m0 + s * rpc + li;
-      if (t >= a.T) continue;
-      TopK8 tk;
-      tk.init();
-      for (int e = 0; e < a.E; ++e) tk.push(logit(li, e), e, a.k);
-      const float mx = tk.v[0];
+      if (li >= rpc || t >= a.T) continue;  // uniform over the group
+      float lv[NV];
+      uint32_t taken = 0;  // bit q: logit q unavailable (taken, or past E)
+#pragma unroll
+      for (int cc = 0; cc < NCH; ++cc) {
+        const int e0 = (g + cc * GS) * 4;
+        if (e0 < a.E) {  // E % 8 == 0: the whole chunk is in range
+          float4 acc = *reinterpret_cast<const float4*>(recv + (size_t)li * C::PITCH + e0);
+          for (int r = 1; r < S; ++r) {
+            const float4 p =
+                *reinterpret_cast<const float4*>(recv + (size_t)(r * rpc + li) * C::PITCH + e0);
+            acc.x += p.x;
+            acc.y += p.y;
+            acc.z += p.z;
+            acc.w += p.w;
+          }
+          float v4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float v = v4[i];
+            if (a.bias) v += __ldg(a.bias + e0 + i);
+            lv[cc * 4 + i] = isnan(v) ? -INFINITY : v;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) lv[cc * 4 + i] = -INFINITY;
+          taken |= 0xfu << (cc * 4);
+        }
+      }
+      float sel_v[kMaxTopK];
+      int sel_id[kMaxTopK];
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j) {
+        sel_v[j] = -INFINITY;
+        sel_id[j] = 0;
+        if (j < a.k) {
+          float bv = -INFINITY;
+          int bq = -1;
+#pragma unroll
+          for (int q = 0; q < NV; ++q)
+            if (!((taken >> q) & 1u) && (bq < 0 || lv[q] > bv)) {
+              bv = lv[q];
+              bq = q;
+            }
+          // local index q = 4*cc + i  <->  expert 4*(g + 8*cc) + i
+          int be = bq < 0 ? 0x7fffffff : ((g + (bq >> 2) * GS) << 2) + (bq & 3);
+#pragma unroll
+          for (int off = GS / 2; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(gmask, bv, off);
+            const int oe = __shfl_xor_sync(gmask, be, off);
+            if (ov > bv || (ov == bv && oe < be)) {
+              bv = ov;
+              be = oe;
+            }
+          }
+          if (be != 0x7fffffff && ((be >> 2) & (GS - 1)) == g)
+            taken |= 1u << (((be >> 5) << 2) | (be & 3));
+          sel_v[j] = bv;
+          sel_id[j] = be;
+        }
+      }
+      const float mx = sel_v[0];
       float ex[kMaxTopK];
       float z = 0.f;
 #pragma unroll
       for (int j = 0; j < kMaxTopK; ++j) {
-        ex[j] = j < a.k ? expf(tk.v[j] - mx) : 0.f;
+        ex[j] = j < a.k ? expf(sel_v[j] - mx) : 0.f;
         z += ex[j];
       }
       if (a.gating != MOE_GATE_TOPK_SOFTMAX) {
         // softmax over all E logits first: p_j = exp(l_j - max) / sum_e exp(l_e - max)
         float zall = 0.f;
-        for (int e = 0; e < a.E; ++e) zall += expf(logit(li, e) - mx);
+#pragma unroll
+        for (int cc = 0; cc < NCH; ++cc)
+          if ((g + cc * GS) * 4 < a.E)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) zall += expf(lv[cc * 4 + i] - mx);
+#pragma unroll
+        for (int off = GS / 2; off > 0; off >>= 1) zall += __shfl_xor_sync(gmask, zall, off);
         float zsel = 0.f;
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j) {
@@ -365,81 +448,18 @@ __global__ void __launch_bounds__(RTHREADS)
         }
         z = a.gating == MOE_GATE_SOFTMAX_TOPK ? 1.f : zsel;
       }
-#pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) {
-        if (j < a.k) {
-          a.ids[(size_t)t * a.k + j] = tk.id[j];
-          a.weights[(size_t)t * a.k + j] = ex[j] / z;
-          atomicAdd(&c.hist[tk.id[j]], 1);
-        }
-      }
-    }
-  } else {
-    constexpr int NU = 2 * NB64;  // 32-expert groups per lane
-    for (int li = warp; li < rpc; li += RTHREADS / 32) {
-      const int t = m0 + s * rpc + li;
-      if (t >= a.T) continue;  // warp-uniform
-      float v[NU];
-      uint32_t taken = 0;  // bit u: expert lane + 32u unavailable
-#pragma unroll
-      for (int u = 0; u < NU; ++u) {
-        const int e = lane + 32 * u;
-        v[u] = -INFINITY;
-        if (e < a.E)
-          v[u] = logit(li, e);
-        else
-          taken |= 1u << u;
-      }
+      // lane g writes the token's g-th choice (k <= 8 = GS)
       int my_id = 0;
-      float my_val = 0.f;
-      for (int j = 0; j < a.k; ++j) {
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
+      float my_w = 0.f;
 #pragma unroll
-        for (int u = 0; u < NU; ++u) {
-          const int e = lane + 32 * u;
-          if (!((taken >> u) & 1u) && (v[u] > bv || (v[u] == bv && e < be))) {
-            bv = v[u];
-            be = e;
-          }
+      for (int j = 0; j < kMaxTopK; ++j)
+        if (j == g) {
+          my_id = sel_id[j];
+          my_w = ex[j] / z;
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-          const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-          if (ov > bv || (ov == bv && oe < be)) {
-            bv = ov;
-            be = oe;
-          }
-        }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        if (lane == j) {
-          my_id = be;
-          my_val = bv;
-        }
-      }
-      const float mx = __shfl_sync(0xffffffffu, my_val, 0);
-      float ex = lane < a.k ? expf(my_val - mx) : 0.f;
-      float z = ex;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-      if (a.gating != MOE_GATE_TOPK_SOFTMAX) {
-        // softmax over all E logits first (lane sums its experts, warp reduces)
-        float zall = 0.f;
-#pragma unroll
-        for (int u = 0; u < NU; ++u)
-          if (lane + 32 * u < a.E) zall += expf(v[u] - mx);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) zall += __shfl_xor_sync(0xffffffffu, zall, off);
-        ex = ex / zall;
-        float zsel = ex;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) zsel += __shfl_xor_sync(0xffffffffu, zsel, off);
-        z = a.gating == MOE_GATE_SOFTMAX_TOPK ? 1.f : zsel;
-      }
-      if (lane < a.k) {
-        a.ids[(size_t)t * a.k + lane] = my_id;
-        a.weights[(size_t)t * a.k + lane] = ex / z;
+      if (g < a.k) {
+        a.ids[(size_t)t * a.k + g] = my_id;
+        a.weights[(size_t)t * a.k + g] = my_w;
         atomicAdd(&c.hist[my_id], 1);
       }
     }
@@ -457,6 +477,7 @@ __global__ void __launch_bounds__(RTHREADS)
   if (s == 0) {
     for (int e = threadIdx.x; e < a.E; e += RTHREADS)
       a.hist[(size_t)blockIdx.y * a.E + e] = c.hist[e];
+    if (a.scan_in_dispatch) return;  // the dispatch kernel scans (uniform over the CTA)
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -474,20 +495,21 @@ __global__ void __launch_bounds__(RTHREADS)
 
 template <int NB64>
 cudaError_t launch_nb(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterArgs& a,
-                      cudaStream_t st) {
+                      cudaStream_t st, bool pdl) {
   using C = RCfg<NB64>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.splits, (unsigned)((a.T + RBM - 1) / RBM), 1);
   cfg.blockDim = dim3(RTHREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)a.splits;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  if (pdl) set_pdl_attr(attr[1]);
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, router_kernel<NB64>, tm_x, tm_w, a);
 }
 
@@ -524,7 +546,7 @@ __global__ void __launch_bounds__(HTHREADS) histogram_kernel(const HistArgs a) {
   __shared__ int s_tot[kMaxExperts];
   __shared__ int s_last;
   pdl_launch_dependents();
-  pdl_wait();  // no-op: launched with full serialization
+  pdl_wait();  // the predecessor grid (any) has completed
   for (int e = threadIdx.x; e < a.E; e += HTHREADS) s_hist[e] = 0;
   __syncthreads();
   const int n = min(a.seg_tokens, a.T - (int)blockIdx.x * a.seg_tokens) * a.k;
@@ -540,6 +562,7 @@ __global__ void __launch_bounds__(HTHREADS) histogram_kernel(const HistArgs a) {
   if (bad) record_status(a.status, MOE_DEV_BAD_ID);
   __syncthreads();
   for (int e = threadIdx.x; e < a.E; e += HTHREADS) a.hist[(size_t)blockIdx.x * a.E + e] = s_hist[e];
+  if (a.scan_in_dispatch) return;  // the dispatch kernel scans
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) s_last = (atomicAdd(a.ticket, 1u) == gridDim.x - 1) ? 1 : 0;
@@ -575,7 +598,7 @@ __global__ void __launch_bounds__(SR_THREADS) router_small_kernel(const SmallRou
   __shared__ int s_run[NE];
   __shared__ int s_off[NE + 1];
   pdl_launch_dependents();
-  pdl_wait();  // no-op: launched with full serialization
+  pdl_wait();  // the predecessor grid (any) has completed
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -741,22 +764,38 @@ cudaError_t router_set_attributes() {
   return set_attr_nb<4>();
 }
 
-cudaError_t launch_router_small(const SmallRouteArgs& a, cudaStream_t st) {
-  const dim3 grid((unsigned)a.T);
-  if (a.E <= 8) router_small_kernel<8><<<grid, SR_THREADS, 0, st>>>(a);
-  else if (a.E <= 16) router_small_kernel<16><<<grid, SR_THREADS, 0, st>>>(a);
-  else if (a.E <= 32) router_small_kernel<32><<<grid, SR_THREADS, 0, st>>>(a);
-  else router_small_kernel<64><<<grid, SR_THREADS, 0, st>>>(a);
-  return cudaGetLastError();
+// One CTA per token; with pdl, programmatic stream serialization.
+template <typename Args>
+cudaError_t launch_plain(void (*k)(Args), unsigned grid, int threads, cudaStream_t st, bool pdl,
+                         const Args& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    set_pdl_attr(attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, k, a);
+}
+
+cudaError_t launch_router_small(const SmallRouteArgs& a, cudaStream_t st, bool pdl) {
+  const unsigned grid = (unsigned)a.T;
+  if (a.E <= 8) return launch_plain(router_small_kernel<8>, grid, SR_THREADS, st, pdl, a);
+  if (a.E <= 16) return launch_plain(router_small_kernel<16>, grid, SR_THREADS, st, pdl, a);
+  if (a.E <= 32) return launch_plain(router_small_kernel<32>, grid, SR_THREADS, st, pdl, a);
+  return launch_plain(router_small_kernel<64>, grid, SR_THREADS, st, pdl, a);
 }
 
 cudaError_t launch_router(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterArgs& a,
-                          cudaStream_t st) {
+                          cudaStream_t st, bool pdl) {
   switch ((a.E + 63) / 64) {
-    case 1: return launch_nb<1>(tm_x, tm_w, a, st);
-    case 2: return launch_nb<2>(tm_x, tm_w, a, st);
-    case 3: return launch_nb<3>(tm_x, tm_w, a, st);
-    default: return launch_nb<4>(tm_x, tm_w, a, st);
+    case 1: return launch_nb<1>(tm_x, tm_w, a, st, pdl);
+    case 2: return launch_nb<2>(tm_x, tm_w, a, st, pdl);
+    case 3: return launch_nb<3>(tm_x, tm_w, a, st, pdl);
+    default: return launch_nb<4>(tm_x, tm_w, a, st, pdl);
   }
 }
 
@@ -786,10 +825,9 @@ cudaError_t router_max_clusters(int E, int splits, int* out) {
   return cudaSuccess;
 }
 
-cudaError_t launch_histogram(const HistArgs& a, cudaStream_t st) {
+cudaError_t launch_histogram(const HistArgs& a, cudaStream_t st, bool pdl) {
   const int nseg = (a.T + a.seg_tokens - 1) / a.seg_tokens;
-  histogram_kernel<<<nseg, HTHREADS, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_plain(histogram_kernel, (unsigned)nseg, HTHREADS, st, pdl, a);
 }
 
 }  // namespace moe
