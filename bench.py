@@ -43,7 +43,10 @@ NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch
     "prefill/expert_gemm1": {"bytes": 1030029e3 + 222244352, "src": "ffn_gemm.cu", "src_sha": "43fdc202f8c9fbc7"},
     "prefill/expert_gemm2": {"bytes": 1443140e3 + 65493504, "src": "ffn_gemm.cu", "src_sha": "43fdc202f8c9fbc7"},
-    "prefill/router": {"bytes": 33687808, "src": "router.cu", "src_sha": "b38c2e7e655d8eba"},
+    "prefill/router": {"bytes": 33692160, "src": "router.cu", "src_sha": "74867526327d7f28"},
+    # router sweep, k = 1 (profiles/router_prefill.md): router_kernel + dispatch_kernel of one call
+    "router_k1/router+dispatch": {"bytes": 17897728 + 40448, "src": ["router.cu", "dispatch_combine.cu"],
+                                  "src_sha": ["74867526327d7f28", "456cbd9bca80ff77"]},
     # decode workload (profiles/decode_weight_stream.md): both GEMMs on the small-batch kernel
     "decode/expert_gemm1": {"bytes": 940161024 + 3989760, "src": "ffn_gemm_small.cu", "src_sha": "ff59fa4c79617713"},
     "decode/expert_gemm2": {"bytes": 941419776 + 5054208, "src": "ffn_gemm_small.cu", "src_sha": "ff59fa4c79617713"},
@@ -91,6 +94,17 @@ def workload_desc(cfg):
 def src_sha(name):
     with open(os.path.join(ROOT, "mixture_experts_layer_12_gb300", "csrc", name), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def ncu_traffic(key):
+    """DRAM bytes of one launch from NCU_TRAFFIC, or None once a source the
+    figure was taken on has changed."""
+    tr = NCU_TRAFFIC.get(key)
+    if not tr:
+        return None
+    srcs = tr["src"] if isinstance(tr["src"], list) else [tr["src"]]
+    shas = tr["src_sha"] if isinstance(tr["src_sha"], list) else [tr["src_sha"]]
+    return tr["bytes"] if all(src_sha(f) == h for f, h in zip(srcs, shas)) else None
 
 
 # ------------------------------------------------------------------ clocks --
@@ -375,11 +389,12 @@ def run_route_only(args, cfg, device):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "step": "moe_route (router + dispatch)",
                    "l2": f"{copies} rotating copies of x ({copies * x0.numel() * 2 / 1e6:.0f} MB > L2)"},
-        "gpu_launches": (1 if moe.moe_forward_plan(s)[0] else 2) * K,  # router (+ dispatch)
+        # status clear + router (+ dispatch)
+        "gpu_launches": (2 if moe.moe_forward_plan(s)[0] else 3) * K,
         "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks.get("hbm_gbs"),
                      "unit": "GB/s", "frac": round(ach / peaks.get("hbm_gbs", 6800.0), 4),
                      "peak_kind": f"HBM copy ({src})", "kernel": "router+dispatch",
-                     "bytes_per_launch": route_bytes, "traffic": None},
+                     "bytes_per_launch": route_bytes, "traffic": ncu_traffic(f"{cfg.name}/router+dispatch")},
         "clocks": clk,
         "e2e": e2e,
     }
@@ -533,8 +548,7 @@ def run_ours(args):
         roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(ach / peak, 4), "peak_kind": f"HBM copy ({peak_src})",
                 "kernel": dominant, "bytes_per_launch": dk["bytes"]}
-    tr = NCU_TRAFFIC.get(f"{cfg.name}/{dominant}")
-    roof["traffic"] = tr["bytes"] if tr and tr.get("src_sha") == src_sha(tr["src"]) else None
+    roof["traffic"] = ncu_traffic(f"{cfg.name}/{dominant}")
 
     # end to end through the public API with host buffers: H2D of x, the
     # forward, D2H of y, every step, inside the timed region.  The headline
@@ -597,7 +611,7 @@ def run_ours(args):
                    "per_kernel_sum_ms": round(sum(per_kernel.values()), 5),
                    "l2": "inputs larger than L2: every step streams all expert weights "
                          f"({2 * (3 if cfg.act == 'swiglu' else 2) * cfg.E * cfg.H * cfg.F / 1e9:.2f} GB)"},
-        "gpu_launches": len(launched) * K,
+        "gpu_launches": (len(launched) + 1) * K,  # + the status clear that opens each call
         "roofline": roof,
         "kernels": kernels,
         "clocks": clk,

@@ -188,6 +188,16 @@ def test_router_edge_shapes(T, H, E, k, bias):
     routing_parity(cfg, inputs, r)
 
 
+@pytest.mark.parametrize("T,E,k", [(2048, 128, 2), (2688, 64, 3), (3840, 128, 1), (6400, 16, 2)])
+def test_router_tile_counts(T, E, k):
+    # 16, 21, 30 and 50 tiles of 128 tokens: the K split per tile (the most
+    # whose clusters fit in one wave) changes across these counts
+    cfg = moe_synth.MoEConfig("tiles", T=T, H=1024, F=0, E=E, k=k, seed=31)
+    inputs = moe_synth.make_inputs(cfg, with_ffn=False)
+    r = gpu_route(cfg, to_dev(inputs))
+    routing_parity(cfg, inputs, r)
+
+
 def test_router_duplicate_columns_tie_to_lower_index():
     cfg = moe_synth.MoEConfig("ties", T=200, H=256, F=0, E=16, k=4, seed=12)
     inputs = moe_synth.make_inputs(cfg, with_ffn=False)
