@@ -49,6 +49,9 @@ __global__ void __launch_bounds__(DTHREADS, 1) dispatch_kernel(const DispatchArg
   const int n = min(a.seg_tokens * a.k, Tk - i0);
   pdl_launch_dependents();
   pdl_wait();
+  // this thread's assignment, loaded first so that its latency overlaps the
+  // counts' below
+  int e = tid < n ? __ldg(a.ids + i0 + tid) : -1;
 
   if (a.scan) {
     // this segment's bases (earlier segments' counts per expert) and the
@@ -119,20 +122,16 @@ __global__ void __launch_bounds__(DTHREADS, 1) dispatch_kernel(const DispatchArg
       }
     }
   } else {
-    for (int e = tid; e < E; e += DTHREADS) {
-      s_base[e] = a.base[(size_t)seg * E + e];
-      s_off[e] = a.offsets[e];
+    for (int x = tid; x < E; x += DTHREADS) {
+      s_base[x] = a.base[(size_t)seg * E + x];
+      s_off[x] = a.offsets[x];
     }
     if (tid == 0) s_off[E] = a.offsets[E];
     for (int idx = tid; idx < DWARPS * E; idx += DTHREADS) s_wc[idx] = 0;
   }
   __syncthreads();
 
-  int e = -1;
-  if (tid < n) {
-    e = __ldg(a.ids + i0 + tid);
-    if (e < 0 || e >= E) e = -1;
-  }
+  if (e < 0 || e >= E) e = -1;
   const unsigned peers = __match_any_sync(0xffffffffu, e);
   const int rank_w = __popc(peers & ((1u << lane) - 1u));
   if (e >= 0 && rank_w == 0) s_wc[warp * E + e] = __popc(peers);

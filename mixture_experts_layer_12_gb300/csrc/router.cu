@@ -390,46 +390,46 @@ __global__ void __launch_bounds__(RTHREADS)
           taken |= 0xfu << (cc * 4);
         }
       }
-      float sel_v[kMaxTopK];
-      int sel_id[kMaxTopK];
+      // k rounds (not unrolled: this code runs once per launch, cold in the
+      // instruction cache, so its size is its cost); lane g keeps choice g
+      int my_id = 0;
+      float my_v = -INFINITY;
+      float mx = 0.f;
+#pragma unroll 1
+      for (int j = 0; j < a.k; ++j) {
+        float bv = -INFINITY;
+        int bq = -1;
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) {
-        sel_v[j] = -INFINITY;
-        sel_id[j] = 0;
-        if (j < a.k) {
-          float bv = -INFINITY;
-          int bq = -1;
-#pragma unroll
-          for (int q = 0; q < NV; ++q)
-            if (!((taken >> q) & 1u) && (bq < 0 || lv[q] > bv)) {
-              bv = lv[q];
-              bq = q;
-            }
-          // local index q = 4*cc + i  <->  expert 4*(g + 8*cc) + i
-          int be = bq < 0 ? 0x7fffffff : ((g + (bq >> 2) * GS) << 2) + (bq & 3);
-#pragma unroll
-          for (int off = GS / 2; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(gmask, bv, off);
-            const int oe = __shfl_xor_sync(gmask, be, off);
-            if (ov > bv || (ov == bv && oe < be)) {
-              bv = ov;
-              be = oe;
-            }
+        for (int q = 0; q < NV; ++q)
+          if (!((taken >> q) & 1u) && (bq < 0 || lv[q] > bv)) {
+            bv = lv[q];
+            bq = q;
           }
-          if (be != 0x7fffffff && ((be >> 2) & (GS - 1)) == g)
-            taken |= 1u << (((be >> 5) << 2) | (be & 3));
-          sel_v[j] = bv;
-          sel_id[j] = be;
+        // local index q = 4*cc + i  <->  expert 4*(g + 8*cc) + i
+        int be = bq < 0 ? 0x7fffffff : ((g + (bq >> 2) * GS) << 2) + (bq & 3);
+#pragma unroll
+        for (int off = GS / 2; off > 0; off >>= 1) {
+          const float ov = __shfl_xor_sync(gmask, bv, off);
+          const int oe = __shfl_xor_sync(gmask, be, off);
+          if (ov > bv || (ov == bv && oe < be)) {
+            bv = ov;
+            be = oe;
+          }
+        }
+        if (be != 0x7fffffff && ((be >> 2) & (GS - 1)) == g)
+          taken |= 1u << (((be >> 5) << 2) | (be & 3));
+        if (j == 0) mx = bv;
+        if (j == g) {
+          my_id = be;
+          my_v = bv;
         }
       }
-      const float mx = sel_v[0];
-      float ex[kMaxTopK];
-      float z = 0.f;
+      // softmax over the k choices: lane g < k holds exp(l_g - l_0), the
+      // group sums by butterfly
+      float ex = g < a.k ? expf(my_v - mx) : 0.f;
+      float z = ex;
 #pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j) {
-        ex[j] = j < a.k ? expf(sel_v[j] - mx) : 0.f;
-        z += ex[j];
-      }
+      for (int off = GS / 2; off > 0; off >>= 1) z += __shfl_xor_sync(gmask, z, off);
       if (a.gating != MOE_GATE_TOPK_SOFTMAX) {
         // softmax over all E logits first: p_j = exp(l_j - max) / sum_e exp(l_e - max)
         float zall = 0.f;
@@ -440,23 +440,13 @@ __global__ void __launch_bounds__(RTHREADS)
             for (int i = 0; i < 4; ++i) zall += expf(lv[cc * 4 + i] - mx);
 #pragma unroll
         for (int off = GS / 2; off > 0; off >>= 1) zall += __shfl_xor_sync(gmask, zall, off);
-        float zsel = 0.f;
+        ex = ex / zall;
+        float zsel = ex;
 #pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-          ex[j] = ex[j] / zall;
-          zsel += ex[j];
-        }
+        for (int off = GS / 2; off > 0; off >>= 1) zsel += __shfl_xor_sync(gmask, zsel, off);
         z = a.gating == MOE_GATE_SOFTMAX_TOPK ? 1.f : zsel;
       }
-      // lane g writes the token's g-th choice (k <= 8 = GS)
-      int my_id = 0;
-      float my_w = 0.f;
-#pragma unroll
-      for (int j = 0; j < kMaxTopK; ++j)
-        if (j == g) {
-          my_id = sel_id[j];
-          my_w = ex[j] / z;
-        }
+      const float my_w = ex / z;
       if (g < a.k) {
         a.ids[(size_t)t * a.k + g] = my_id;
         a.weights[(size_t)t * a.k + g] = my_w;
