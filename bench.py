@@ -43,10 +43,10 @@ NCU_TRAFFIC = {
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch
     "prefill/expert_gemm1": {"bytes": 1030029e3 + 222244352, "src": "ffn_gemm.cu", "src_sha": "43fdc202f8c9fbc7"},
     "prefill/expert_gemm2": {"bytes": 1443140e3 + 65493504, "src": "ffn_gemm.cu", "src_sha": "43fdc202f8c9fbc7"},
-    "prefill/router": {"bytes": 33692160, "src": "router.cu", "src_sha": "74867526327d7f28"},
+    "prefill/router": {"bytes": 33676032, "src": "router.cu", "src_sha": "b23bef11f9baa1a1"},
     # router sweep, k = 1 (profiles/router_prefill.md): router_kernel + dispatch_kernel of one call
-    "router_k1/router+dispatch": {"bytes": 17897728 + 40448, "src": ["router.cu", "dispatch_combine.cu"],
-                                  "src_sha": ["74867526327d7f28", "456cbd9bca80ff77"]},
+    "router_k1/router+dispatch": {"bytes": 17889024 + 40448, "src": ["router.cu", "dispatch_combine.cu"],
+                                  "src_sha": ["b23bef11f9baa1a1", "67a1c639e9ea246b"]},
     # decode workload (profiles/decode_weight_stream.md): both GEMMs on the small-batch kernel
     "decode/expert_gemm1": {"bytes": 940161024 + 3989760, "src": "ffn_gemm_small.cu", "src_sha": "ff59fa4c79617713"},
     "decode/expert_gemm2": {"bytes": 941419776 + 5054208, "src": "ffn_gemm_small.cu", "src_sha": "ff59fa4c79617713"},
