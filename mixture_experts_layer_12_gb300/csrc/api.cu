@@ -367,6 +367,10 @@ int enqueue_expert_gemms(const moe_shape* s, int n_seg, const uint16_t* xp, cons
   if ((rc = map_2d(&tm_xp, xp, (uint64_t)s->H, rows, 64, small1 ? 32 : 128, "xp")) != MOE_OK) return rc;
   if ((rc = map_3d(&tm_w1, w1, w1_cols, (uint64_t)s->H, (uint64_t)s->E, 64, 64, "W1")) != MOE_OK) return rc;
   if ((rc = map_2d(&tm_h, h, (uint64_t)s->F, rows, 64, small2 ? 32 : 128, "h")) != MOE_OK) return rc;
+  // 64-row boxes for the main kernel's M = 128 tiles
+  CUtensorMap tm_xp64, tm_h64;
+  if ((rc = map_2d(&tm_xp64, xp, (uint64_t)s->H, rows, 64, 64, "xp")) != MOE_OK) return rc;
+  if ((rc = map_2d(&tm_h64, h, (uint64_t)s->F, rows, 64, 64, "h")) != MOE_OK) return rc;
   if ((rc = map_3d(&tm_w2, w2, (uint64_t)s->H, (uint64_t)s->F, (uint64_t)s->E, 64, 64, "W2")) != MOE_OK) return rc;
 
   // pair tiles of the main kernel are 2*kGemmBM rows: a segment with n rows
@@ -394,7 +398,7 @@ int enqueue_expert_gemms(const moe_shape* s, int n_seg, const uint16_t* xp, cons
   } else {
     const int out_cols = swiglu ? kGemmBN / 2 : kGemmBN;  // h columns per pair tile
     const int64_t ub = row_blocks_ub * ((s->F + out_cols - 1) / out_cols);
-    e = launch_grouped_gemm(swiglu ? kGemmSwiGLU : kGemmGelu, tm_xp, tm_w1, g,
+    e = launch_grouped_gemm(swiglu ? kGemmSwiGLU : kGemmGelu, tm_xp, tm_w1, tm_xp64, g,
                             (int)(ub < (1 << 30) ? ub : (1 << 30)), st, pdl_first);
   }
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM1 launch");
@@ -412,7 +416,7 @@ int enqueue_expert_gemms(const moe_shape* s, int n_seg, const uint16_t* xp, cons
     if (e == cudaSuccess && splits_used) *splits_used = S2;
   } else {
     const int64_t ub = row_blocks_ub * ((s->H + kGemmBN - 1) / kGemmBN);
-    e = launch_grouped_gemm(combine_k1 ? kGemmCombineK1 : kGemmPlain, tm_h, tm_w2, g,
+    e = launch_grouped_gemm(combine_k1 ? kGemmCombineK1 : kGemmPlain, tm_h, tm_w2, tm_h64, g,
                             (int)(ub < (1 << 30) ? ub : (1 << 30)), st, pdl);
   }
   if (e != cudaSuccess) return cuda_fail(e, "expert GEMM2 launch");

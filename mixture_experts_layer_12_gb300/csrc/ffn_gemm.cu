@@ -62,6 +62,13 @@ constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
 constexpr int TMEM_COLS = ACC * BN;  // 512
 constexpr uint16_t PAIR_MASK = 0x3;
 constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, BN, /*a_mn=*/false, /*b_mn=*/true);
+// An expert's last row block with at most 128 rows runs as an M = 128 pair
+// MMA (64 rows per CTA): half the tensor work of a padded 256-row tile.  Its
+// accumulator sits in TMEM columns 0..127 of the slot: lanes 0-63 hold the
+// CTA's 64 rows for output columns 0..127, lanes 64-127 the same rows for
+// columns 128..255 (read back per warp: rows 32 (q & 1) + lane, columns
+// 128 (q >> 1) + c for lane quadrant q).
+constexpr uint32_t IDESC_HALF = idesc_bf16_f32(PAIR_M / 2, BN, /*a_mn=*/false, /*b_mn=*/true);
 
 static_assert(BK == 64, "one 128-byte swizzle atom of K per stage");
 static_assert(BN_CTA % 64 == 0 && BN <= 256, "UMMA N");
@@ -88,21 +95,34 @@ constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(Ctrl)
 struct Tile {
   int e, nb;
   int row0;        // this CTA's first dispatch row
-  int rows_valid;  // rows of this CTA's half that belong to the expert (may be <= 0)
+  int rows_valid;  // rows of this CTA's part that belong to the expert (may be <= 0)
+  bool half;       // M = 128 tile: 64 rows per CTA
 };
 
 // Tiles of one pair increase monotonically, so the expert cursor only moves
 // forward; experts without rows own no tiles and are skipped.
-__device__ __forceinline__ Tile decode_tile(const Ctrl& c, int tile, int& e, int rank) {
+// Tiles of one pair increase monotonically, so the expert cursor only moves
+// forward; experts without rows own no tiles and are skipped.  Within an
+// expert the row blocks run fastest, so a weight tile's readers follow one
+// another while it is in L2.  allow_half: the expert's last row block runs
+// as an M = 128 tile when it holds at most 128 rows (not for SwiGLU, whose
+// gate and up columns of one output would land in different lane halves).
+// (Moving those tiles to the end of the list, to fill the last wave, was
+// slower: their weight tiles had left L2 by then.)
+__device__ __forceinline__ Tile decode_tile(const Ctrl& c, int tile, int& e, int rank,
+                                            bool allow_half) {
   while (tile >= c.tile_start[e + 1]) ++e;
   const int local = tile - c.tile_start[e];
   const int mbs = c.mblocks[e];
   const int mb = local % mbs;
+  const int base = mb * PAIR_M;  // the block's first row within the expert
   Tile t;
   t.e = e;
   t.nb = local / mbs;
-  t.row0 = c.row_off[e] + mb * PAIR_M + rank * BM;
-  t.rows_valid = min(BM, c.rows[e] - mb * PAIR_M - rank * BM);
+  t.half = allow_half && mb == mbs - 1 && c.rows[e] - base <= PAIR_M / 2;
+  const int per = t.half ? BM / 2 : BM;  // rows per CTA
+  t.row0 = c.row_off[e] + base + rank * per;
+  t.rows_valid = min(per, c.rows[e] - base - rank * per);
   return t;
 }
 
@@ -149,7 +169,8 @@ __device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __e
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
-                        const __grid_constant__ CUtensorMap tm_b, const GemmArgs p) {
+                        const __grid_constant__ CUtensorMap tm_b,
+                        const __grid_constant__ CUtensorMap tm_a64, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -158,6 +179,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   Ctrl& c = *reinterpret_cast<Ctrl*>(smem + STAGES * STAGE_BYTES);
   constexpr bool SWIGLU = MODE == kGemmSwiGLU;
   constexpr bool COMBINE = MODE == kGemmCombineK1;  // k = 1: scale by the gate, write y[t]
+  constexpr bool HALF = !SWIGLU;  // M = 128 tiles for short last row blocks
   // output columns per pair tile: SwiGLU pairs 128 gate with 128 up columns
   constexpr int BN_OUT = SWIGLU ? BN / 2 : BN;
 
@@ -241,6 +263,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------ producer (one thread)
     if (lane == 0) {
       tma_prefetch_desc(&tm_a);
+      if (HALF) tma_prefetch_desc(&tm_a64);
       tma_prefetch_desc(&tm_b);
       const uint32_t full0 = dsmem_map(smem_u32(&c.full[0]), 0);  // leader's barriers
       // An expert with a single row block reads each weight tile once: those
@@ -256,7 +279,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int e = 0;
       bool ok = true;
       for (int tile = pair; tile < n_tiles && ok; tile += n_pairs) {
-        const Tile t = decode_tile(c, tile, e, rank);
+        const Tile t = decode_tile(c, tile, e, rank, HALF);
         // B columns of this CTA: its half of the 256-wide tile, or for
         // SwiGLU the gate (rank 0) / up (rank 1) columns of the same 128
         // outputs (W1 = [W_gate | W_up], so up starts at column N)
@@ -269,17 +292,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           const uint32_t full_cl = full0 + (uint32_t)(stage * sizeof(uint64_t));
-          mbar_arrive_expect_tx_cluster(full_cl, STAGE_BYTES);
+          // an M = 128 tile reads 64 A rows per CTA (the first 8 KB of the
+          // stage, laid out as the first 64 rows of a 128-row box)
+          const CUtensorMap* ma = t.half ? &tm_a64 : &tm_a;
+          mbar_arrive_expect_tx_cluster(full_cl, t.half ? STAGE_BYTES - A_BYTES / 2 : STAGE_BYTES);
           // rows past the expert's end belong to the next expert (or lie past
           // the last row: zero-filled); they are computed but never stored
           if (once) {
-            tma_load_2d_pair_hint(sA + stage * A_BYTES, &tm_a, full_cl, kb * BK, t.row0, pol_last);
+            tma_load_2d_pair_hint(sA + stage * A_BYTES, ma, full_cl, kb * BK, t.row0, pol_last);
 #pragma unroll
             for (int cb = 0; cb < BN_CTA / 64; ++cb)
               tma_load_3d_pair_hint(sB + stage * B_BYTES + cb * B_CHUNK, &tm_b, full_cl,
                                     bcol + cb * 64, kb * BK, we, pol_first);
           } else {
-            tma_load_2d_pair(sA + stage * A_BYTES, &tm_a, full_cl, kb * BK, t.row0);
+            tma_load_2d_pair(sA + stage * A_BYTES, ma, full_cl, kb * BK, t.row0);
 #pragma unroll
             for (int cb = 0; cb < BN_CTA / 64; ++cb)
               tma_load_3d_pair(sB + stage * B_BYTES + cb * B_CHUNK, &tm_b, full_cl, bcol + cb * 64,
@@ -310,7 +336,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
+      int e = 0;
       for (int tile = pair; tile < n_tiles && ok; tile += n_pairs) {
+        const uint32_t idesc = decode_tile(c, tile, e, rank, HALF).half ? IDESC_HALF : IDESC;
         if (!mbar_wait(&c.tempty[acc], acc_phase ^ 1u, wc)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * BN);
@@ -328,7 +356,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // B: MN-major, advance 16 K rows = two 1024-byte atoms.
             const uint64_t ad = sdesc_sw128(a0 + j * 32, 16, 1024);
             const uint64_t bd = sdesc_sw128(b0 + j * 2048, B_CHUNK, 1024);
-            umma_bf16_pair(d, ad, bd, IDESC, (kb | j) != 0 ? 1u : 0u);
+            umma_bf16_pair(d, ad, bd, idesc, (kb | j) != 0 ? 1u : 0u);
           }
           umma_commit_pair_mc(&c.empty[stage], PAIR_MASK);
           if (++stage == STAGES) {
@@ -356,13 +384,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t acc_phase = 0;
     int e = 0;
     for (int tile = pair; tile < n_tiles; tile += n_pairs) {
-      const Tile t = decode_tile(c, tile, e, rank);
+      const Tile t = decode_tile(c, tile, e, rank, HALF);
       int got = 1;
       if (lane == 0) got = mbar_wait(&c.tfull[acc], acc_phase, wc);
       got = __shfl_sync(0xffffffffu, got, 0);
       if (!got) break;
       tc_fence_after();
-      const int row = q * 32 + lane;
+      // M = 128 tile: this warp's lanes hold rows 32 (q & 1) + lane for the
+      // output columns 128 (q >> 1) .. +127 (TMEM columns 0..127)
+      const int row = t.half ? (q & 1) * 32 + lane : q * 32 + lane;
+      const int col_base = t.half ? (q >> 1) * 128 : 0;
+      const int n_chunks = t.half ? 4 : 8;  // 32-column chunks
       bool row_ok = row < t.rows_valid;
       uint16_t* orow = p.out + (size_t)(row_ok ? t.row0 + row : 0) * (size_t)p.N;
       float gw = 1.0f;
@@ -407,12 +439,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else {
 #pragma unroll 1
-      for (int ch = 0; ch < 8; ++ch) {
+      for (int ch = 0; ch < n_chunks; ++ch) {
         const int col = ch * 32;
         uint32_t v[32];
         tmem_ld_x32(tbase + (uint32_t)col, v);
         tmem_ld_wait();
-        const int gcol = t.nb * BN + col;
+        const int gcol = t.nb * BN + col_base + col;
         if (row_ok) {
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
@@ -458,7 +490,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 template <int MODE>
-cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const GemmArgs& a,
+cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_a64,
+                        const GemmArgs& a,
                         int pairs, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
@@ -473,7 +506,7 @@ cudaError_t launch_pair(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const 
   if (pdl) set_pdl_attr(attr[1]);
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, tm_a, tm_b, a);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, tm_a, tm_b, tm_a64, a);
 }
 
 // Co-resident CTA pairs of the GEMM kernel on this device (one per TPC).
@@ -509,6 +542,7 @@ cudaError_t query_max_pairs(int dev, int* out) {
 size_t grouped_gemm_smem_bytes() { return SMEM_BYTES; }
 
 cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
+                                const CUtensorMap& tm_a64,
                                 const GemmArgs& a, int max_tiles, cudaStream_t st, bool pdl) {
   if (max_tiles <= 0) return cudaSuccess;
   int dev = 0, pairs = 0;
@@ -517,10 +551,10 @@ cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tm_a, const CUtenso
   if ((e = query_max_pairs(dev, &pairs)) != cudaSuccess) return e;
   if (pairs > max_tiles) pairs = max_tiles;
   switch (mode) {
-    case kGemmGelu: return launch_pair<kGemmGelu>(tm_a, tm_b, a, pairs, st, pdl);
-    case kGemmSwiGLU: return launch_pair<kGemmSwiGLU>(tm_a, tm_b, a, pairs, st, pdl);
-    case kGemmCombineK1: return launch_pair<kGemmCombineK1>(tm_a, tm_b, a, pairs, st, pdl);
-    default: return launch_pair<kGemmPlain>(tm_a, tm_b, a, pairs, st, pdl);
+    case kGemmGelu: return launch_pair<kGemmGelu>(tm_a, tm_b, tm_a64, a, pairs, st, pdl);
+    case kGemmSwiGLU: return launch_pair<kGemmSwiGLU>(tm_a, tm_b, tm_a64, a, pairs, st, pdl);
+    case kGemmCombineK1: return launch_pair<kGemmCombineK1>(tm_a, tm_b, tm_a64, a, pairs, st, pdl);
+    default: return launch_pair<kGemmPlain>(tm_a, tm_b, tm_a64, a, pairs, st, pdl);
   }
 }
 

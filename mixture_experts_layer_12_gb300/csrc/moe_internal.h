@@ -150,8 +150,11 @@ constexpr int kMaxKSplits = 4;
 // access, which waits for the whole predecessor grid (this library's or the
 // caller's) to complete and its writes to become visible; the early launch
 // overlaps only launch latency and shared-memory setup.
+// tm_a: A [rows, K] bf16, box {64, 128}; tm_a64: the same tensor, box {64, 64}
+// (the M = 128 tiles of short last row blocks).
 cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tm_a, const CUtensorMap& tm_b,
-                                const GemmArgs& a, int max_tiles, cudaStream_t st, bool pdl);
+                                const CUtensorMap& tm_a64, const GemmArgs& a, int max_tiles,
+                                cudaStream_t st, bool pdl);
 size_t grouped_gemm_smem_bytes();
 constexpr int kGemmBM = 128;  // rows per CTA; a CTA pair covers 256
 constexpr int kGemmBN = 256;

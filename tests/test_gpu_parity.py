@@ -611,6 +611,31 @@ def test_gelu_epilogue_small_batch_kernel():
     _gelu_reference_check(x, Y)
 
 
+def test_expert_ffn_row_block_boundaries():
+    # segments of 0, 1, 64, 127, 128, 129, 255, 256, 257, 384 and 385 rows
+    # (segment i on expert i % 4): every kind of last row block -- none, at
+    # most 128 rows (an M = 128 tile, 64 rows per CTA), a full 256-row tile
+    # -- checked row by row against the oracle
+    sizes = [0, 1, 64, 127, 128, 129, 255, 256, 257, 384, 385]
+    rows = sum(sizes)
+    cfg = moe_synth.MoEConfig("tailblocks", T=rows, H=256, F=384, E=4, k=1, seed=37)
+    inp = moe_synth.make_inputs(cfg)
+    s = moe.make_shape(rows, cfg.H, cfg.F, cfg.E, 1)
+    ws = moe.alloc_workspace(s, DEV)
+    seg = torch.tensor(np.concatenate([[0], np.cumsum(sizes)]), dtype=torch.int32, device=DEV)
+    Y = torch.empty(rows, cfg.H, dtype=torch.bfloat16, device=DEV)
+    moe.moe_expert_ffn(s, len(sizes), inp["x"].to(DEV), inp["w1"].to(DEV), inp["w2"].to(DEV), seg,
+                       Y, ws)
+    assert moe.moe_get_device_status(ws) == 0
+    ref = np.empty((rows, cfg.H))
+    r = 0
+    for i, n in enumerate(sizes):
+        for _ in range(n):
+            ref[r] = oracle.expert_ffn(inp["x"][r], inp["w1"][i % cfg.E], inp["w2"][i % cfg.E])
+            r += 1
+    check_y(Y.float().cpu().numpy(), ref)
+
+
 # ----------------------------------------------- small batches (T*k <= 64 rows) --
 
 # The small-batch kernel runs a GEMM when it has at least two waves of column
