@@ -39,10 +39,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # one ncu capture, keyed by workload/kernel and by the sha256 of the kernel
 # source it was taken on; reported as null once the source changes.
 NCU_TRAFFIC = {
-    # prefill workload, `ncu --set full` (profiles/expert_gemm_prefill.md, profiles/router_prefill.md):
+    # prefill workload (profiles/expert_gemm_prefill.md, profiles/router_prefill.md):
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch
-    "prefill/expert_gemm1": {"bytes": 1030029e3 + 222244352, "src": "ffn_gemm.cu", "src_sha": "43fdc202f8c9fbc7"},
-    "prefill/expert_gemm2": {"bytes": 1443140e3 + 65493504, "src": "ffn_gemm.cu", "src_sha": "43fdc202f8c9fbc7"},
+    "prefill/expert_gemm1": {"bytes": 1034973184 + 221586432, "src": "ffn_gemm.cu", "src_sha": "c0d35effae941a05"},
+    "prefill/expert_gemm2": {"bytes": 1471127296 + 65170944, "src": "ffn_gemm.cu", "src_sha": "c0d35effae941a05"},
     "prefill/router": {"bytes": 33676032, "src": "router.cu", "src_sha": "b23bef11f9baa1a1"},
     # router sweep, k = 1 (profiles/router_prefill.md): router_kernel + dispatch_kernel of one call
     "router_k1/router+dispatch": {"bytes": 17889024 + 40448, "src": ["router.cu", "dispatch_combine.cu"],
