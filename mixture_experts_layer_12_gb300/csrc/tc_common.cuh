@@ -48,8 +48,8 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-// Launch attribute for a kernel whose predecessor on the stream is one of
-// this library's kernels of the same call (never the caller's work).
+// Launch attribute for programmatic stream serialization (every kernel of
+// this library waits on its predecessor grid before touching global memory).
 inline void set_pdl_attr(cudaLaunchAttribute& at) {
   at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at.val.programmaticStreamSerializationAllowed = 1;
