@@ -69,6 +69,11 @@ constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_M, BN, /*a_mn=*/false, /*b_mn=*/t
 // columns 128..255 (read back per warp: rows 32 (q & 1) + lane, columns
 // 128 (q >> 1) + c for lane quadrant q).
 constexpr uint32_t IDESC_HALF = idesc_bf16_f32(PAIR_M / 2, BN, /*a_mn=*/false, /*b_mn=*/true);
+// A 256-row tile whose column block holds at most 128 valid columns (the
+// last one when N % 256 is 1..128) runs as an N = 128 MMA: each CTA loads
+// one 64-column B box, and lanes = rows, TMEM columns 0..127 = the block's
+// columns, as for N = 256.
+constexpr uint32_t IDESC_NHALF = idesc_bf16_f32(PAIR_M, BN / 2, /*a_mn=*/false, /*b_mn=*/true);
 
 static_assert(BK == 64, "one 128-byte swizzle atom of K per stage");
 static_assert(BN_CTA % 64 == 0 && BN <= 256, "UMMA N");
@@ -97,6 +102,7 @@ struct Tile {
   int row0;        // this CTA's first dispatch row
   int rows_valid;  // rows of this CTA's part that belong to the expert (may be <= 0)
   bool half;       // M = 128 tile: 64 rows per CTA
+  bool nhalf;      // N = 128 tile (256 rows): 64 B columns per CTA
 };
 
 // Tiles of one pair increase monotonically, so the expert cursor only moves
@@ -109,8 +115,10 @@ struct Tile {
 // gate and up columns of one output would land in different lane halves).
 // (Moving those tiles to the end of the list, to fill the last wave, was
 // slower: their weight tiles had left L2 by then.)
+// n_cols: output columns (N); the last column block runs as an N = 128
+// tile when it holds at most 128 of them (allow_half, 256-row tiles only).
 __device__ __forceinline__ Tile decode_tile(const Ctrl& c, int tile, int& e, int rank,
-                                            bool allow_half) {
+                                            bool allow_half, int n_cols) {
   while (tile >= c.tile_start[e + 1]) ++e;
   const int local = tile - c.tile_start[e];
   const int mbs = c.mblocks[e];
@@ -120,6 +128,7 @@ __device__ __forceinline__ Tile decode_tile(const Ctrl& c, int tile, int& e, int
   t.e = e;
   t.nb = local / mbs;
   t.half = allow_half && mb == mbs - 1 && c.rows[e] - base <= PAIR_M / 2;
+  t.nhalf = allow_half && !t.half && n_cols - t.nb * BN <= BN / 2;
   const int per = t.half ? BM / 2 : BM;  // rows per CTA
   t.row0 = c.row_off[e] + base + rank * per;
   t.rows_valid = min(per, c.rows[e] - base - rank * per);
@@ -279,11 +288,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       int e = 0;
       bool ok = true;
       for (int tile = pair; tile < n_tiles && ok; tile += n_pairs) {
-        const Tile t = decode_tile(c, tile, e, rank, HALF);
+        const Tile t = decode_tile(c, tile, e, rank, HALF, p.N);
         // B columns of this CTA: its half of the 256-wide tile, or for
         // SwiGLU the gate (rank 0) / up (rank 1) columns of the same 128
         // outputs (W1 = [W_gate | W_up], so up starts at column N)
-        const int bcol = SWIGLU ? rank * p.N + t.nb * BN_OUT : t.nb * BN + rank * BN_CTA;
+        const int bcol = SWIGLU  ? rank * p.N + t.nb * BN_OUT
+                         : t.nhalf ? t.nb * BN + rank * (BN_CTA / 2)
+                                   : t.nb * BN + rank * BN_CTA;
+        const int n_boxes = t.nhalf ? 1 : BN_CTA / 64;  // 64-column B boxes per CTA
         const int we = t.e % p.E_w;  // the segment's expert weights
         const bool once = c.mblocks[t.e] == 1;
         for (int kb = 0; kb < KB; ++kb) {
@@ -295,19 +307,19 @@ __global__ void __launch_bounds__(THREADS, 1)
           // an M = 128 tile reads 64 A rows per CTA (the first 8 KB of the
           // stage, laid out as the first 64 rows of a 128-row box)
           const CUtensorMap* ma = t.half ? &tm_a64 : &tm_a;
-          mbar_arrive_expect_tx_cluster(full_cl, t.half ? STAGE_BYTES - A_BYTES / 2 : STAGE_BYTES);
+          mbar_arrive_expect_tx_cluster(full_cl, (t.half ? A_BYTES / 2 : A_BYTES) + n_boxes * B_CHUNK);
           // rows past the expert's end belong to the next expert (or lie past
           // the last row: zero-filled); they are computed but never stored
           if (once) {
             tma_load_2d_pair_hint(sA + stage * A_BYTES, ma, full_cl, kb * BK, t.row0, pol_last);
 #pragma unroll
-            for (int cb = 0; cb < BN_CTA / 64; ++cb)
+            for (int cb = 0; cb < n_boxes; ++cb)
               tma_load_3d_pair_hint(sB + stage * B_BYTES + cb * B_CHUNK, &tm_b, full_cl,
                                     bcol + cb * 64, kb * BK, we, pol_first);
           } else {
             tma_load_2d_pair(sA + stage * A_BYTES, ma, full_cl, kb * BK, t.row0);
 #pragma unroll
-            for (int cb = 0; cb < BN_CTA / 64; ++cb)
+            for (int cb = 0; cb < n_boxes; ++cb)
               tma_load_3d_pair(sB + stage * B_BYTES + cb * B_CHUNK, &tm_b, full_cl, bcol + cb * 64,
                                kb * BK, we);
           }
@@ -338,7 +350,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       int e = 0;
       for (int tile = pair; tile < n_tiles && ok; tile += n_pairs) {
-        const uint32_t idesc = decode_tile(c, tile, e, rank, HALF).half ? IDESC_HALF : IDESC;
+        const Tile tt = decode_tile(c, tile, e, rank, HALF, p.N);
+        const uint32_t idesc = tt.half ? IDESC_HALF : tt.nhalf ? IDESC_NHALF : IDESC;
         if (!mbar_wait(&c.tempty[acc], acc_phase ^ 1u, wc)) break;
         tc_fence_after();
         const uint32_t d = tmem + (uint32_t)(acc * BN);
@@ -384,7 +397,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t acc_phase = 0;
     int e = 0;
     for (int tile = pair; tile < n_tiles; tile += n_pairs) {
-      const Tile t = decode_tile(c, tile, e, rank, HALF);
+      const Tile t = decode_tile(c, tile, e, rank, HALF, p.N);
       int got = 1;
       if (lane == 0) got = mbar_wait(&c.tfull[acc], acc_phase, wc);
       got = __shfl_sync(0xffffffffu, got, 0);
@@ -394,7 +407,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // output columns 128 (q >> 1) .. +127 (TMEM columns 0..127)
       const int row = t.half ? (q & 1) * 32 + lane : q * 32 + lane;
       const int col_base = t.half ? (q >> 1) * 128 : 0;
-      const int n_chunks = t.half ? 4 : 8;  // 32-column chunks
+      const int n_chunks = t.half || t.nhalf ? 4 : 8;  // 32-column chunks
       bool row_ok = row < t.rows_valid;
       uint16_t* orow = p.out + (size_t)(row_ok ? t.row0 + row : 0) * (size_t)p.N;
       float gw = 1.0f;
