@@ -41,8 +41,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # prefill workload (profiles/expert_gemm_prefill.md, profiles/router_prefill.md):
     # dram__bytes_read.sum + dram__bytes_write.sum of one launch
-    "prefill/expert_gemm1": {"bytes": 1027551744 + 221377280, "src": "ffn_gemm.cu", "src_sha": "e5c6f56b163f7f22"},
-    "prefill/expert_gemm2": {"bytes": 1417872640 + 65498880, "src": "ffn_gemm.cu", "src_sha": "e5c6f56b163f7f22"},
+    "prefill/expert_gemm1": {"bytes": 1027551744 + 221377280, "src": "ffn_gemm.cu", "src_sha": "9c589b4d85665278"},
+    "prefill/expert_gemm2": {"bytes": 1417872640 + 65498880, "src": "ffn_gemm.cu", "src_sha": "9c589b4d85665278"},
     "prefill/router": {"bytes": 33676032, "src": "router.cu", "src_sha": "b23bef11f9baa1a1"},
     # router sweep, k = 1 (profiles/router_prefill.md): router_kernel + dispatch_kernel of one call
     "router_k1/router+dispatch": {"bytes": 17889024 + 40448, "src": ["router.cu", "dispatch_combine.cu"],

@@ -21,7 +21,10 @@
 //     so pairs working at the same time share the expert's weight columns
 //     through L2 (the pages' expert-block / token-block tiling, made ragged:
 //     an expert owns ceil(n_e / 256) row blocks); the tile list is built on
-//     the device from `offsets`, with no host synchronisation.
+//     the device from `offsets`, with no host synchronisation.  An expert's
+//     last row block with at most 128 rows runs as an M = 128 MMA (64 rows
+//     per CTA), a column block with at most 128 valid columns as N = 128,
+//     so short blocks do not pay for padding.
 //   * warp 0: producer.  One thread per CTA issues the TMA loads of the
 //     stage: the A tile (128 rows of xp or h, one box) and the weight tile
 //     (two 64-column boxes of W[e], N contiguous = MN-major operand); both
