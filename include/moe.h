@@ -137,10 +137,11 @@ MOE_API int64_t moe_expert_capacity(const moe_shape* s);
 
 /* Workspace bytes needed by moe_forward and moe_expert_ffn_combine (and
  * enough for every other entry point): a 1 KB status block, per-128-token
- * expert counts [ceil(T/128), E] int32, h [T*k, F] bf16 and a [T*k, H]
- * bf16 region that holds first the token rows in dispatch order, then the
- * expert outputs.  Returns 0 for an invalid shape (E may be any 1..256
- * here, as moe_expert_ffn allows). */
+ * expert counts [ceil(T/128), E] int32, h [T*k, F] bf16, a [T*k, H] bf16
+ * region that holds first the token rows in dispatch order, then the
+ * expert outputs, and for T*k <= 64 rows fp32 partial expert outputs of up
+ * to 4 K splits [4, T*k, H] (the small-batch second GEMM).  Returns 0 for
+ * an invalid shape (E may be any 1..256 here, as moe_expert_ffn allows). */
 MOE_API size_t moe_workspace_size(const moe_shape* s);
 
 /* Workspace bytes needed by moe_route and moe_dispatch (status block and
