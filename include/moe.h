@@ -265,8 +265,12 @@ MOE_API int moe_combine(const moe_shape* s, const uint16_t* Y, const float* weig
 /*
  * The whole layer (the op "MoEFusion::Compute(x, w_router, expert_weights,
  * y)" of section "3. 完整调用流程"): moe_route followed by
- * moe_expert_ffn_combine, six kernels (five when k = 1) on `stream` and no host
- * synchronisation.  The routing outputs are written as in moe_route.
+ * moe_expert_ffn_combine on `stream` with no host synchronisation: a
+ * one-warp kernel that clears the status block, then router, dispatch,
+ * permute, expert GEMM1, expert GEMM2 and combine -- seven kernels, one
+ * fewer when the router also dispatches (moe_forward_plan: small batches)
+ * and one fewer when GEMM2 also combines (k = 1).  The routing outputs are
+ * written as in moe_route.
  */
 MOE_API int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
                 const float* b_router, const uint16_t* w1, const uint16_t* w2, uint16_t* y,
@@ -310,10 +314,11 @@ MOE_API int moe_expert_ffn_combine_noalloc(const moe_shape* s, const uint16_t* x
 /*
  * moe_forward with timing hooks (no counterpart on the pages): `events`
  * points to 7 cudaEvent_t handles (any may be NULL; `events` itself may be
- * NULL), recorded on `stream` before the router kernel and after each of
- * the six kernels: router, dispatch, permute (token rows into dispatch
- * order), expert GEMM1, expert GEMM2, combine.  With k = 1 there is no
- * combine kernel and the last two events are recorded back to back.
+ * NULL), recorded on `stream` before the router kernel (after the status
+ * clear) and after each of the six steps: router, dispatch, permute (token
+ * rows into dispatch order), expert GEMM1, expert GEMM2, combine.  A step
+ * that runs inside another kernel (dispatch in the small-batch router,
+ * combine in GEMM2 when k = 1) has its two events recorded back to back.
  * The events are caller-owned; the library only records them.
  */
 MOE_API int moe_forward_profiled(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
