@@ -191,11 +191,10 @@ def test_router_edge_shapes(T, H, E, k, bias):
 @pytest.mark.parametrize("T,E,k", [(2048, 128, 2), (2688, 64, 3), (3840, 128, 1), (6400, 16, 2),
                                    (2688, 192, 2)])
 def test_router_tile_counts(T, E, k):
-    # 16, 21, 30 and 50 tiles of 128 tokens: the router takes the most K
-    # splits (1..8) whose clusters all fit in one wave -- not always a power
-    # of two, so the ranks' owned row blocks (r*128/S ..) differ in size.
-    # E <= 128 exchanges partial rows by bulk copies, E = 192 by per-thread
-    # DSMEM stores.
+    # 16, 21, 30 and 50 tiles of 128 tokens: the K split per tile (the most,
+    # up to 8, whose clusters all fit in one wave) changes across these
+    # counts, and with it the rows each rank reduces; E = 192 takes the
+    # widest accumulator (three 64-expert column blocks)
     cfg = moe_synth.MoEConfig("tiles", T=T, H=1024, F=0, E=E, k=k, seed=31)
     inputs = moe_synth.make_inputs(cfg, with_ffn=False)
     r = gpu_route(cfg, to_dev(inputs))
