@@ -15,7 +15,8 @@
 //   * a tile of 128 tokens x E experts (E <= 256) is one tcgen05.mma
 //     accumulator (M = 128, N = E rounded up to 16) in TMEM, fed by a TMA
 //     ring of up to 8 stages;
-//   * the K = H reduction is split across a cluster of S CTAs (S = 1..8) so
+//   * the K = H reduction is split across a cluster of S CTAs (S = 1, 2, 4
+//     or 8: the most whose clusters all fit in one wave) so
 //     that ceil(T/128) x S CTAs stream x from HBM in parallel.  Each CTA
 //     pushes the fp32 partial rows owned by rank r (rows [r*128/S, ...))
 //     into rank r's shared memory with DSMEM stores; after one cluster
