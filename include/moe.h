@@ -96,8 +96,9 @@ extern "C" {
  *   (the router kernel of "用Ascend C写一个MoE融合算子", section "1. Routing +
  *   Gating 合并": Softmax over the top-k scores only).
  * MOE_GATE_SOFTMAX_TOPK (1): softmax over all E logits, then the k selected
- *   probabilities as they are (the Softmax -> Top-k order of the article's
- *   section 2.1); a token's weights sum to less than 1 unless k = E.
+ *   probabilities as they are (the Softmax -> Top-k order of section 2.1 of
+ *   the article "CANN ops-transformer MoE"); a token's weights sum to less
+ *   than 1 unless k = E.
  * MOE_GATE_SOFTMAX_TOPK_RENORM (2): as 1, then the k probabilities divided
  *   by their sum (mathematically equal to 0; computed in this order).
  * The selected experts are the same in all three modes. */
@@ -294,22 +295,32 @@ MOE_API int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w
  * hidden activations and expert outputs live in a static device array of
  * MOE_NOALLOC_SCRATCH_BYTES bytes inside the library.
  *   - Shapes whose workspace (moe_workspace_size) exceeds
- *     MOE_NOALLOC_SCRATCH_BYTES are rejected with MOE_ERR_UNSUPPORTED
- *     (about T*k*(F+H)*2 bytes: e.g. T*k = 64 rows at H = 4096, F = 14336).
+ *     MOE_NOALLOC_SCRATCH_BYTES are rejected with MOE_ERR_UNSUPPORTED.  The
+ *     workspace is about T*k*(F+H)*2 bytes, plus T*k*H*16 bytes of fp32
+ *     split-K partials when T*k <= 64 rows: at H = 4096, F = 14336 the limit
+ *     is about 900 rows of T*k (a 32-token, k = 2 decode step needs 6.4 MB).
  *   - Nothing is allocated or freed.  The first call on a device looks up
  *     the scratch's device address (cudaGetSymbolAddress) with that device
  *     current; make that first call before any stream capture.
  *   - Every call on a device shares the one scratch array: calls that
  *     overlap on the GPU (different streams, or different host threads)
  *     race and corrupt each other's results; serialise them.
- *   - Device status bits of this call are kept in the scratch and are not
- *     readable through moe_get_device_status.
+ *   - Device status bits of these calls are kept in the scratch; read (and
+ *     clear) them with moe_noalloc_device_status, not moe_get_device_status.
  */
 MOE_API int moe_expert_ffn_combine_noalloc(const moe_shape* s, const uint16_t* x,
                                            const uint16_t* w1, const uint16_t* w2,
                                            const float* weights, const int32_t* offsets,
                                            const int32_t* perm, const int32_t* slot, uint16_t* y,
                                            void* stream);
+
+/*
+ * The device status word of moe_expert_ffn_combine_noalloc's built-in
+ * scratch on the current device (no counterpart on the pages): synchronises
+ * `stream`, reads the word into *status and clears it, with the return codes
+ * of moe_get_device_status.  Allocates nothing.
+ */
+MOE_API int moe_noalloc_device_status(void* stream, int32_t* status);
 
 /*
  * moe_forward with timing hooks (no counterpart on the pages): `events`

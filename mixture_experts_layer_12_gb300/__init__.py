@@ -39,7 +39,7 @@ EXPORTS = ("moe_version", "moe_last_error_string", "moe_expert_capacity", "moe_w
            "moe_route", "moe_dispatch", "moe_expert_ffn_combine", "moe_forward",
            "moe_get_device_status", "moe_selftest_wait_timeout", "moe_forward_profiled",
            "moe_expert_ffn_combine_noalloc", "moe_route_workspace_size", "moe_dispatch_rows",
-           "moe_expert_ffn", "moe_combine", "moe_forward_plan")
+           "moe_expert_ffn", "moe_combine", "moe_forward_plan", "moe_noalloc_device_status")
 MOE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -98,6 +98,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "moe_expert_ffn_combine": ([S, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "moe_forward": ([S, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "moe_get_device_status": ([P, P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+            "moe_noalloc_device_status": ([P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
             "moe_selftest_wait_timeout": ([P, ctypes.c_size_t, ctypes.c_uint64, P], ctypes.c_int),
             "moe_forward_profiled": ([S, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P],
                                      ctypes.c_int),
@@ -122,18 +123,49 @@ def _check(rc: int):
         raise MoEError(rc, msg)
 
 
-def _ptr(t, dtype=None, name="tensor"):
-    if t is None:
-        return None
-    if not isinstance(t, torch.Tensor):
-        raise TypeError(f"{name} must be a torch.Tensor")
+def _current_cuda_index() -> int:
+    return torch.cuda.current_device()
+
+
+def check_tensor(t, dtype=None, name="tensor", min_numel: int = 0, device_index=None) -> None:
+    """Host-side checks of one tensor argument, before anything is launched:
+    dtype, contiguity, at least `min_numel` elements (the library indexes
+    its buffers from the shape alone, so an undersized tensor would become
+    out-of-bounds device accesses), and -- when it holds elements -- that it
+    lives on CUDA device `device_index` (the current device, whose stream
+    and built-in scratch the call uses)."""
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    if t.device.type != "cuda" and t.numel() > 0:
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.numel() < min_numel:
+        raise ValueError(f"{name} holds {t.numel()} elements; the shape needs at least {min_numel}")
+    if t.numel() > 0:
+        if t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor, got device {t.device}")
+        if device_index is not None and t.device.index != device_index:
+            raise ValueError(f"{name} is on cuda:{t.device.index}, the current device is "
+                             f"cuda:{device_index}")
+
+
+def _ptr(t, dtype=None, name="tensor", min_numel: int = 0):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    dev = _current_cuda_index() if (t.numel() > 0 and t.device.type == "cuda") else None
+    check_tensor(t, dtype, name, min_numel, dev)
     return ctypes.c_void_p(t.data_ptr())
+
+
+def _req(shape, n_segments: int = 0) -> dict:
+    """Minimum element counts of every tensor argument for `shape`."""
+    T, H, F, E, k = shape.T, shape.H, shape.F, shape.E, shape.k
+    f1 = 2 * F if shape.expert_act == MOE_EXPERT_SWIGLU else F
+    tk = max(T, 0) * k
+    return dict(x=T * H, w_router=H * E, b_router=E, ids=tk, weights=tk, counts=E, offsets=E + 1,
+                perm=tk, slot=tk, w1=E * H * f1, w2=E * F * H, y=T * H, xp=tk * H, Y=tk * H,
+                seg_offsets=n_segments + 1)
 
 
 def _stream(stream):
@@ -176,57 +208,65 @@ def moe_route_workspace_size(shape: moe_shape) -> int:
     return n
 
 
+def _args(shape, *specs, n_segments: int = 0):
+    """ctypes pointers of (tensor, dtype, name) argument specs, each checked
+    against the element count the shape needs (see check_tensor)."""
+    need = _req(shape, n_segments)
+    return [_ptr(t, dt, name, need.get(name, 0)) for t, dt, name in specs]
+
+
+_BF, _I32, _F32 = torch.bfloat16, torch.int32, torch.float32
+
+
+def _ws(ws):
+    return _ptr(ws, None, "ws"), ws.numel() * ws.element_size()
+
+
 def moe_route(shape, x, w_router, b_router, ids, weights, counts, offsets, perm, slot, ws,
               stream=None):
-    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
-    _check(load_library().moe_route(
-        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(w_router, bf, "w_router"),
-        _ptr(b_router, f32, "b_router"), _ptr(ids, i32, "ids"), _ptr(weights, f32, "weights"),
-        _ptr(counts, i32, "counts"), _ptr(offsets, i32, "offsets"), _ptr(perm, i32, "perm"),
-        _ptr(slot, i32, "slot"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
-        _stream(stream)))
+    p = _args(shape, (x, _BF, "x"), (w_router, _BF, "w_router"), (b_router, _F32, "b_router"),
+              (ids, _I32, "ids"), (weights, _F32, "weights"), (counts, _I32, "counts"),
+              (offsets, _I32, "offsets"), (perm, _I32, "perm"), (slot, _I32, "slot"))
+    _check(load_library().moe_route(ctypes.byref(shape), *p, *_ws(ws), _stream(stream)))
 
 
 def moe_dispatch(shape, ids, counts, offsets, perm, slot, ws, stream=None):
-    i32 = torch.int32
-    _check(load_library().moe_dispatch(
-        ctypes.byref(shape), _ptr(ids, i32, "ids"), _ptr(counts, i32, "counts"),
-        _ptr(offsets, i32, "offsets"), _ptr(perm, i32, "perm"), _ptr(slot, i32, "slot"),
-        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+    p = _args(shape, (ids, _I32, "ids"), (counts, _I32, "counts"), (offsets, _I32, "offsets"),
+              (perm, _I32, "perm"), (slot, _I32, "slot"))
+    _check(load_library().moe_dispatch(ctypes.byref(shape), *p, *_ws(ws), _stream(stream)))
+
+
+def _ffn_combine_specs(x, w1, w2, weights, offsets, perm, slot, y):
+    return ((x, _BF, "x"), (w1, _BF, "w1"), (w2, _BF, "w2"), (weights, _F32, "weights"),
+            (offsets, _I32, "offsets"), (perm, _I32, "perm"), (slot, _I32, "slot"), (y, _BF, "y"))
 
 
 def moe_expert_ffn_combine(shape, x, w1, w2, weights, offsets, perm, slot, y, ws, stream=None):
-    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
-    _check(load_library().moe_expert_ffn_combine(
-        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(w1, bf, "w1"), _ptr(w2, bf, "w2"),
-        _ptr(weights, f32, "weights"), _ptr(offsets, i32, "offsets"), _ptr(perm, i32, "perm"),
-        _ptr(slot, i32, "slot"), _ptr(y, bf, "y"), _ptr(ws, None, "ws"),
-        ws.numel() * ws.element_size(), _stream(stream)))
+    p = _args(shape, *_ffn_combine_specs(x, w1, w2, weights, offsets, perm, slot, y))
+    _check(load_library().moe_expert_ffn_combine(ctypes.byref(shape), *p, *_ws(ws),
+                                                 _stream(stream)))
 
 
 def moe_dispatch_rows(shape, x, perm, offsets, xp, stream=None):
     """xp[r] = x[perm[r] // k] for the kept rows, in dispatch order."""
-    bf, i32 = torch.bfloat16, torch.int32
-    _check(load_library().moe_dispatch_rows(
-        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(perm, i32, "perm"),
-        _ptr(offsets, i32, "offsets"), _ptr(xp, bf, "xp"), _stream(stream)))
+    p = _args(shape, (x, _BF, "x"), (perm, _I32, "perm"), (offsets, _I32, "offsets"),
+              (xp, _BF, "xp"))
+    _check(load_library().moe_dispatch_rows(ctypes.byref(shape), *p, _stream(stream)))
 
 
 def moe_expert_ffn(shape, n_segments, xp, w1, w2, seg_offsets, Y, ws, stream=None):
     """Expert FFN on rows grouped in segments; segment i uses expert i % E."""
-    bf, i32 = torch.bfloat16, torch.int32
-    _check(load_library().moe_expert_ffn(
-        ctypes.byref(shape), int(n_segments), _ptr(xp, bf, "xp"), _ptr(w1, bf, "w1"),
-        _ptr(w2, bf, "w2"), _ptr(seg_offsets, i32, "seg_offsets"), _ptr(Y, bf, "Y"),
-        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+    p = _args(shape, (xp, _BF, "xp"), (w1, _BF, "w1"), (w2, _BF, "w2"),
+              (seg_offsets, _I32, "seg_offsets"), (Y, _BF, "Y"), n_segments=int(n_segments))
+    _check(load_library().moe_expert_ffn(ctypes.byref(shape), int(n_segments), *p, *_ws(ws),
+                                         _stream(stream)))
 
 
 def moe_combine(shape, Y, weights, slot, y, stream=None):
     """y[t] = sum_j weights[t, j] * Y[slot[t, j]] over the kept slots."""
-    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
-    _check(load_library().moe_combine(
-        ctypes.byref(shape), _ptr(Y, bf, "Y"), _ptr(weights, f32, "weights"),
-        _ptr(slot, i32, "slot"), _ptr(y, bf, "y"), _stream(stream)))
+    p = _args(shape, (Y, _BF, "Y"), (weights, _F32, "weights"), (slot, _I32, "slot"),
+              (y, _BF, "y"))
+    _check(load_library().moe_combine(ctypes.byref(shape), *p, _stream(stream)))
 
 
 def moe_expert_ffn_combine_noalloc(shape, x, w1, w2, weights, offsets, perm, slot, y, stream=None):
@@ -234,23 +274,23 @@ def moe_expert_ffn_combine_noalloc(shape, x, w1, w2, weights, offsets, perm, slo
     built-in device scratch (MOE_NOALLOC_SCRATCH_BYTES) holds the
     intermediates, for callers that cannot allocate device memory.  Calls
     that overlap on the GPU share that scratch and must be serialised."""
-    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
-    _check(load_library().moe_expert_ffn_combine_noalloc(
-        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(w1, bf, "w1"), _ptr(w2, bf, "w2"),
-        _ptr(weights, f32, "weights"), _ptr(offsets, i32, "offsets"), _ptr(perm, i32, "perm"),
-        _ptr(slot, i32, "slot"), _ptr(y, bf, "y"), _stream(stream)))
+    p = _args(shape, *_ffn_combine_specs(x, w1, w2, weights, offsets, perm, slot, y))
+    _check(load_library().moe_expert_ffn_combine_noalloc(ctypes.byref(shape), *p,
+                                                         _stream(stream)))
+
+
+def _forward_specs(x, w_router, b_router, w1, w2, y, ids, weights, counts, offsets, perm, slot):
+    return ((x, _BF, "x"), (w_router, _BF, "w_router"), (b_router, _F32, "b_router"),
+            (w1, _BF, "w1"), (w2, _BF, "w2"), (y, _BF, "y"), (ids, _I32, "ids"),
+            (weights, _F32, "weights"), (counts, _I32, "counts"), (offsets, _I32, "offsets"),
+            (perm, _I32, "perm"), (slot, _I32, "slot"))
 
 
 def moe_forward(shape, x, w_router, b_router, w1, w2, y, ids, weights, counts, offsets, perm,
                 slot, ws, stream=None):
-    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
-    _check(load_library().moe_forward(
-        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(w_router, bf, "w_router"),
-        _ptr(b_router, f32, "b_router"), _ptr(w1, bf, "w1"), _ptr(w2, bf, "w2"),
-        _ptr(y, bf, "y"), _ptr(ids, i32, "ids"), _ptr(weights, f32, "weights"),
-        _ptr(counts, i32, "counts"), _ptr(offsets, i32, "offsets"), _ptr(perm, i32, "perm"),
-        _ptr(slot, i32, "slot"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
-        _stream(stream)))
+    p = _args(shape, *_forward_specs(x, w_router, b_router, w1, w2, y, ids, weights, counts,
+                                     offsets, perm, slot))
+    _check(load_library().moe_forward(ctypes.byref(shape), *p, *_ws(ws), _stream(stream)))
 
 
 KERNEL_NAMES = ("router", "dispatch", "permute", "expert_gemm1", "expert_gemm2", "combine")
@@ -261,7 +301,6 @@ def moe_forward_profiled(shape, x, w_router, b_router, w1, w2, y, ids, weights, 
     """moe_forward recording ``events`` (len(KERNEL_NAMES) + 1 torch.cuda.Event
     or None) at the kernel boundaries: before the router, then after each of
     KERNEL_NAMES."""
-    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
     n = len(KERNEL_NAMES) + 1
     if len(events) != n:
         raise ValueError(f"moe_forward_profiled takes {n} events, got {len(events)}")
@@ -271,13 +310,10 @@ def moe_forward_profiled(shape, x, w_router, b_router, w1, w2, y, ids, weights, 
             if not ev.cuda_event:
                 ev.record()  # materialise the underlying cudaEvent_t
             handles[i] = ev.cuda_event
-    _check(load_library().moe_forward_profiled(
-        ctypes.byref(shape), _ptr(x, bf, "x"), _ptr(w_router, bf, "w_router"),
-        _ptr(b_router, f32, "b_router"), _ptr(w1, bf, "w1"), _ptr(w2, bf, "w2"),
-        _ptr(y, bf, "y"), _ptr(ids, i32, "ids"), _ptr(weights, f32, "weights"),
-        _ptr(counts, i32, "counts"), _ptr(offsets, i32, "offsets"), _ptr(perm, i32, "perm"),
-        _ptr(slot, i32, "slot"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
-        _stream(stream), handles))
+    p = _args(shape, *_forward_specs(x, w_router, b_router, w1, w2, y, ids, weights, counts,
+                                     offsets, perm, slot))
+    _check(load_library().moe_forward_profiled(ctypes.byref(shape), *p, *_ws(ws),
+                                               _stream(stream), handles))
 
 
 def moe_get_device_status(ws, stream=None) -> int:
@@ -286,6 +322,17 @@ def moe_get_device_status(ws, stream=None) -> int:
     v = ctypes.c_int32(0)
     rc = load_library().moe_get_device_status(_ptr(ws, None, "ws"), _stream(stream), ctypes.byref(v))
     if rc not in (MOE_OK,):
+        raise MoEError(rc, load_library().moe_last_error_string().decode(errors="replace"))
+    return v.value
+
+
+def moe_noalloc_device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the status word of
+    moe_expert_ffn_combine_noalloc's built-in scratch on the current device.
+    Raises MoEError if a status bit is set."""
+    v = ctypes.c_int32(0)
+    rc = load_library().moe_noalloc_device_status(_stream(stream), ctypes.byref(v))
+    if rc != MOE_OK:
         raise MoEError(rc, load_library().moe_last_error_string().decode(errors="replace"))
     return v.value
 

@@ -816,6 +816,14 @@ int moe_get_device_status(void* ws, void* stream, int32_t* status) {
   return fail(MOE_ERR_DEVICE, "device status 0x%x", v);
 }
 
+int moe_noalloc_device_status(void* stream, int32_t* status) {
+  if (!status) return fail(MOE_ERR_INVALID_ARG, "status is null");
+  void* scratch = nullptr;
+  int rc = noalloc_scratch(&scratch);
+  if (rc != MOE_OK) return rc;
+  return moe_get_device_status(scratch, stream, status);
+}
+
 int moe_selftest_wait_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns, void* stream) {
   if (!ws || !aligned16(ws) || ws_bytes < MOE_WS_MIN_BYTES)
     return fail(MOE_ERR_INVALID_ARG, "workspace null, misaligned or too small");

@@ -26,9 +26,10 @@
 //     (4-expert chunks) in registers; k rounds of a local scan plus a
 //     shuffle argmax over the 8 lanes.  Larger value first, equal values ->
 //     lower index.  Gate
-//     weights (fp32 expf): softmax over the k logits, or (the article's
-//     section 2.1 order) softmax over all E then the k probabilities, with
-//     or without renormalisation;
+//     weights (fp32 expf): softmax over the k logits, or (the Softmax ->
+//     Top-k order of section 2.1 of the article on CANN ops-transformer MoE
+//     operators) softmax over all E then the k probabilities, with or
+//     without renormalisation;
 //   * per-tile expert counts go to the workspace (summed through DSMEM
 //     atomics into rank 0).  For few tiles the dispatch kernel scans them;
 //     otherwise the last tile to finish (an atomic ticket, no waiting) scans

@@ -5,11 +5,15 @@ memory (for example a runtime that reserves all device memory up front and
 forbids cudaMalloc afterwards, or a plain C host that owns only its inputs
 and outputs): instead of a caller workspace it uses a static scratch array
 inside the library.  These tests call it through the C ABI and check that
-it gives the same y as the workspace entry point, on two calls in a row
-(the second call must not see the first one's leftovers), and that shapes
-beyond the scratch are refused with a clear error.  This file is collected
-last so that a failure here cannot hide another test's result.
+it gives bit for bit the same y as the workspace entry point (both run the
+same kernels, so any difference -- stale scratch from the previous call in
+a few rows, say -- is a fault), on calls in a row of different shapes, that
+its status word reads back clean, and that shapes beyond the scratch are
+refused with a clear error.  This file is collected last so that a failure
+here cannot hide another test's result.
 """
+import ctypes
+
 import pytest
 import torch
 
@@ -19,8 +23,6 @@ import mixture_experts_layer_12_gb300 as moe
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
-Y_MAX_REL = 1e-2  # same acceptance as the oracle parity tests
-Y_MEAN_REL = 5e-3
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -40,13 +42,6 @@ def _routed(cfg):
     return s, inputs, r, ws
 
 
-def _close(y, y_ref):
-    d = (y.float() - y_ref.float()).abs()
-    ref = y_ref.float().abs()
-    assert d.max().item() <= Y_MAX_REL * ref.max().item()
-    assert d.mean().item() <= Y_MEAN_REL * ref.mean().item()
-
-
 def test_noalloc_matches_workspace_entry_point_on_two_calls():
     # two different shapes in a row: a decode-sized batch, then a smaller one
     # with a capacity limit, so stale scratch from the first call would show
@@ -64,18 +59,17 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
         y = torch.full((cfg.T, cfg.H), float("nan"), dtype=torch.bfloat16, device=DEV)
         moe.moe_expert_ffn_combine_noalloc(s, inp["x"], inp["w1"], inp["w2"], r.weights, r.offsets,
                                            r.perm, r.slot, y)
-        torch.cuda.synchronize()
+        assert moe.moe_noalloc_device_status() == 0
         assert torch.isfinite(y.float()).all()
-        _close(y, y_ref)
+        assert torch.equal(y, y_ref), cfg.name
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch():
+    # through the C ABI directly: the shape is refused on the host before any
+    # pointer is looked at, so placeholder addresses are never dereferenced
     s = moe.make_shape(4096, 4096, 14336, 8, 2)  # ~300 MB of intermediates
     assert moe.moe_workspace_size(s) > moe.MOE_NOALLOC_SCRATCH_BYTES
-    bf = torch.empty(8, dtype=torch.bfloat16, device=DEV)
-    f32 = torch.empty(4, dtype=torch.float32, device=DEV)
-    i32 = torch.empty(4, dtype=torch.int32, device=DEV)
-    with pytest.raises(moe.MoEError) as e:  # refused on the host, nothing is launched
-        moe.moe_expert_ffn_combine_noalloc(s, bf, bf, bf, f32, i32, i32, i32, bf)
-    assert e.value.code == moe.MOE_ERR_UNSUPPORTED
-    assert "scratch" in str(e.value)
+    lib = moe.load_library()
+    rc = lib.moe_expert_ffn_combine_noalloc(ctypes.byref(s), *([ctypes.c_void_p(256)] * 8), None)
+    assert rc == moe.MOE_ERR_UNSUPPORTED
+    assert b"scratch" in lib.moe_last_error_string()
