@@ -22,6 +22,8 @@ Parity status of each function (what pins it, in ``tests/test_oracle.py``):
   expert_ffn     identity experts (GELU(z)-GELU(-z)=z); numpy fp64 FFN with
                  math.erf; GELU fixed points.
   combine_rows   dense masked formulation; identical experts; permutation.
+  combine_given  dense [T, rows] gate matrix times Y (numpy matmul as a
+                 step); k = 1 with w = 1 copies rows; all dropped gives 0.
   expert_swiglu  numpy fp64 gated FFN with np.exp; SiLU fixed points; a zero
                  gate or zero up projection gives 0; swapped halves differ.
 """
@@ -73,11 +75,12 @@ def _load():
         lib.oracle_combine_rows.argtypes = [I, I, I, I, I, P, P, P, P, P, P, I, P, P, I]
         lib.oracle_combine_rows_act.argtypes = [I, I, I, I, I, I, P, P, P, P, P, P, I, P, P, I]
         lib.oracle_expert_swiglu.argtypes = [I, I, P, P, P, P]
+        lib.oracle_combine_given.argtypes = [I, I, I, I, P, P, P, P]
         lib.oracle_max_threads.argtypes = []
         for name in ("oracle_router_logits", "oracle_topk", "oracle_gate_softmax",
                      "oracle_gate_softmax_all",
                      "oracle_dispatch", "oracle_expert_ffn", "oracle_combine_rows",
-                     "oracle_combine_rows_act", "oracle_expert_swiglu",
+                     "oracle_combine_rows_act", "oracle_expert_swiglu", "oracle_combine_given",
                      "oracle_max_threads"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -218,6 +221,20 @@ def combine_rows(x, w1, w2, ids, w, slot, rows=None, nthreads: int = 0, act: str
                                            _ptr(w1b), _ptr(w2b), _ptr(idz), _ptr(wz), _ptr(sz),
                                            int(r.shape[0]), _ptr(r), _ptr(y), nthreads),
            "combine_rows")
+    return y
+
+
+def combine_given(Y, w: np.ndarray, slot: np.ndarray) -> np.ndarray:
+    """y[t] = sum over kept j of w[t, j] * Y[slot[t, j]] in fp64; Y [n, H]
+    bf16 expert outputs in dispatch order, w [T, k] fp32, slot [T, k]."""
+    Yb = _bits(Y)
+    n_Y, H = Yb.shape
+    wz = np.ascontiguousarray(w, dtype=np.float32)
+    sz = np.ascontiguousarray(slot, dtype=np.int32)
+    T, k = sz.shape
+    y = np.empty((T, H), dtype=np.float64)
+    _check(_load().oracle_combine_given(T, H, k, n_Y, _ptr(Yb), _ptr(wz), _ptr(sz), _ptr(y)),
+           "combine_given")
     return y
 
 

@@ -409,3 +409,33 @@ int oracle_combine_rows_act(int T, int H, int F, int E, int k, int act, const ui
     }
     return bad;
 }
+
+/*
+ * Step 5 on expert outputs that are given rather than computed: the expert
+ * kernel's ScatterWithWeights (output(orig_pos, d) += weight * expert_out)
+ * for every token t, over its kept slots j in ascending order:
+ *   y[t] = sum_{j: slot[t][j] >= 0} w[t][j] * Y[slot[t][j]]
+ * Y [n_Y][H] holds the expert outputs in dispatch order (bf16 bit patterns,
+ * decoded exactly); the sum is in double; a token with no kept slot gets 0.
+ * A slot outside [-1, n_Y) is an error (return 3).
+ */
+int oracle_combine_given(int T, int H, int k, int n_Y, const uint16_t *Y, const float *w,
+                         const int32_t *slot, double *y)
+{
+    if (T < 0 || H < 1 || k < 1 || n_Y < 0 || !w || !slot || (T && !y)) return 1;
+    if (n_Y && !Y) return 1;
+    for (long i = 0; i < (long)T * k; i++)
+        if (slot[i] < -1 || slot[i] >= n_Y) return 3;
+    for (int t = 0; t < T; t++) {
+        double *yt = y + (size_t)t * H;
+        for (int h = 0; h < H; h++) yt[h] = 0.0;
+        for (int j = 0; j < k; j++) {
+            int32_t r = slot[(size_t)t * k + j];
+            if (r < 0) continue; /* dropped */
+            double wt = (double)w[(size_t)t * k + j];
+            const uint16_t *Yr = Y + (size_t)r * H;
+            for (int h = 0; h < H; h++) yt[h] += wt * bf16_value(Yr[h]);
+        }
+    }
+    return 0;
+}

@@ -526,14 +526,81 @@ def test_expert_parallel_ranks_match_whole_layer(G, T, H, F, E, k, cf, bias, act
     backs = _exchange_locally(layers, routed)
     whole = moe.MoELayer(full["w_router"], full["w1"], full["w2"], k, bias=full["bias"],
                          capacity_factor=cf, act=act)
+    full_cpu = moe_synth.make_inputs(cfg)
     for r in range(G):
         y = layers[r].finish(routed[r], backs[r])
+        # against the oracle: each rank's routing and dispatch over its own
+        # tokens, and its y from the oracle's combine on those decisions
+        inputs_r = dict(full_cpu, x=xs[r].cpu())
+        logits, _ = routing_parity(cfg, inputs_r, routed[r])
+        y_ora = reference_y(inputs_r, logits, np_(routed[r].ids), np_(routed[r].slot),
+                            np.arange(T, dtype=np.int32))
+        check_y(y.float().cpu().numpy(), y_ora)
+        # and against the single-GPU layer on the same tokens
         y_ref = whole(xs[r]).clone()
         assert moe.moe_get_device_status(whole.ws) == 0
         if k > 1:
             assert torch.equal(y, y_ref), f"rank {r}"
         else:  # the whole layer rounds w * acc once; here Y is rounded first
             check_y(y.float().cpu().numpy(), y_ref.double().cpu().numpy())
+
+
+# ------------------------------------------- the step entry points, one by one --
+
+@pytest.mark.parametrize("T,H,E,k,cf", [(300, 256, 16, 3, 0.7), (64, 136, 8, 1, None),
+                                        (1000, 64, 32, 8, 0.4)])
+def test_combine_entry_point_against_oracle(T, H, E, k, cf):
+    # moe_combine alone on random expert outputs Y and a dispatch with drops:
+    # y[t] = sum over kept j of w[t, j] * Y[slot[t, j]] against the oracle
+    rng = np.random.default_rng(T + H)
+    ids = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    _, offsets, _, slot = oracle.dispatch(ids, E, cf)
+    g = torch.Generator().manual_seed(T)
+    Y = torch.randn(T * k, H, generator=g).to(torch.bfloat16)
+    w = rng.uniform(0.0, 1.0, size=(T, k)).astype(np.float32)
+    y = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    moe.moe_combine(moe.make_shape(T, H, 8, E, k, cf), Y.to(DEV), torch.from_numpy(w).to(DEV),
+                    torch.from_numpy(slot).to(DEV), y)
+    torch.cuda.synchronize()
+    ref = oracle.combine_given(Y, w, slot)
+    got = y.double().cpu().numpy()
+    check_y(got, ref)
+    # an fp32 sum of at most k products, rounded once to bf16: within half a
+    # bf16 step of the exact sum, plus the fp32 rounding of the terms
+    absum = oracle.combine_given(Y.abs(), np.abs(w), slot)
+    bound = 2.0 ** -8 * np.abs(ref) + 1e-6 * absum
+    assert np.all(np.abs(got - ref) <= bound)
+    assert np.all(got[np.all(slot < 0, axis=1)] == 0.0)
+
+
+@pytest.mark.parametrize("T,H,F,E,k,cf,act", [(500, 256, 384, 16, 2, 0.8, "gelu"),
+                                              (96, 128, 256, 8, 4, None, "swiglu")])
+def test_step_entry_points_against_oracle(T, H, F, E, k, cf, act):
+    # moe_route -> moe_dispatch_rows -> moe_expert_ffn -> moe_combine: the
+    # regrouped rows are x[perm // k] bit for bit, and y is the oracle's
+    # combine on the GPU's routing decisions
+    cfg = moe_synth.MoEConfig("steps", T=T, H=H, F=F, E=E, k=k, seed=85, capacity_factor=cf,
+                              act=act)
+    inputs = moe_synth.make_inputs(cfg)
+    dev_in = to_dev(inputs)
+    s = moe.make_shape(T, H, F, E, k, cf, act=act)
+    r = moe.alloc_routing(T, E, k, DEV)
+    ws = moe.alloc_workspace(s, DEV)
+    moe.moe_route(s, dev_in["x"], dev_in["w_router"], None, r.ids, r.weights, r.counts, r.offsets,
+                  r.perm, r.slot, ws)
+    logits, rep = routing_parity(cfg, inputs, r)
+    kept = rep["kept"]
+    xp = torch.zeros(T * k, H, dtype=torch.bfloat16, device=DEV)
+    moe.moe_dispatch_rows(s, dev_in["x"], r.perm, r.offsets, xp)
+    perm = np_(r.perm)[:kept].astype(np.int64)
+    assert torch.equal(xp[:kept].cpu(), inputs["x"][perm // k])
+    Y = torch.empty(T * k, H, dtype=torch.bfloat16, device=DEV)
+    moe.moe_expert_ffn(s, E, xp, dev_in["w1"], dev_in["w2"], r.offsets, Y, ws)
+    y = torch.empty(T, H, dtype=torch.bfloat16, device=DEV)
+    moe.moe_combine(s, Y, r.weights, r.slot, y)
+    assert moe.moe_get_device_status(ws) == 0
+    y_ref = reference_y(inputs, logits, np_(r.ids), np_(r.slot), np.arange(T, dtype=np.int32))
+    check_y(y.float().cpu().numpy(), y_ref)
 
 
 # ---------------------------------------------- host batches, copies overlapped --

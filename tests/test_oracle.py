@@ -440,3 +440,36 @@ def test_thread_count_does_not_change_results():
     b = oracle.moe_forward(inp["x"], inp["w_router"], inp["w1"], inp["w2"], cfg.k, nthreads=4)
     np.testing.assert_array_equal(a["y"], b["y"])
     np.testing.assert_array_equal(a["logits"], b["logits"])
+
+
+# ------------------------------------------- combine of given expert outputs --
+
+@pytest.mark.parametrize("T,H,k,cf", [(9, 16, 3, None), (40, 8, 2, 0.6), (1, 24, 1, None)])
+def test_combine_given_dense_gate_matrix(T, H, k, cf):
+    # a second formulation: the gates as a dense [T, rows] matrix G with
+    # G[t, slot[t, j]] = w[t, j], and y = G Y by numpy's matmul
+    rng = np.random.default_rng(T * 7 + k)
+    E = 4
+    ids = np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    _, offsets, _, slot = oracle.dispatch(ids, E, cf)
+    n = int(offsets[-1])
+    Y = rand_bf16((max(n, 1), H), 1.0, T + H)
+    w = rng.uniform(0.05, 1.0, size=(T, k)).astype(np.float32)
+    G = np.zeros((T, Y.shape[0]))
+    for t in range(T):
+        for j in range(k):
+            if slot[t, j] >= 0:
+                G[t, slot[t, j]] = w[t, j]
+    np.testing.assert_allclose(oracle.combine_given(Y, w, slot), G @ f64(Y), rtol=1e-12, atol=1e-12)
+
+
+def test_combine_given_copies_rows_and_zeroes_dropped_tokens():
+    Y = rand_bf16((5, 8), 1.0, 3)
+    slot = np.array([[4], [-1], [0], [2], [-1]], dtype=np.int32)
+    w = np.ones((5, 1), dtype=np.float32)
+    y = oracle.combine_given(Y, w, slot)
+    Yd = f64(Y)
+    for t, r in enumerate(slot[:, 0]):
+        np.testing.assert_array_equal(y[t], Yd[r] if r >= 0 else np.zeros(8))
+    with pytest.raises(RuntimeError):
+        oracle.combine_given(Y, w, np.array([[5], [0], [0], [0], [0]], dtype=np.int32))
