@@ -55,9 +55,12 @@
  *     out of range) do not trap: kernels set bits in the status word, which
  *     moe_get_device_status() reads back.
  *
- * Limits (MOE_ERR_UNSUPPORTED beyond them): 1 <= E <= 256, E % 8 == 0,
+ * Limits (MOE_ERR_UNSUPPORTED beyond them): 1 <= E <= 256,
  * 1 <= k <= min(8, E), H % 8 == 0, F % 8 == 0, H >= 8, F >= 8,
  * T * k <= 2^24.  T == 0 is accepted and only clears counts/offsets.
+ * When E % 8 != 0 the rows of W_router are not 16-byte aligned; the route
+ * then first copies W_router into the workspace with its rows padded to a
+ * multiple of 8 experts (zeros, never selected).
  */
 #ifndef MOE_GB300_MOE_H
 #define MOE_GB300_MOE_H
@@ -138,15 +141,17 @@ MOE_API int64_t moe_expert_capacity(const moe_shape* s);
 
 /* Workspace bytes needed by moe_forward and moe_expert_ffn_combine (and
  * enough for every other entry point): a 1 KB status block, per-128-token
- * expert counts [ceil(T/128), E] int32, h [T*k, F] bf16, a [T*k, H] bf16
+ * expert counts [ceil(T/128), E] int32, the padded W_router copy when
+ * E % 8 != 0 (see moe_route_workspace_size), h [T*k, F] bf16, a [T*k, H] bf16
  * region that holds first the token rows in dispatch order, then the
  * expert outputs, and for T*k <= 64 rows fp32 partial expert outputs of up
  * to 4 K splits [4, T*k, H] (the small-batch second GEMM).  Returns 0 for
- * an invalid shape (E may be any 1..256 here, as moe_expert_ffn allows). */
+ * an invalid shape. */
 MOE_API size_t moe_workspace_size(const moe_shape* s);
 
-/* Workspace bytes needed by moe_route and moe_dispatch (status block and
- * per-128-token expert counts; F is ignored).  Returns 0 for an invalid
+/* Workspace bytes needed by moe_route and moe_dispatch (status block,
+ * per-128-token expert counts and, when E % 8 != 0, the padded copy of
+ * W_router [H, E rounded up to 8]; F is ignored).  Returns 0 for an invalid
  * shape. */
 MOE_API size_t moe_route_workspace_size(const moe_shape* s);
 
@@ -237,8 +242,8 @@ MOE_API int moe_dispatch_rows(const moe_shape* s, const uint16_t* x, const int32
  * rows [seg_offsets[i], seg_offsets[i+1]) of xp form segment i, computed by
  * expert i % E:  Y[r] = act(xp[r] · W1[e]) · W2[e]  (GELU, or SwiGLU with
  * W1 = [W_gate | W_up]), h and Y rounded to bf16.
- *   s: H, F, E (the experts whose weights W1 / W2 hold; any 1..256, the
- *     router's E % 8 rule does not apply), expert_act; T*k is the row
+ *   s: H, F, E (the experts whose weights W1 / W2 hold, 1..256),
+ *     expert_act; T*k is the row
  *     capacity of xp and Y (e.g. T = rows, k = 1); gating is ignored.
  *   n_segments: 1..256; seg_offsets [n_segments+1] int32 (device), non-
  *     decreasing, seg_offsets[n_segments] <= T*k (not re-validated).

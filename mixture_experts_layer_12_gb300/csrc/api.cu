@@ -114,15 +114,11 @@ int map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// experts_only: the shape describes only experts' weights (moe_expert_ffn),
-// so the router's E % 8 == 0 does not apply.
-int check_shape(const moe_shape* s, bool need_ffn, bool experts_only = false) {
+int check_shape(const moe_shape* s, bool need_ffn) {
   if (!s) return fail(MOE_ERR_INVALID_ARG, "shape is null");
   if (s->T < 0) return fail(MOE_ERR_INVALID_ARG, "T = %d < 0", s->T);
-  if (experts_only && (s->E < 1 || s->E > kMaxExperts))
+  if (s->E < 1 || s->E > kMaxExperts)
     return fail(MOE_ERR_UNSUPPORTED, "E = %d: need 1 <= E <= %d", s->E, kMaxExperts);
-  if (!experts_only && (s->E < 1 || s->E > kMaxExperts || s->E % 8 != 0))
-    return fail(MOE_ERR_UNSUPPORTED, "E = %d: need 8 <= E <= %d and E %% 8 == 0", s->E, kMaxExperts);
   if (s->k < 1 || s->k > kMaxTopK || s->k > s->E)
     return fail(MOE_ERR_UNSUPPORTED, "k = %d: need 1 <= k <= min(8, E)", s->k);
   if (s->H < 8 || s->H % 8 != 0) return fail(MOE_ERR_UNSUPPORTED, "H = %d: need H >= 8, H %% 8 == 0", s->H);
@@ -155,9 +151,10 @@ int64_t capacity_of(const moe_shape* s) {
 
 // --------------------------------------------------------------- workspace --
 
-// Workspace: [status block | per-tile expert counts | h | Y].  The status
-// block holds the device status word (byte 0) and the router's completion
-// ticket (byte 64); both are cleared at the start of every call.
+// Workspace: [status block | per-tile expert counts | padded W_router | h |
+// Y | fp32 partials].  The status block holds the device status word (byte
+// 0) and the router's completion ticket (byte 64); both are cleared at the
+// start of every call.  The padded W_router copy exists only when E % 8 != 0.
 constexpr size_t kStatusBytes = 1024;
 constexpr size_t kTicketOffset = 64;
 
@@ -165,9 +162,14 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 size_t hist_bytes(const moe_shape* s) {
   return align_up((size_t)((s->T + kSegTokens - 1) / kSegTokens) * s->E * 4, 1024);
 }
+// W_router's row pitch as the route reads it: E rounded up to 8 (16 bytes)
+int router_ldw(const moe_shape* s) { return (s->E + 7) / 8 * 8; }
+size_t wpad_bytes(const moe_shape* s) {
+  return s->E % 8 ? align_up((size_t)s->H * router_ldw(s) * 2, 1024) : 0;
+}
 size_t h_bytes(const moe_shape* s) { return align_up((size_t)s->T * s->k * s->F * 2, 1024); }
 size_t y_bytes(const moe_shape* s) { return align_up((size_t)s->T * s->k * s->H * 2, 1024); }
-size_t route_ws_bytes(const moe_shape* s) { return kStatusBytes + hist_bytes(s); }
+size_t route_ws_bytes(const moe_shape* s) { return kStatusBytes + hist_bytes(s) + wpad_bytes(s); }
 // small batches: fp32 partial expert outputs of a K-split second GEMM
 size_t part_bytes(const moe_shape* s) {
   const size_t rows = (size_t)s->T * s->k;
@@ -183,6 +185,9 @@ unsigned int* ticket_ptr(void* ws) {
 }
 int32_t* hist_ptr(void* ws) {
   return reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kStatusBytes);
+}
+uint16_t* wpad_ptr(void* ws, const moe_shape* s) {
+  return reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + kStatusBytes + hist_bytes(s));
 }
 uint16_t* h_ptr(void* ws, const moe_shape* s) {
   return reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + route_ws_bytes(s));
@@ -218,6 +223,15 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
                   int32_t* offsets, int32_t* perm, int32_t* slot, void* ws, cudaStream_t st,
                   void* const* ev = nullptr) {
   int rc;
+  // W_router rows that are not 16-byte aligned (E % 8 != 0) are read from a
+  // zero-padded copy in the workspace (the padded experts are never chosen)
+  const int ldw = router_ldw(s);
+  if (s->E % 8) {
+    uint16_t* wp = wpad_ptr(ws, s);
+    cudaError_t e = launch_pad_router_weights(w_router, s->H, s->E, ldw, wp, sms, st, ev == nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "router weight padding launch");
+    w_router = wp;
+  }
   if (s->T <= kSmallRouteTokens && s->E <= kSmallRouteExperts) {
     // small batch: logits on the CUDA cores and the dispatch by the last
     // CTA, one launch (a 32-token decode step routes in well under half the
@@ -225,6 +239,7 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
     SmallRouteArgs sa;
     sa.x = x;
     sa.w = w_router;
+    sa.ldw = ldw;
     sa.bias = b_router;
     sa.T = s->T;
     sa.H = s->H;
@@ -247,7 +262,7 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
   }
   CUtensorMap tm_x, tm_w;
   if ((rc = map_2d(&tm_x, x, (uint64_t)s->H, (uint64_t)s->T, 64, 128, "x (router)")) != MOE_OK) return rc;
-  if ((rc = map_2d(&tm_w, w_router, (uint64_t)s->E, (uint64_t)s->H, 64, 64, "w_router")) != MOE_OK) return rc;
+  if ((rc = map_2d(&tm_w, w_router, (uint64_t)ldw, (uint64_t)s->H, 64, 64, "w_router")) != MOE_OK) return rc;
   RouterArgs ra;
   ra.T = s->T;
   ra.H = s->H;
@@ -529,7 +544,7 @@ int64_t moe_expert_capacity(const moe_shape* s) {
 }
 
 size_t moe_workspace_size(const moe_shape* s) {
-  if (check_shape(s, true, /*experts_only=*/true) != MOE_OK) return 0;
+  if (check_shape(s, true) != MOE_OK) return 0;
   return ws_bytes_for(s);
 }
 
@@ -681,7 +696,7 @@ int moe_dispatch_rows(const moe_shape* s, const uint16_t* x, const int32_t* perm
 int moe_expert_ffn(const moe_shape* s, int32_t n_segments, const uint16_t* xp, const uint16_t* w1,
                    const uint16_t* w2, const int32_t* seg_offsets, uint16_t* Y, void* ws,
                    size_t ws_bytes, void* stream) {
-  int rc = check_shape(s, true, /*experts_only=*/true);
+  int rc = check_shape(s, true);
   if (rc != MOE_OK) return rc;
   if (n_segments < 1 || n_segments > kMaxExperts)
     return fail(MOE_ERR_INVALID_ARG, "n_segments = %d, must be 1..%d", n_segments, kMaxExperts);

@@ -43,7 +43,8 @@ struct RouterArgs {
 };
 // Launches ceil(T/128) x splits CTAs in clusters of `splits`.
 // tm_x: x [T, H] bf16, box {64, 128}, 128B swizzle.
-// tm_w: w_router [H, E] bf16, box {64, 64}, 128B swizzle.
+// tm_w: w_router [H, ldw] bf16 (ldw = E rounded up to 8, zero past E),
+// box {64, 64}, 128B swizzle.
 cudaError_t launch_router(const CUtensorMap& tm_x, const CUtensorMap& tm_w, const RouterArgs& a,
                           cudaStream_t st, bool pdl);
 size_t router_smem_bytes(int E);
@@ -54,7 +55,8 @@ constexpr int kSmallRouteTokens = 128;
 constexpr int kSmallRouteExperts = 64;
 struct SmallRouteArgs {
   const uint16_t* x;  // [T, H] bf16
-  const uint16_t* w;  // [H, E] bf16
+  const uint16_t* w;  // [H, ldw] bf16, columns past E zero
+  int ldw;            // W_router row pitch in elements: E rounded up to 8
   const float* bias;  // [E] or null
   int T, H, E, k;
   int capacity;       // -1: unlimited
@@ -68,6 +70,11 @@ struct SmallRouteArgs {
   unsigned int* ticket;  // zero before the launch
 };
 cudaError_t launch_router_small(const SmallRouteArgs& a, cudaStream_t st, bool pdl);
+// W_router [H, E] (E % 8 != 0) -> wp [H, ldw], ldw = E rounded up to 8,
+// zero past E: the copy the route reads when the rows are not 16-byte
+// aligned.
+cudaError_t launch_pad_router_weights(const uint16_t* w, int H, int E, int ldw, uint16_t* wp,
+                                      int sms, cudaStream_t st, bool pdl);
 // Clusters of `splits` router CTAs that can be resident at once.
 cudaError_t router_max_clusters(int E, int splits, int* out);
 

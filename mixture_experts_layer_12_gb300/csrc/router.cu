@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(RTHREADS)
 #pragma unroll
       for (int cc = 0; cc < NCH; ++cc) {
         const int e0 = (g + cc * GS) * 4;
-        if (e0 < a.E) {  // E % 8 == 0: the whole chunk is in range
+        if (e0 < a.E) {
           float4 acc = *reinterpret_cast<const float4*>(recv + (size_t)li * C::PITCH + e0);
           for (int r = 1; r < S; ++r) {
             const float4 p =
@@ -382,9 +382,14 @@ __global__ void __launch_bounds__(RTHREADS)
           float v4[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            float v = v4[i];
-            if (a.bias) v += __ldg(a.bias + e0 + i);
-            lv[cc * 4 + i] = isnan(v) ? -INFINITY : v;
+            if (e0 + i < a.E) {
+              float v = v4[i];
+              if (a.bias) v += __ldg(a.bias + e0 + i);
+              lv[cc * 4 + i] = isnan(v) ? -INFINITY : v;
+            } else {  // a zero-padded column of W_router: never selected
+              lv[cc * 4 + i] = -INFINITY;
+              taken |= 1u << (cc * 4 + i);
+            }
           }
         } else {
 #pragma unroll
@@ -566,6 +571,33 @@ __global__ void __launch_bounds__(HTHREADS) histogram_kernel(const HistArgs a) {
   }
 }
 
+// ---- W_router [H, E] with E % 8 != 0: its rows are not 16-byte aligned,
+// which TMA (and the 16-byte loads of the small-batch router) need, so the
+// route reads a copy with ldw = E rounded up to 8 columns, zero-filled
+// past E.  One thread per 8 columns of a row.
+__global__ void __launch_bounds__(256) pad_router_weights_kernel(const uint16_t* __restrict__ w,
+                                                                 int H, int E, int ldw,
+                                                                 uint16_t* __restrict__ wp) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int groups = ldw / 8;
+  const long long n = (long long)H * groups;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int h = (int)(i / groups);
+    const int e0 = (int)(i % groups) * 8;
+    uint16_t v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = e0 + u < E ? w[(size_t)h * E + e0 + u] : (uint16_t)0;
+    uint4 o;
+    o.x = (uint32_t)v[0] | ((uint32_t)v[1] << 16);
+    o.y = (uint32_t)v[2] | ((uint32_t)v[3] << 16);
+    o.z = (uint32_t)v[4] | ((uint32_t)v[5] << 16);
+    o.w = (uint32_t)v[6] | ((uint32_t)v[7] << 16);
+    *reinterpret_cast<uint4*>(wp + (size_t)h * ldw + e0) = o;
+  }
+}
+
 // ---- small batches (T <= kSmallRouteTokens, E <= 64): the whole route in
 // one launch on the CUDA cores.  One CTA per token: each thread keeps
 // partial logits for every expert over a strided slice of H (16-byte loads
@@ -596,7 +628,7 @@ __global__ void __launch_bounds__(SR_THREADS) router_small_kernel(const SmallRou
   const int lane = tid & 31;
   const int t = blockIdx.x;
   const int E = a.E;
-  const int Q = E / 8;  // 16-byte groups of experts in a W_router row
+  const int Q = a.ldw / 8;  // 16-byte groups of experts in a W_router row
 
   // ---- logits of token t
   float acc[NE];
@@ -609,7 +641,7 @@ __global__ void __launch_bounds__(SR_THREADS) router_small_kernel(const SmallRou
                          bf16_lo(xv.z), bf16_hi(xv.z), bf16_lo(xv.w), bf16_hi(xv.w)};
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-      const uint4* wrow = reinterpret_cast<const uint4*>(a.w + (size_t)(h0 + r) * E);
+      const uint4* wrow = reinterpret_cast<const uint4*>(a.w + (size_t)(h0 + r) * a.ldw);
 #pragma unroll
       for (int q = 0; q < NE / 8; ++q) {
         if (q < Q) {
@@ -815,6 +847,26 @@ cudaError_t router_max_clusters(int E, int splits, int* out) {
   if (dev >= 0 && dev < 64) cache[dev][nb][si] = n;
   *out = n;
   return cudaSuccess;
+}
+
+cudaError_t launch_pad_router_weights(const uint16_t* w, int H, int E, int ldw, uint16_t* wp,
+                                      int sms, cudaStream_t st, bool pdl) {
+  const long long n = (long long)H * (ldw / 8);
+  long long blocks = (n + 255) / 256;
+  const long long cap = (long long)(sms > 0 ? sms : 1) * 4;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    set_pdl_attr(attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, pad_router_weights_kernel, w, H, E, ldw, wp);
 }
 
 cudaError_t launch_histogram(const HistArgs& a, cudaStream_t st, bool pdl) {

@@ -58,6 +58,20 @@ def test_workspace_size_and_capacity_host_only(lib):
     assert moe.moe_expert_capacity(moe.make_shape(64, 128, 256, 8, 2, 1.0)) == 16
 
 
+def test_any_expert_count_is_accepted_and_pads_w_router(lib):
+    # E % 8 != 0: the route reads a copy of W_router with its rows padded to
+    # a multiple of 8 experts, [H, E rounded up to 8] bf16, in the workspace
+    for E in (1, 2, 4, 6, 13, 250):
+        k = min(E, 2)
+        s = moe.make_shape(300, 4096, 256, E, k)
+        pad = -(-4096 * (-(-E // 8) * 8) * 2 // 1024) * 1024
+        hist = -(-(3 * E * 4) // 1024) * 1024
+        assert moe.moe_route_workspace_size(s) == 1024 + hist + pad
+        assert moe.moe_workspace_size(s) == 1024 + hist + pad + 300 * k * (256 + 4096) * 2
+    s8 = moe.make_shape(300, 4096, 256, 16, 2)
+    assert moe.moe_route_workspace_size(s8) == 1024 + 1024  # no copy when E % 8 == 0
+
+
 @pytest.mark.parametrize("T,k,E,cf", [(8192, 4, 64, 1.2), (64, 2, 8, 1.0), (10, 1, 8, 0.8),
                                       (3, 2, 8, 1.0), (100, 8, 256, 0.37), (7, 3, 16, float("nan"))])
 def test_capacity_matches_oracle(lib, T, k, E, cf):
@@ -66,7 +80,7 @@ def test_capacity_matches_oracle(lib, T, k, E, cf):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(E=7), moe.MOE_ERR_UNSUPPORTED), (dict(E=264), moe.MOE_ERR_UNSUPPORTED),
+    (dict(E=0), moe.MOE_ERR_UNSUPPORTED), (dict(E=264), moe.MOE_ERR_UNSUPPORTED),
     (dict(k=9), moe.MOE_ERR_UNSUPPORTED), (dict(k=0), moe.MOE_ERR_UNSUPPORTED),
     (dict(H=100), moe.MOE_ERR_UNSUPPORTED), (dict(F=12), moe.MOE_ERR_UNSUPPORTED),
     (dict(T=-1), moe.MOE_ERR_INVALID_ARG), (dict(T=1 << 22, k=8), moe.MOE_ERR_UNSUPPORTED),
@@ -76,10 +90,7 @@ def test_bad_shapes_rejected_before_launch(lib, kw, code):
     base = dict(T=64, H=128, F=256, E=8, k=2)
     base.update(kw)
     s = moe.make_shape(**base)
-    if kw == dict(E=7):  # a valid expert count for moe_expert_ffn, not for the router
-        assert lib.moe_workspace_size(ctypes.byref(s)) > 0
-    else:
-        assert lib.moe_workspace_size(ctypes.byref(s)) == 0
+    assert lib.moe_workspace_size(ctypes.byref(s)) == 0
     rc = lib.moe_forward(ctypes.byref(s), *([None] * 13), 0, None)
     assert rc == code
     assert lib.moe_last_error_string()
@@ -132,9 +143,11 @@ def test_step_entry_points_validate_before_touching_the_device(lib):
     for n in (0, 257, -3):
         assert lib.moe_expert_ffn(ctypes.byref(s), n, None, None, None, None, None, ws, 1 << 30,
                                   None) == moe.MOE_ERR_INVALID_ARG
-    bad = moe.make_shape(64, 128, 256, 7, 1)  # E not a multiple of 8
-    assert lib.moe_dispatch_rows(ctypes.byref(bad), None, None, None, None, None) != moe.MOE_OK
-    assert lib.moe_combine(ctypes.byref(bad), None, None, None, None, None) != moe.MOE_OK
+    bad = moe.make_shape(64, 128, 256, 300, 1)  # more experts than the limit
+    assert lib.moe_dispatch_rows(ctypes.byref(bad), None, None, None, None, None) == \
+        moe.MOE_ERR_UNSUPPORTED
+    assert lib.moe_combine(ctypes.byref(bad), None, None, None, None, None) == \
+        moe.MOE_ERR_UNSUPPORTED
 
 
 def test_forward_plan_is_a_host_only_shape_rule(lib):

@@ -180,7 +180,13 @@ def test_small_batch_route_in_one_launch(T, E, k, cf, gating, bias):
 
 @pytest.mark.parametrize("T,H,E,k,bias", [(1, 64, 8, 1, None), (130, 200, 16, 3, 0.5),
                                           (257, 520, 256, 8, None), (64, 4096, 40, 5, 2.0),
-                                          (300, 72, 192, 2, None)])
+                                          (300, 72, 192, 2, None),
+                                          # E % 8 != 0 (W_router read from a padded copy):
+                                          # small-batch and tensor-core routers
+                                          (100, 256, 1, 1, None), (64, 264, 4, 3, 1.0),
+                                          (128, 136, 6, 6, None), (200, 136, 2, 2, None),
+                                          (300, 520, 6, 4, 0.5), (1000, 256, 13, 5, None),
+                                          (300, 128, 250, 8, None), (129, 64, 1, 1, None)])
 def test_router_edge_shapes(T, H, E, k, bias):
     cfg = moe_synth.MoEConfig("edge", T=T, H=H, F=0, E=E, k=k, seed=11, bias0=bias)
     inputs = moe_synth.make_inputs(cfg, with_ffn=False)
@@ -253,6 +259,11 @@ def test_forward_skewed_sampled(cfg):
     (150, 64, 128, 8, 1, None, 50.0),       # all tokens to expert 0, others empty
     (33, 512, 1408, 64, 4, 1.0, None),      # many experts with 0-3 rows
     (129, 72, 8, 8, 3, None, None),         # F = 8
+    (50, 128, 256, 1, 1, None, None),       # one expert
+    (200, 64, 128, 2, 2, None, None),       # two experts, both chosen by every token
+    (129, 256, 264, 4, 3, None, 1.0),       # four experts, tensor-core router
+    (300, 136, 200, 6, 4, 0.8, None),       # six experts, drops
+    (500, 256, 256, 13, 2, None, None),     # thirteen experts
 ])
 def test_forward_edge_shapes(T, H, F, E, k, cf, bias):
     cfg = moe_synth.MoEConfig("edge", T=T, H=H, F=F, E=E, k=k, seed=21, capacity_factor=cf,
