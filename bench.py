@@ -13,6 +13,11 @@ N > 1 runs under torchrun: every rank runs its own batch of T tokens with the
 same weights (data-parallel replicas, no collective on the data path);
 value = all ranks' tokens / max over ranks of the timed region.
 --impl reference times the plain CPU oracle on the host cores instead.
+
+At N = 1 the default run also measures, after the headline line's own
+workload, the decode step (weight-stream bound) and the router sweep at
+k = 2 (routing bound), each with its own roofline, under "extra_workloads"
+(--no-extras skips them).
 """
 from __future__ import annotations
 
@@ -39,21 +44,20 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # one ncu capture, keyed by workload/kernel and by the sha256 of the kernel
 # source it was taken on; reported as null once the source changes.
 NCU_TRAFFIC = {
-    # prefill workload (profiles/expert_gemm_prefill.md, profiles/router_prefill.md):
-    # dram__bytes_read.sum + dram__bytes_write.sum of one launch
+    # prefill workload: dram__bytes_read.sum + dram__bytes_write.sum of one launch
     "prefill/expert_gemm1": {"bytes": 1027551744 + 221377280, "src": "ffn_gemm.cu", "src_sha": "9c589b4d85665278"},
     "prefill/expert_gemm2": {"bytes": 1417872640 + 65498880, "src": "ffn_gemm.cu", "src_sha": "9c589b4d85665278"},
     "prefill/router": {"bytes": 33676032, "src": "router.cu", "src_sha": "d3b06cd2819ee340"},
-    # router sweep, k = 1 (profiles/router_prefill.md): router_kernel + dispatch_kernel of one call
+    # router sweep, k = 1: router_kernel + dispatch_kernel of one call
     "router_k1/router+dispatch": {"bytes": 17889024 + 40448, "src": ["router.cu", "dispatch_combine.cu"],
                                   "src_sha": ["d3b06cd2819ee340", "67a1c639e9ea246b"]},
-    # decode workload (profiles/decode_weight_stream.md): both GEMMs on the small-batch kernel
+    # decode workload: both GEMMs on the small-batch kernel
     "decode/expert_gemm1": {"bytes": 940161024 + 3989760, "src": "ffn_gemm_small.cu", "src_sha": "ff59fa4c79617713"},
     "decode/expert_gemm2": {"bytes": 941419776 + 5054208, "src": "ffn_gemm_small.cu", "src_sha": "ff59fa4c79617713"},
 }
 
 
-def parse_args():
+def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=1000)
@@ -64,9 +68,11 @@ def parse_args():
     p.add_argument("--graph-steps", type=int, default=20,
                    help="forward steps captured per CUDA graph in the timed region")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-sample-tokens", type=int, default=1366,
-                   help="tokens of the workload the oracle runs for cpu_baseline")
-    return p.parse_args()
+    p.add_argument("--cpu-stride", type=int, default=16,
+                   help="cpu_baseline: the oracle's FFN and combine run on every n-th token")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the decode and router-sweep measurements after the headline")
+    return p.parse_args(argv)
 
 
 def load_peaks():
@@ -235,29 +241,92 @@ def kernel_work(cfg, n_rows, experts_hit):
     }
 
 
+# ---------------------------------------------------------------- rooflines --
+
+# A timed region shorter than this, with no power-cap throttling seen in it,
+# runs at burst clocks: its GEMMs are measured against the burst bf16 peak.
+SUSTAINED_REGION_MS = 1000.0
+
+
+def tensor_peak(peaks, region_ms, clocks):
+    """(peak TFLOP/s, kind) for a contraction timed over `region_ms` with the
+    sampled `clocks`: the burst figure for a short region at full clocks, the
+    sustained one for a region of a second or more or one that hit the
+    power cap."""
+    capped = bool(clocks) and "sw_power_cap" in clocks.get("reasons", [])
+    if region_ms >= SUSTAINED_REGION_MS or capped:
+        return peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]), "sustained"
+    return peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]), "burst"
+
+
+def roofline(work, ms, peaks, peak_src, region_ms, clocks, name):
+    """The roofline object of one kernel: tensor-bound when its arithmetic
+    intensity exceeds the ridge of the measured peaks, HBM-bound otherwise."""
+    ridge = (peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) * 1e12 /
+             (peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]) * 1e9))
+    if work["flops"] / max(work["bytes"], 1.0) > ridge:
+        ach = work["flops"] / (ms * 1e-3) / 1e12
+        peak, kind = tensor_peak(peaks, region_ms, clocks)
+        burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+        sus = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+        return {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4),
+                "peak_kind": f"bf16 dense, {kind} ({peak_src}): timed region {region_ms:.0f} ms",
+                "frac_of_burst": round(ach / burst, 4), "frac_of_sustained": round(ach / sus, 4),
+                "kernel": name, "flops_per_launch": work["flops"]}
+    ach = work["bytes"] / (ms * 1e-3) / 1e9
+    peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(ach / peak, 4), "peak_kind": f"HBM copy ({peak_src})",
+            "kernel": name, "bytes_per_launch": work["bytes"]}
+
+
 # ------------------------------------------------------------ cpu baseline --
 
-def oracle_sample_run(inputs, cfg, rows):
-    """The oracle as it stands on a token sample: routing, dispatch, expert
-    FFN and combine for the sampled tokens (no capacity limit, so a token's
-    result does not depend on the unsampled ones)."""
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.machine()
+
+
+def oracle_step(inputs, cfg, rows):
+    """The oracle as it stands on one batch of the workload: routing and
+    dispatch (capacity included) for all T tokens, then the expert FFN and
+    combine for the tokens in `rows` (tokens are independent once routed and
+    dispatched).  Returns (seconds of routing + dispatch, seconds of FFN +
+    combine)."""
     import oracle
-    xs = inputs["x"][rows]
     t0 = time.perf_counter()
-    oracle.moe_forward(xs, inputs["w_router"], inputs["w1"], inputs["w2"], cfg.k,
-                       bias=inputs["bias"], capacity_factor=cfg.capacity_factor, act=cfg.act)
-    return time.perf_counter() - t0
+    logits, ids, _, w = oracle.route(inputs["x"], inputs["w_router"], cfg.k, bias=inputs["bias"])
+    _, _, _, slot = oracle.dispatch(ids, cfg.E, cfg.capacity_factor)
+    t1 = time.perf_counter()
+    if rows and cfg.has_ffn:
+        oracle.combine_rows(inputs["x"], inputs["w1"], inputs["w2"], ids, w, slot, rows,
+                            act=cfg.act)
+    return t1 - t0, time.perf_counter() - t1
 
 
-def cpu_baseline(inputs, cfg, n_tokens):
+def cpu_baseline(inputs, cfg, stride):
+    """Oracle-equivalent full time of one batch: routing + dispatch of all T
+    tokens, plus the FFN and combine of every `stride`-th token scaled by
+    T / (tokens computed)."""
     import oracle
     oracle.build()
-    stride = max(1, cfg.T // max(1, n_tokens))
-    rows = list(range(0, cfg.T, stride))[:n_tokens]
-    dt = oracle_sample_run(inputs, cfg, rows)
-    return {"value": len(rows) / dt, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"{len(rows)} of {cfg.T} tokens (token stride {stride}): routing, dispatch, "
-                      f"fp64 expert FFN and combine for those tokens; {dt:.1f} s"}
+    rows = list(range(0, cfg.T, stride)) if cfg.has_ffn else []
+    t_route, t_ffn = oracle_step(inputs, cfg, rows)
+    full = t_route + (t_ffn * cfg.T / len(rows) if rows else 0.0)
+    what = (f"routing + dispatch of all {cfg.T} tokens ({t_route:.2f} s)"
+            + (f" + {cfg.T / len(rows):.0f} x FFN and combine of every {stride}-th token "
+               f"({len(rows)} tokens, {t_ffn:.2f} s)" if rows else ""))
+    return {"value": cfg.T / full, "unit": UNIT, "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"oracle-equivalent full time {full:.2f} s: {what}",
+            "cpu": cpu_model(), "nproc": os.cpu_count()}
 
 
 # --------------------------------------------------------------- reference --
@@ -271,33 +340,38 @@ def run_reference(args):
     oracle.build()
     cfg = workload_cfg(args.workload)
     inputs = moe_synth.make_inputs(cfg)
-    # size each step's token sample so that warm-up + steps take ~90 s
-    probe = list(range(0, cfg.T, max(1, cfg.T // 4)))[:4]
-    per_token = oracle_sample_run(inputs, cfg, probe) / len(probe)
+    # each step: routing + dispatch of all T tokens and the FFN of a strided
+    # token sample, sized so that warm-up + steps take about 90 s
     n_steps = max(1, args.warmup + args.steps)
-    per_step = int(max(1, min(64, cfg.T, 90.0 / (n_steps * per_token))))
-    stride = max(1, cfg.T // per_step)
-    total, times = 0, []
-    for i in range(args.warmup + args.steps):
-        start = (i * 7) % stride
-        rows = list(range(start, cfg.T, stride))[:per_step]
-        dt = oracle_sample_run(inputs, cfg, rows)
+    probe = list(range(0, cfg.T, max(1, cfg.T // 4)))[:4] if cfg.has_ffn else []
+    t_route, t_probe = oracle_step(inputs, cfg, probe)
+    per_token = t_probe / len(probe) if probe else 0.0
+    budget = max(0.0, 90.0 / n_steps - t_route)
+    n_ffn = 0
+    if cfg.has_ffn:
+        n_ffn = int(max(1, min(cfg.T // 16 or 1, budget / max(per_token, 1e-9))))
+    stride = max(1, cfg.T // n_ffn) if n_ffn else 0
+    full_times = []
+    for i in range(n_steps):
+        rows = list(range((i * 7) % stride, cfg.T, stride))[:n_ffn] if n_ffn else []
+        tr, tf = oracle_step(inputs, cfg, rows)
         if i >= args.warmup:
-            times.append(dt)
-            total += len(rows)
-    elapsed = sum(times)
-    value = total / elapsed
+            full_times.append(tr + (tf * cfg.T / len(rows) if rows else 0.0))
+    elapsed = sum(full_times)
+    value = cfg.T * len(full_times) / elapsed
+    sample = (f"per step: routing + dispatch of all {cfg.T} tokens"
+              + (f", FFN and combine of {n_ffn} tokens (stride {stride}) scaled to all {cfg.T}"
+                 if n_ffn else ""))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1000.0 * elapsed / max(1, args.steps), "higher_is_better": True,
+        "ms_per_step": 1000.0 * elapsed / max(1, len(full_times)), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(cfg), "tokens_per_step": per_step,
+        "config": {"workload": workload_desc(cfg), "ffn_tokens_per_step": n_ffn,
                    "parallelism": "host cores (OpenMP over tokens)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.max_threads(),
-                         "kind": "oracle",
-                         "sample": f"{per_step} of {cfg.T} tokens per step (strided), routing, "
-                                   "dispatch, fp64 expert FFN and combine"},
+                         "kind": "oracle", "sample": sample, "cpu": cpu_model(),
+                         "nproc": os.cpu_count()},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -306,7 +380,7 @@ def run_reference(args):
 
 # -------------------------------------------------------------------- ours --
 
-def run_route_only(args, cfg, device):
+def measure_route(args, cfg, device, with_cpu=True):
     """Router sweep: one step = moe_route (router + dispatch) over T tokens.
     Rotates through enough copies of x that the set exceeds L2."""
     import torch
@@ -381,47 +455,40 @@ def run_route_only(args, cfg, device):
 
     peaks, src = load_peaks()
     w = kernel_work(cfg, cfg.T * cfg.k, 0)
-    route_bytes = w["router"]["bytes"] + w["dispatch"]["bytes"]
-    ach = route_bytes / (ms * 1e-3) / 1e9
-    line = {
+    route_work = {"flops": w["router"]["flops"],
+                  "bytes": w["router"]["bytes"] + w["dispatch"]["bytes"]}
+    roof = roofline(route_work, ms, peaks, src, elapsed, clk, "route (router + dispatch)")
+    roof["traffic"] = ncu_traffic(f"{cfg.name}/router+dispatch")
+    return {
         "metric": METRIC, "value": cfg.T / (ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "step": "moe_route (router + dispatch)",
                    "l2": f"{copies} rotating copies of x ({copies * x0.numel() * 2 / 1e6:.0f} MB > L2)"},
-        # status clear + router (+ dispatch)
-        "gpu_launches": (2 if moe.moe_forward_plan(s)[0] else 3) * K,
-        "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks.get("hbm_gbs"),
-                     "unit": "GB/s", "frac": round(ach / peaks.get("hbm_gbs", 6800.0), 4),
-                     "peak_kind": f"HBM copy ({src})", "kernel": "router+dispatch",
-                     "bytes_per_launch": route_bytes, "traffic": ncu_traffic(f"{cfg.name}/router+dispatch")},
+        "gpu_launches": route_launches(s) * K,
+        "roofline": roof,
         "clocks": clk,
         "e2e": e2e,
+        "cpu_baseline": (cpu_baseline(inputs, cfg, args.cpu_stride)
+                         if with_cpu and not args.no_cpu_baseline else None),
     }
-    print(json.dumps(line), flush=True)
-    return 0
 
 
-def run_ours(args):
+def route_launches(shape):
+    """Kernels one moe_route call launches: the status clear, the W_router
+    padding when E % 8 != 0, the router, and the dispatch unless the router
+    does it."""
+    import mixture_experts_layer_12_gb300 as moe
+    in_router, _ = moe.moe_forward_plan(shape)
+    return 2 + (0 if in_router else 1) + (1 if shape.E % 8 else 0)
+
+
+def measure_forward(args, cfg, device, world=1, rank=0, with_cpu=True):
+    """One step = one moe_forward over T tokens (every kernel of the layer)."""
     import torch
     import torch.distributed as dist
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl")
-    device = torch.device("cuda", local_rank)
-    torch.cuda.set_device(device)
-
-    from mixture_experts_layer_12_gb300 import build as moe_build
-    moe_build.build()
     import mixture_experts_layer_12_gb300 as moe
-    import moe_synth
 
-    cfg = workload_cfg(args.workload)
-    if not cfg.has_ffn:
-        return run_route_only(args, cfg, device)
     inputs = rank_inputs(cfg, rank, world)
     dev = {k: (None if v is None else v.to(device)) for k, v in inputs.items()}
     layer = moe.MoELayer(dev["w_router"], dev["w1"], dev["w2"], cfg.k, bias=dev["bias"],
@@ -529,25 +596,8 @@ def run_ours(args):
         kernels[n] = {"ms": round(ms, 5), "share": round(ms / sum(per_kernel.values()), 4),
                       "tflops": round(work[n]["flops"] / (ms * 1e-3) / 1e12, 2),
                       "gbs": round(work[n]["bytes"] / (ms * 1e-3) / 1e9, 1)}
-    dk = work[dominant]
-    # tensor-bound when the kernel's arithmetic intensity exceeds the ridge
-    # point of the measured peaks, HBM-bound otherwise
-    ridge = (peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) * 1e12 /
-             (peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]) * 1e9))
-    if dk["flops"] / max(dk["bytes"], 1.0) > ridge:
-        ach = dk["flops"] / (per_kernel[dominant] * 1e-3) / 1e12
-        peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(ach / peak, 4),
-                "peak_kind": f"bf16 dense, sustained ({peak_src})",
-                "frac_of_burst": round(ach / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]), 4),
-                "kernel": dominant, "flops_per_launch": dk["flops"]}
-    else:
-        ach = dk["bytes"] / (per_kernel[dominant] * 1e-3) / 1e9
-        peak = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(ach / peak, 4), "peak_kind": f"HBM copy ({peak_src})",
-                "kernel": dominant, "bytes_per_launch": dk["bytes"]}
+    roof = roofline(work[dominant], per_kernel[dominant], peaks, peak_src, elapsed_ms, clk,
+                    dominant)
     roof["traffic"] = ncu_traffic(f"{cfg.name}/{dominant}")
 
     # end to end through the public API with host buffers: H2D of x, the
@@ -591,33 +641,82 @@ def run_ours(args):
            "serial_value": whole_job_throughput(cfg.T, world, E2E, serial_ms)}
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(inputs, cfg, args.cpu_sample_tokens)
+    if with_cpu and rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inputs, cfg, args.cpu_stride)
 
-    if world > 1:
-        dist.destroy_process_group()
-    if rank != 0:
-        return 0
-    line = {
+    # free the layer's device memory before the next workload is measured
+    del layer, dev, x, x_dev, graph, graph_prof, pipe
+    torch.cuda.synchronize(device)
+    torch.cuda.empty_cache()
+    return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(cfg), "tokens_per_gpu": cfg.T,
                    "parallelism": f"replicas x{world} (token data-parallel, no collective)",
                    "kept_rows": n_rows, "experts_hit": experts_hit,
-                   "timing": f"CUDA events around {reps} replays of a CUDA graph of {R} forward steps; "
-                             "per-kernel times from a second graph of the same steps with "
-                             "events between the kernels",
+                   "timing": f"CUDA events around {reps} replays of a CUDA graph of {R} forward steps "
+                             f"({elapsed_ms:.1f} ms); per-kernel times from a second graph of the "
+                             "same steps with events between the kernels",
                    "per_kernel_sum_ms": round(sum(per_kernel.values()), 5),
                    "l2": "inputs larger than L2: every step streams all expert weights "
                          f"({2 * (3 if cfg.act == 'swiglu' else 2) * cfg.E * cfg.H * cfg.F / 1e9:.2f} GB)"},
-        "gpu_launches": (len(launched) + 1) * K,  # + the status clear that opens each call
+        # + the status clear that opens each call (+ the W_router padding when E % 8 != 0)
+        "gpu_launches": (len(launched) + 1 + (1 if cfg.E % 8 else 0)) * K,
         "roofline": roof,
         "kernels": kernels,
         "clocks": clk,
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
+
+
+def measure(args, cfg, device, world=1, rank=0, with_cpu=True):
+    if cfg.has_ffn:
+        return measure_forward(args, cfg, device, world, rank, with_cpu)
+    return measure_route(args, cfg, device, with_cpu)
+
+
+EXTRA_WORKLOADS = ("decode", "router_k2")
+
+
+def extra_summary(line):
+    """The parts of a workload's line that the headline line carries for it."""
+    keep = ("value", "unit", "ms_per_step", "steps", "roofline", "clocks", "e2e", "cpu_baseline",
+            "gpu_launches")
+    out = {k: line[k] for k in keep if k in line}
+    out["workload"] = line["config"]["workload"]
+    if "kernels" in line:
+        out["kernels"] = line["kernels"]
+    return out
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+
+    from mixture_experts_layer_12_gb300 import build as moe_build
+    moe_build.build()
+
+    cfg = workload_cfg(args.workload)
+    if not cfg.has_ffn and world > 1:
+        raise SystemExit("router-only workloads run on one GPU")
+    line = measure(args, cfg, device, world, rank)
+    if world == 1 and not args.no_extras and args.workload == "prefill":
+        line["extra_workloads"] = {name: extra_summary(measure(args, workload_cfg(name), device))
+                                   for name in EXTRA_WORKLOADS}
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
     print(json.dumps(line), flush=True)
     return 0
 

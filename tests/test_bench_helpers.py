@@ -64,3 +64,41 @@ def test_ncu_traffic_only_for_the_sources_it_was_taken_on(monkeypatch):
     monkeypatch.setitem(bench.NCU_TRAFFIC, multi, dict(m, src_sha=[shas[0], "0" * 16]))
     assert bench.ncu_traffic(multi) is None
     assert bench.ncu_traffic("no/such") is None
+
+
+def test_tensor_peak_follows_the_timed_region_and_clocks():
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    full = {"sm_mhz": 2070.0, "reasons": []}
+    capped = {"sm_mhz": 1650.0, "reasons": ["sw_power_cap"]}
+    # a short region at full clocks is a burst; a long one, or one that hit
+    # the power cap, runs at the sustained rate
+    assert bench.tensor_peak(peaks, 25.0, full) == (1900.0, "burst")
+    assert bench.tensor_peak(peaks, 25.0, capped) == (1700.0, "sustained")
+    assert bench.tensor_peak(peaks, 1400.0, full) == (1700.0, "sustained")
+    assert bench.tensor_peak(peaks, 25.0, None) == (1900.0, "burst")
+
+
+def test_roofline_reports_both_tensor_fractions():
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0}
+    gemm = {"flops": 1.0e12, "bytes": 1.0e9}  # intensity 1000 FLOP/B > ridge
+    r = bench.roofline(gemm, 1.0, peaks, "measured", 20.0, {"reasons": []}, "expert_gemm1")
+    assert r["bound"] == "tensor" and r["achieved"] == 1000.0
+    assert r["frac"] == 0.5 and r["frac_of_burst"] == 0.5 and r["frac_of_sustained"] == 0.625
+    assert "burst" in r["peak_kind"]
+    stream = {"flops": 1.0e9, "bytes": 3.0e9}
+    h = bench.roofline(stream, 1.0, peaks, "measured", 20.0, None, "route")
+    assert h["bound"] == "hbm" and h["achieved"] == 3000.0 and h["frac"] == 0.5
+
+
+def test_cpu_baseline_is_the_oracle_equivalent_full_time():
+    import oracle
+    oracle.build()
+    cfg = moe_synth.TINY
+    inputs = moe_synth.make_inputs(cfg)
+    cb = bench.cpu_baseline(inputs, cfg, 16)
+    assert cb["kind"] == "oracle" and cb["unit"] == "tokens/s" and cb["value"] > 0
+    assert "every 16-th token (4 tokens" in cb["sample"] and cb["nproc"] >= 1
+    route_only = bench.cpu_baseline(moe_synth.make_inputs(moe_synth.ROUTER[2].with_(T=64, H=128),
+                                                          with_ffn=False),
+                                    moe_synth.ROUTER[2].with_(T=64, H=128), 16)
+    assert "FFN" not in route_only["sample"]

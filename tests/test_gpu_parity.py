@@ -17,6 +17,9 @@ from parity import check_dispatch, check_routing, check_y, reference_y
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
+# the seeded workloads whose oracle routing figures tests/golden/routing_stats.json holds
+STATS_WORKLOADS = ("tiny", "prefill", "router_k1", "router_k2", "router_k4", "router_k8", "skewed",
+                   "skewed_cf1.2", "decode", "prefill_k1")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -61,7 +64,28 @@ def routing_parity(cfg, inputs, r, nthreads=0, gating=0):
     rep = check_routing(logits, o_ids, o_w, gids, np_(r.weights), gating)
     rep.update(check_dispatch(gids, cfg.E, cfg.capacity_factor, np_(r.counts), np_(r.offsets),
                               np_(r.perm), np_(r.slot)))
+    rep["ids_equal_oracle_everywhere"] = bool(np.array_equal(gids, o_ids))
+    if cfg.name in STATS_WORKLOADS and gating == 0:
+        check_stats(cfg, rep, gids, o_ids)
     return logits, rep
+
+
+def check_stats(cfg, rep, gpu_ids, ora_ids):
+    """The GPU's routing against the oracle's figures stored in
+    tests/golden/routing_stats.json (written from the oracle alone): the
+    near-tie count, and the kept / dropped assignments -- exactly when the
+    GPU chose the oracle's experts for every token, else within the tokens
+    whose expert set may differ."""
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "routing_stats.json")) as f:
+        st = json.load(f)["workloads"][cfg.name]
+    assert rep["near_tie_tokens"] == st["near_tie_tokens"]
+    if np.array_equal(gpu_ids, ora_ids):
+        assert (rep["kept"], rep["dropped"]) == (st["kept_assignments"], st["dropped_assignments"])
+    else:
+        assert abs(rep["dropped"] - st["dropped_assignments"]) <= cfg.k * st["membership_ties"]
+    return st
 
 
 def forward_parity(cfg, stride=1, nthreads=0, gating=0):

@@ -473,3 +473,17 @@ def test_combine_given_copies_rows_and_zeroes_dropped_tokens():
         np.testing.assert_array_equal(y[t], Yd[r] if r >= 0 else np.zeros(8))
     with pytest.raises(RuntimeError):
         oracle.combine_given(Y, w, np.array([[5], [0], [0], [0], [0]], dtype=np.int32))
+
+
+def test_stored_routing_stats_match_the_oracle():
+    # tests/golden/routing_stats.json is written by make_routing_stats.py
+    # from the oracle; recompute the small workloads' rows
+    import importlib.util
+    path = os.path.join(os.path.dirname(__file__), "golden", "make_routing_stats.py")
+    spec = importlib.util.spec_from_file_location("make_routing_stats", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    with open(os.path.join(os.path.dirname(__file__), "golden", "routing_stats.json")) as f:
+        stored = json.load(f)["workloads"]
+    for name in ("tiny", "decode"):
+        assert mod.stats(moe_synth.ALL[name]) == stored[name]
