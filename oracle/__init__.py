@@ -46,10 +46,14 @@ _lib = None
 def build(force: bool = False) -> str:
     """Compile ``moe_oracle.c`` into ``libmoe_oracle.so`` with gcc/OpenMP."""
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC),
+                                                   os.path.getmtime(os.path.abspath(__file__)))):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+    # -ffp-contract=off: every product and sum is its own IEEE double
+    # operation, as written; gcc would otherwise fuse them into FMAs on
+    # aarch64 (not on x86-64), and the results would differ between machines
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
            "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
