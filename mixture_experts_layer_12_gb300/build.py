@@ -17,8 +17,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libmoe.so")
-SOURCES = ["api.cu", "router.cu", "dispatch_combine.cu", "ffn_gemm.cu", "ffn_gemm_small.cu"]
-HEADERS = ["tc_common.cuh", "moe_internal.h"]
+SOURCES = ["api.cu", "router.cu", "route_fused.cu", "dispatch_combine.cu", "ffn_gemm.cu",
+           "ffn_gemm_small.cu"]
+HEADERS = ["tc_common.cuh", "moe_internal.h", "route_topk.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

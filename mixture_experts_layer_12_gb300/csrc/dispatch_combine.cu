@@ -373,10 +373,10 @@ cudaError_t launch_1d(Kernel k, dim3 grid, int threads, cudaStream_t st, bool pd
   return cudaLaunchKernelEx(&cfg, k, a);
 }
 
-// Zeroes a call's status block (status word and ticket, 32 ints) as a
-// kernel: a memset node between two kernels costs several microseconds of
-// serialisation, and a kernel can start early under programmatic dependent
-// launch like every other kernel of the call.
+// Zeroes a call's status block (status word, ticket and the fused route's
+// counters: 256 ints) as a kernel: a memset node between two kernels costs
+// several microseconds of serialisation, and a kernel can start early under
+// programmatic dependent launch like every other kernel of the call.
 __global__ void clear_status_kernel(int* p) {
   pdl_launch_dependents();
   pdl_wait();
@@ -384,7 +384,7 @@ __global__ void clear_status_kernel(int* p) {
 }
 
 cudaError_t launch_clear_status(int* p, cudaStream_t st, bool pdl) {
-  return launch_1d(clear_status_kernel, dim3(1), 32, st, pdl, p);
+  return launch_1d(clear_status_kernel, dim3(1), 256, st, pdl, p);
 }
 
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st, bool pdl) {

@@ -49,6 +49,41 @@ cudaError_t launch_router(const CUtensorMap& tm_x, const CUtensorMap& tm_w, cons
                           cudaStream_t st, bool pdl);
 size_t router_smem_bytes(int E);
 
+// ---- the whole route (router + dispatch) in one launch for batches of up
+// to kFusedMaxTiles tiles of 128 tokens (route_fused.cu): tiles x splits
+// CTAs, all resident at once, K split across the CTAs of a tile with the
+// fp32 partials exchanged through the workspace.
+constexpr int kFusedMaxTiles = 128;   // T <= 16384 tokens
+constexpr int kFusedMaxSplits = 12;   // K splits per tile
+constexpr int kFusedMaxCtas = 256;    // tiles x splits
+struct FusedRouteArgs {
+  int T, H, E, k;
+  int npad;        // E rounded up to 16: MMA N and the partial's row pitch (floats)
+  int ep;          // E rounded up to 16: row pitch of the per-CTA counts (bytes)
+  int tmem_cols;   // power of two >= max(32, npad)
+  int capacity;    // -1: unlimited
+  int gating;      // MOE_GATE_*
+  const float* bias;  // [E] or null
+  int32_t* ids;       // [T, k]
+  float* weights;     // [T, k]
+  int32_t* counts;    // [E]
+  int32_t* offsets;   // [E+1]
+  int32_t* perm;      // [T*k]
+  int32_t* slot;      // [T, k]
+  float* part;        // workspace: [tiles * splits][128][npad] fp32 partial logits
+  uint8_t* grp_hist;  // workspace: [tiles * splits][ep] assignments per expert
+  unsigned* tile_cnt; // [tiles] zero before the launch
+  unsigned* grid_cnt; // zero before the launch
+  int* status;
+  uint64_t wait_limit_ns;
+};
+// tm_x / tm_w as for launch_router; grid (splits, ceil(T/128)).
+cudaError_t launch_route_fused(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
+                               const FusedRouteArgs& a, int splits, cudaStream_t st, bool pdl);
+// CTAs of the fused route kernel (for E experts) resident per SM on the
+// current device (0 before route_fused_set_attributes ran on it).
+int route_fused_resident_per_sm(int E);
+
 // ---- small-batch route (router + dispatch in one launch, CUDA cores):
 // for T <= kSmallRouteTokens and E <= kSmallRouteExperts.
 constexpr int kSmallRouteTokens = 128;
@@ -120,7 +155,7 @@ struct DispatchArgs {
   int* status;
 };
 cudaError_t launch_dispatch(const DispatchArgs& a, cudaStream_t st, bool pdl);
-// The status block (32 ints at p) set to zero by a one-warp kernel.
+// The status block (256 ints at p) set to zero by a one-CTA kernel.
 cudaError_t launch_clear_status(int* p, cudaStream_t st, bool pdl);
 
 // ---- grouped expert GEMM (tcgen05 + TMA, persistent ragged scheduler).

@@ -1,0 +1,548 @@
+// route_fused.cu -- the whole route in one launch that fills the GPU:
+// router logits on the tensor cores, per-token TopK and gate weights, and
+// the dispatch (histogram, scan, stable counting sort with the capacity
+// clip), for batches of up to kFusedMaxTiles tiles of 128 tokens.
+//
+// Follows "用Ascend C写一个MoE融合算子": section "1. Routing + Gating 合并"
+// (x × W_router, TopK per sample, Softmax over the top-k scores only) and
+// listing "Gather操作" of section "2. Dispatch + Expert + Combine 流水线"
+// (each expert's rows are its assignments in ascending (token, slot) order);
+// token dropping past the capacity from "CANN ops-transformer：MoE 路由算子的
+// 负载均衡策略", section "负载不均衡的根源".
+//
+// Design (sm_103a).  A batch of `tiles` tiles of 128 tokens runs as
+// tiles x S CTAs, one per SM, all resident at once (S = K splits per tile,
+// as many as fit):
+//   1. each CTA streams its K slice of the tile's x rows and of W_router by
+//      TMA (128-byte swizzle, a ring of up to 8 stages) into one tcgen05.mma
+//      accumulator, 128 tokens x E experts in TMEM;
+//   2. it writes that fp32 partial to the workspace (L2) and arrives on the
+//      tile's counter; rank s of the tile owns rows [128 s / S, 128 (s+1) / S)
+//      and, once all S partials are in, sums each owned row's S partials in
+//      rank order (deterministic) -- with S up to 12 each SM takes in about
+//      a twelfth of the tile's bytes, and no thread-block cluster is needed
+//      (clusters of 8 do not all fit on the GPU at once);
+//   3. TopK and the gate weights of the owned tokens by groups of 8 lanes
+//      (route_topk.cuh); the logits never reach HBM;
+//   4. the dispatch: each CTA ranks its own assignments within each expert
+//      (warp match, then a scan across warps), publishes its per-expert
+//      counts as bytes, and arrives on the grid's counter; once every CTA
+//      has arrived it reads all counts, takes the exclusive sum over the
+//      CTAs before it (its base, in token order) and the totals (capacity
+//      clip, exclusive scan = offsets), and writes slot / perm of its own
+//      assignments -- the serial scan's order, with no second kernel.
+// Every wait (TMA ring, MMA completion, the two counters) is bounded; on
+// expiry MOE_DEV_TIMEOUT is recorded and the CTA returns.
+#include "route_topk.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int FBM = 128;
+constexpr int FBK = 64;
+constexpr int FTHREADS = 256;
+constexpr int FWARPS = FTHREADS / 32;
+constexpr int FMAX_STAGES = 8;
+
+struct FCtrl {
+  uint64_t full[FMAX_STAGES];
+  uint64_t empty[FMAX_STAGES];
+  uint64_t done;
+  uint32_t tmem_base;
+  int abort_flag;
+  int go;
+};
+
+// Shared memory of the steps after the MMAs (overlays the TMA ring).
+struct FPost {
+  int ids[FBM * kMaxTopK];          // the group's choices, token-major; -1 past T
+  int lrank[FBM * kMaxTopK];        // rank within the expert inside this CTA
+  int wc[FWARPS][kMaxExperts];      // per-warp counts, then their exclusive scan
+  int run[kMaxExperts];             // this CTA's assignments per expert
+  int pre[kMaxExperts];             // assignments of the CTAs before this one
+  int tot[kMaxExperts];             // all assignments
+  int off[kMaxExperts + 1];         // expert offsets (capacity-clipped scan)
+  int red[2][FTHREADS * 16];        // per-thread partial sums of 16 experts
+};
+
+template <int NB64>
+struct FCfg {
+  static constexpr int A_BYTES = FBM * FBK * 2;  // 16 KB
+  static constexpr int B_CHUNK = FBK * 64 * 2;   // 8 KB
+  static constexpr int B_BYTES = NB64 * B_CHUNK;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (196608 / STAGE) < FMAX_STAGES ? (196608 / STAGE) : FMAX_STAGES;
+  static constexpr int PIPE = STAGES * STAGE;
+  static constexpr size_t SMEM = 1024 + (size_t)PIPE + sizeof(FCtrl);
+  static_assert(sizeof(FPost) <= (size_t)PIPE, "post-MMA state fits in the ring");
+};
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Thread 0 only: arrive on `cnt` (after the CTA's global writes, ordered by
+// the preceding __syncthreads and this fence) and wait until it reaches
+// `target`, at most limit_ns.  Returns false (and records the timeout) if it
+// did not.
+__device__ bool arrive_and_wait(unsigned* cnt, unsigned target, uint64_t limit_ns, int* status) {
+  __threadfence();
+  atomicAdd(cnt, 1u);
+  if (ld_acquire_gpu(cnt) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(cnt) >= target) return true;
+    if (global_timer_ns() - t0 > limit_ns) {
+      record_status(status, MOE_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ bool fwait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns, int* status) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) {
+      record_status(status, MOE_DEV_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+template <int NB64>
+__global__ void __launch_bounds__(FTHREADS, 1)
+    route_fused_kernel(const __grid_constant__ CUtensorMap tm_x,
+                       const __grid_constant__ CUtensorMap tm_w, const FusedRouteArgs a) {
+  using C = FCfg<NB64>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+  FPost& P = *reinterpret_cast<FPost*>(smem);  // after the MMAs
+  FCtrl& c = *reinterpret_cast<FCtrl*>(smem + C::PIPE);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int S = (int)gridDim.x;
+  const int s = (int)blockIdx.x;
+  const int tile = (int)blockIdx.y;
+  const int G = S * (int)gridDim.y;
+  const int grp = tile * S + s;  // this CTA's group of tokens, in token order
+  const int m0 = tile * FBM;
+  const int KB = (a.H + FBK - 1) / FBK;
+  const int kb0 = (int)(((long long)KB * s) / S);
+  const int kb1 = (int)(((long long)KB * (s + 1)) / S);
+  const int nkb = kb1 - kb0;
+  const int r0 = FBM * s / S;  // owned rows of the tile
+  const int R = FBM * (s + 1) / S - r0;
+  pdl_launch_dependents();
+
+  if (tid == 0) {
+    for (int i = 0; i < C::STAGES; ++i) {
+      mbar_init(&c.full[i], 1);
+      mbar_init(&c.empty[i], 1);
+    }
+    mbar_init(&c.done, 1);
+    c.abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&c.tmem_base, (uint32_t)a.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // shared memory and TMEM only so far; global memory may still belong to
+  // the predecessor grid
+  pdl_wait();
+  const uint32_t tmem = c.tmem_base;
+  const WaitCtl wc{&c.abort_flag, a.status, a.wait_limit_ns};
+
+  // ---- 1. partial logits [128 x npad] over this CTA's K slice
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_w);
+    int stage = 0;
+    uint32_t phase = 0;
+    int armed = 0;
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (!mbar_wait(&c.empty[stage], phase ^ 1u, wc)) break;
+      mbar_arrive_expect_tx(&c.full[stage], C::STAGE);
+      tma_load_2d(sA + stage * C::A_BYTES, &tm_x, &c.full[stage], kb * FBK, m0);
+#pragma unroll
+      for (int cb = 0; cb < NB64; ++cb)
+        tma_load_2d(sB + stage * C::B_BYTES + cb * C::B_CHUNK, &tm_w, &c.full[stage], cb * 64,
+                    kb * FBK);
+      ++armed;
+      if (++stage == C::STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    // the ring is reused below: every armed stage's bytes must have landed
+    for (int m = max(0, armed - C::STAGES); m < armed; ++m)
+      fwait_drain(&c.full[m % C::STAGES], (uint32_t)((m / C::STAGES) & 1), a.wait_limit_ns,
+                  a.status);
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t idesc = idesc_bf16_f32(FBM, a.npad, false, true);
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int i = 0; i < nkb; ++i) {
+      if (!mbar_wait(&c.full[stage], phase, wc)) break;
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(sA + stage * C::A_BYTES);
+      const uint32_t b0 = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+      for (int j = 0; j < FBK / 16; ++j) {
+        const uint64_t ad = sdesc_sw128(a0 + j * 32, 16, 1024);
+        const uint64_t bd = sdesc_sw128(b0 + j * 2048, C::B_CHUNK, 1024);
+        umma_bf16(tmem, ad, bd, idesc, (i | j) != 0 ? 1u : 0u);
+      }
+      umma_commit(&c.empty[stage]);
+      if (++stage == C::STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    umma_commit(&c.done);  // fires once every MMA issued above has completed
+  }
+  __syncwarp();
+  int ok = 1;
+  if (lane == 0) ok = fwait_drain(&c.done, 0, a.wait_limit_ns, a.status);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  tc_fence_after();
+  const bool have = ok && nkb > 0 && c.abort_flag == 0;
+
+  // ---- 2. the partial of all 128 rows to the workspace.  Warps w and w+4
+  // read TMEM lanes 32 (w % 4) .. +31 (their lane quadrant) and take
+  // alternate 16-column chunks, four loads in flight per wait.
+  {
+    const int q = warp & 3;
+    const int h = warp >> 2;
+    const int row = q * 32 + lane;
+    float* dst = a.part + ((size_t)grp * FBM + row) * a.npad;
+    const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16);
+    const int nch = a.npad / 16;
+    for (int c0 = h; c0 < nch; c0 += 8) {
+      uint32_t v[4][16];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (c0 + 2 * u < nch) tmem_ld_x16(tb + (uint32_t)((c0 + 2 * u) * 16), v[u]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (c0 + 2 * u < nch) {
+          float4* d4 = reinterpret_cast<float4*>(dst + (c0 + 2 * u) * 16);
+#pragma unroll
+          for (int g4 = 0; g4 < 4; ++g4) {
+            float4 f;
+            f.x = have ? __uint_as_float(v[u][4 * g4 + 0]) : 0.f;
+            f.y = have ? __uint_as_float(v[u][4 * g4 + 1]) : 0.f;
+            f.z = have ? __uint_as_float(v[u][4 * g4 + 2]) : 0.f;
+            f.w = have ? __uint_as_float(v[u][4 * g4 + 3]) : 0.f;
+            d4[g4] = f;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, (uint32_t)a.tmem_cols);
+  }
+  if (tid == 0)
+    c.go = arrive_and_wait(a.tile_cnt + tile, (unsigned)S, a.wait_limit_ns, a.status) ? 1 : 0;
+  __syncthreads();
+  if (!c.go) return;
+
+  // ---- 3. owned tokens: sum the S partials (ranks ascending, then + bias;
+  // NaN -> -inf), TopK and the gate weights; 8 lanes per token
+  {
+    constexpr int GS = kTopkGroup;
+    constexpr int NCH = 2 * NB64;  // chunks per lane when E = 64 * NB64
+    const int g = lane & (GS - 1);
+    const unsigned gmask = 0xffu << (lane & ~(GS - 1));
+    for (int li0 = 0; li0 < R; li0 += FTHREADS / GS) {
+      const int li = li0 + tid / GS;
+      if (li >= R) continue;  // uniform over the group
+      const int t = m0 + r0 + li;
+      if (t >= a.T) {
+        if (g < a.k) P.ids[li * a.k + g] = -1;
+        continue;
+      }
+      const float* prow = a.part + ((size_t)tile * S * FBM + r0 + li) * a.npad;
+      const size_t rank_stride = (size_t)FBM * a.npad;
+      float lv[NCH * 4];
+      uint32_t taken = 0;
+#pragma unroll
+      for (int cc = 0; cc < NCH; ++cc) {
+        const int e0 = (g + cc * GS) * 4;
+        if (e0 < a.E) {
+          float4 acc = __ldcg(reinterpret_cast<const float4*>(prow + e0));
+          for (int r = 1; r < S; ++r) {
+            const float4 p = __ldcg(reinterpret_cast<const float4*>(prow + r * rank_stride + e0));
+            acc.x += p.x;
+            acc.y += p.y;
+            acc.z += p.z;
+            acc.w += p.w;
+          }
+          const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (e0 + i < a.E) {
+              float v = v4[i];
+              if (a.bias) v += __ldg(a.bias + e0 + i);
+              lv[cc * 4 + i] = isnan(v) ? -INFINITY : v;
+            } else {  // past E (a zero-padded W_router column): never selected
+              lv[cc * 4 + i] = -INFINITY;
+              taken |= 1u << (cc * 4 + i);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) lv[cc * 4 + i] = -INFINITY;
+          taken |= 0xfu << (cc * 4);
+        }
+      }
+      int my_id;
+      float my_w;
+      topk_gate_group<NCH>(lv, taken, g, gmask, a.k, a.E, a.gating, my_id, my_w);
+      if (g < a.k) {
+        a.ids[(size_t)t * a.k + g] = my_id;
+        a.weights[(size_t)t * a.k + g] = my_w;
+        P.ids[li * a.k + g] = my_id;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- 4a. rank of each assignment within its expert inside this CTA, in
+  // (token, slot) order: warp match, then an exclusive scan across warps
+  const int E = a.E;
+  const int n = R * a.k;
+  for (int e = tid; e < E; e += FTHREADS) P.run[e] = 0;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int c0 = 0; c0 < n; c0 += FTHREADS) {
+    for (int idx = tid; idx < FWARPS * kMaxExperts; idx += FTHREADS) (&P.wc[0][0])[idx] = 0;
+    __syncthreads();
+    const int i = c0 + tid;
+    const int e = i < n ? P.ids[i] : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int below = __popc(peers & lt);
+    if (e >= 0 && below == 0) P.wc[warp][e] = __popc(peers);
+    __syncthreads();
+    for (int e2 = tid; e2 < E; e2 += FTHREADS) {
+      int run = P.run[e2];
+      for (int w = 0; w < FWARPS; ++w) {
+        const int v = P.wc[w][e2];
+        P.wc[w][e2] = run;
+        run += v;
+      }
+      P.run[e2] = run;
+    }
+    __syncthreads();
+    if (i < n) P.lrank[i] = e >= 0 ? P.wc[warp][e] + below : -1;
+    __syncthreads();
+  }
+
+  // ---- 4b. publish this CTA's counts (bytes: at most 128 tokens each)
+  const int EP = a.ep;  // E rounded up to 16
+  const int NC = EP / 16;
+  for (int cgi = tid; cgi < NC; cgi += FTHREADS) {
+    uint32_t w4[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint32_t word = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int e = cgi * 16 + q * 4 + b;
+        word |= (uint32_t)(e < E ? P.run[e] : 0) << (8 * b);
+      }
+      w4[q] = word;
+    }
+    *reinterpret_cast<uint4*>(a.grp_hist + (size_t)grp * EP + cgi * 16) =
+        make_uint4(w4[0], w4[1], w4[2], w4[3]);
+  }
+  __syncthreads();
+  if (tid == 0) c.go = arrive_and_wait(a.grid_cnt, (unsigned)G, a.wait_limit_ns, a.status) ? 1 : 0;
+  __syncthreads();
+  if (!c.go) return;
+
+  // ---- 4c. bases (CTAs before this one) and totals from every CTA's counts:
+  // thread t < NT sums the 16 experts of chunk t % NC over CTAs
+  // t / NC + j * (NT / NC), NT = the largest multiple of NC up to 256
+  const int NT = (FTHREADS / NC) * NC;
+  {
+    const int cgi = tid % NC;
+    int pre[16], tot[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pre[i] = tot[i] = 0;
+    for (int gg = tid / NC; tid < NT && gg < G; gg += FTHREADS / NC) {
+      const uint4 v = __ldcg(reinterpret_cast<const uint4*>(a.grp_hist + (size_t)gg * EP + cgi * 16));
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int b = (int)((w4[i >> 2] >> (8 * (i & 3))) & 0xffu);
+        tot[i] += b;
+        if (gg < grp) pre[i] += b;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      P.red[0][tid * 16 + i] = pre[i];
+      P.red[1][tid * 16 + i] = tot[i];
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += FTHREADS) {
+    const int cgi = e >> 4;
+    const int i = e & 15;
+    int p = 0, t2 = 0;
+    for (int th = cgi; th < NT; th += NC) {
+      p += P.red[0][th * 16 + i];
+      t2 += P.red[1][th * 16 + i];
+    }
+    P.pre[e] = p;
+    P.tot[e] = t2;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // kept counts (capacity clip) and their exclusive scan: lane l holds
+    // experts 8l .. 8l+7 (E <= 256)
+    int loc[8];
+    int sum = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = lane * 8 + u;
+      int k2 = 0;
+      if (e < E) {
+        k2 = P.tot[e];
+        if (a.capacity >= 0) k2 = min(k2, a.capacity);
+      }
+      loc[u] = k2;
+      sum += k2;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    int run = incl - sum;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = lane * 8 + u;
+      if (e < E) {
+        P.off[e] = run;
+        if (grp == 0) {
+          a.offsets[e] = run;
+          a.counts[e] = loc[u];
+        }
+      }
+      run += loc[u];
+    }
+    if (lane == 31) {
+      P.off[E] = incl;
+      if (grp == 0) a.offsets[E] = incl;
+    }
+  }
+  __syncthreads();
+
+  // ---- 4d. slot / perm of this CTA's assignments; the unused tail of perm
+  // split across the CTAs
+  for (int i = tid; i < n; i += FTHREADS) {
+    const int t = m0 + r0 + i / a.k;
+    if (t >= a.T) continue;
+    const int e = P.ids[i];
+    int sl = -1;
+    if (e >= 0) {
+      const int r = P.pre[e] + P.lrank[i];
+      if (a.capacity < 0 || r < a.capacity) {
+        sl = P.off[e] + r;
+        a.perm[sl] = t * a.k + i % a.k;
+      }
+    }
+    a.slot[(size_t)t * a.k + i % a.k] = sl;
+  }
+  const int Tk = a.T * a.k;
+  const int Nk = P.off[E];
+  const int per = (Tk - Nk + G - 1) / G;
+  const int lo = Nk + grp * per;
+  const int hi = min(Tk, lo + per);
+  for (int i = lo + tid; i < hi; i += FTHREADS) a.perm[i] = -1;
+}
+
+template <int NB64>
+cudaError_t launch_fused_nb(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
+                            const FusedRouteArgs& a, int splits, cudaStream_t st, bool pdl) {
+  using C = FCfg<NB64>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)splits, (unsigned)((a.T + FBM - 1) / FBM), 1);
+  cfg.blockDim = dim3(FTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (pdl) {
+    set_pdl_attr(attr[0]);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, route_fused_kernel<NB64>, tm_x, tm_w, a);
+}
+
+template <int NB64>
+cudaError_t fused_setup_nb(int* per_sm) {
+  cudaError_t e = cudaFuncSetAttribute(route_fused_kernel<NB64>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)FCfg<NB64>::SMEM);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, route_fused_kernel<NB64>, FTHREADS,
+                                                       FCfg<NB64>::SMEM);
+}
+
+int g_fused_per_sm[64][4];
+
+}  // namespace
+
+cudaError_t route_fused_set_attributes() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int n[4] = {0, 0, 0, 0};
+  if ((e = fused_setup_nb<1>(&n[0])) != cudaSuccess) return e;
+  if ((e = fused_setup_nb<2>(&n[1])) != cudaSuccess) return e;
+  if ((e = fused_setup_nb<3>(&n[2])) != cudaSuccess) return e;
+  if ((e = fused_setup_nb<4>(&n[3])) != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64)
+    for (int i = 0; i < 4; ++i) g_fused_per_sm[dev][i] = n[i];
+  return cudaSuccess;
+}
+
+int route_fused_resident_per_sm(int E) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  return g_fused_per_sm[dev][(E + 63) / 64 - 1];
+}
+
+cudaError_t launch_route_fused(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
+                               const FusedRouteArgs& a, int splits, cudaStream_t st, bool pdl) {
+  switch ((a.E + 63) / 64) {
+    case 1: return launch_fused_nb<1>(tm_x, tm_w, a, splits, st, pdl);
+    case 2: return launch_fused_nb<2>(tm_x, tm_w, a, splits, st, pdl);
+    case 3: return launch_fused_nb<3>(tm_x, tm_w, a, splits, st, pdl);
+    default: return launch_fused_nb<4>(tm_x, tm_w, a, splits, st, pdl);
+  }
+}
+
+}  // namespace moe

@@ -46,13 +46,35 @@ def test_version(lib):
     assert moe.moe_version() >> 16 == 1
 
 
+def _al(v, a=1024):
+    return -(-v // a) * a
+
+
+def fused_route_bytes(T, H, E):
+    """The fused route's workspace regions (T > 128 or E > 64, at most 128
+    tiles of 128 tokens): per-CTA counts [ctas, E16] bytes and fp32 partial
+    logits [ctas, 128, E16], ctas <= min(tiles * min(12, H / 64), 256)."""
+    tiles = -(-T // 128)
+    if (T <= 128 and E <= 64) or tiles > 128:
+        return 0
+    ctas = min(tiles * min(12, -(-H // 64)), 256)
+    e16 = -(-E // 16) * 16
+    return _al(ctas * e16) + _al(ctas * 128 * e16 * 4)
+
+
 def test_workspace_size_and_capacity_host_only(lib):
     s = moe.make_shape(4096, 4096, 14336, 8, 2)
-    # status block + per-128-token expert counts + h [T*k, F] + Y [T*k, H], bf16
-    assert moe.moe_workspace_size(s) == 1024 + 1024 + 8192 * 14336 * 2 + 8192 * 4096 * 2
-    assert moe.moe_route_workspace_size(s) == 1024 + 1024  # 32 tiles x 8 experts x 4 B
+    # status block + per-128-token expert counts + the fused route's regions
+    # + h [T*k, F] + Y [T*k, H], bf16
+    route = 1024 + 1024 + fused_route_bytes(4096, 4096, 8)
+    assert fused_route_bytes(4096, 4096, 8) == 4096 + 256 * 128 * 16 * 4
+    assert moe.moe_workspace_size(s) == route + 8192 * 14336 * 2 + 8192 * 4096 * 2
+    assert moe.moe_route_workspace_size(s) == route  # 32 tiles x 8 experts x 4 B of counts
     s3 = moe.make_shape(2048, 4096, 0, 128, 8)
-    assert moe.moe_route_workspace_size(s3) == 1024 + 16 * 128 * 4
+    assert moe.moe_route_workspace_size(s3) == 1024 + 16 * 128 * 4 + 192 * 128 + 192 * 128 * 128 * 4
+    # past 128 tiles the route is router + dispatch kernels: no fused regions
+    s4 = moe.make_shape(40000, 256, 0, 8, 2)
+    assert moe.moe_route_workspace_size(s4) == 1024 + _al(313 * 8 * 4)
     assert moe.moe_expert_capacity(moe.make_shape(8192, 2048, 1408, 64, 4, 1.2)) == 615
     assert moe.moe_expert_capacity(moe.make_shape(8192, 2048, 1408, 64, 4, None)) == -1
     assert moe.moe_expert_capacity(moe.make_shape(64, 128, 256, 8, 2, 1.0)) == 16
@@ -64,12 +86,14 @@ def test_any_expert_count_is_accepted_and_pads_w_router(lib):
     for E in (1, 2, 4, 6, 13, 250):
         k = min(E, 2)
         s = moe.make_shape(300, 4096, 256, E, k)
-        pad = -(-4096 * (-(-E // 8) * 8) * 2 // 1024) * 1024
-        hist = -(-(3 * E * 4) // 1024) * 1024
-        assert moe.moe_route_workspace_size(s) == 1024 + hist + pad
-        assert moe.moe_workspace_size(s) == 1024 + hist + pad + 300 * k * (256 + 4096) * 2
+        pad = _al(4096 * (-(-E // 8) * 8) * 2)
+        hist = _al(3 * E * 4)
+        route = 1024 + hist + pad + fused_route_bytes(300, 4096, E)
+        assert moe.moe_route_workspace_size(s) == route
+        assert moe.moe_workspace_size(s) == route + 300 * k * (256 + 4096) * 2
     s8 = moe.make_shape(300, 4096, 256, 16, 2)
-    assert moe.moe_route_workspace_size(s8) == 1024 + 1024  # no copy when E % 8 == 0
+    # no copy when E % 8 == 0
+    assert moe.moe_route_workspace_size(s8) == 1024 + 1024 + fused_route_bytes(300, 4096, 16)
 
 
 @pytest.mark.parametrize("T,k,E,cf", [(8192, 4, 64, 1.2), (64, 2, 8, 1.0), (10, 1, 8, 0.8),
@@ -152,14 +176,16 @@ def test_step_entry_points_validate_before_touching_the_device(lib):
 
 def test_forward_plan_is_a_host_only_shape_rule(lib):
     import moe_synth
+    # the route runs as one launch up to 128 tiles of 128 tokens (CUDA cores
+    # for T <= 128 with E <= 64, the fused tensor-core route otherwise)
     for cfg, want in [(moe_synth.DECODE, (True, False)), (moe_synth.TINY, (True, False)),
-                      (moe_synth.PREFILL, (False, False)), (moe_synth.PREFILL_K1, (False, True)),
-                      (moe_synth.SKEWED, (False, False))]:
+                      (moe_synth.PREFILL, (True, False)), (moe_synth.PREFILL_K1, (True, True)),
+                      (moe_synth.SKEWED, (True, False))]:
         s = moe.make_shape(cfg.T, cfg.H, cfg.F, cfg.E, cfg.k, cfg.capacity_factor)
         assert moe.moe_forward_plan(s) == want, cfg.name
     assert moe.moe_forward_plan(moe.make_shape(128, 64, 64, 64, 2)) == (True, False)
-    assert moe.moe_forward_plan(moe.make_shape(129, 64, 64, 64, 2)) == (False, False)
-    assert moe.moe_forward_plan(moe.make_shape(128, 64, 64, 72, 2)) == (False, False)
+    assert moe.moe_forward_plan(moe.make_shape(16384, 64, 64, 64, 2)) == (True, False)
+    assert moe.moe_forward_plan(moe.make_shape(16385, 64, 64, 72, 2)) == (False, False)
     c = ctypes.c_int32(0)
     good = moe.make_shape(64, 128, 256, 8, 2)
     assert lib.moe_forward_plan(ctypes.byref(good), None, ctypes.byref(c)) == moe.MOE_ERR_INVALID_ARG

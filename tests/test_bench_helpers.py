@@ -21,12 +21,14 @@ def _shape(cfg):
 
 def test_launched_kernels_follow_the_forward_plan():
     every = set(moe.KERNEL_NAMES)
-    # large batch, k = 2: all six steps are kernels of their own
-    assert set(bench.launched_kernels(_shape(moe_synth.PREFILL))) == every
-    # small batch: the router also dispatches
+    # up to 128 tiles of 128 tokens the route (router + dispatch) is one launch
+    assert set(bench.launched_kernels(_shape(moe_synth.PREFILL))) == every - {"dispatch"}
     assert set(bench.launched_kernels(_shape(moe_synth.DECODE))) == every - {"dispatch"}
+    # past that, all six steps are kernels of their own
+    assert set(bench.launched_kernels(_shape(moe_synth.PREFILL.with_(T=20000)))) == every
     # k = 1: the second GEMM also combines
-    assert set(bench.launched_kernels(_shape(moe_synth.PREFILL_K1))) == every - {"combine"}
+    assert set(bench.launched_kernels(_shape(moe_synth.PREFILL_K1))) == \
+        every - {"combine", "dispatch"}
     for name in every - set(bench.launched_kernels(_shape(moe_synth.DECODE))):
         assert name in bench.FUSED_INTO
 

@@ -171,11 +171,35 @@ def test_router_sweep_full_size(k):
     print(cfg.name, rep)
 
 
+@pytest.mark.parametrize("T,E,k,cf", [(16384, 128, 2, None), (16384, 8, 1, 0.7),
+                                      (3000, 200, 8, 0.3), (9000, 64, 4, None)])
+def test_route_in_one_launch_at_scale(T, E, k, cf):
+    # the fused route: 128 tiles (the most it takes: one K split each), E that
+    # fills an uneven number of count chunks (200 -> 13), drops, many tiles
+    cfg = moe_synth.MoEConfig("fused", T=T, H=512, F=0, E=E, k=k, seed=28, capacity_factor=cf)
+    assert moe.moe_forward_plan(moe.make_shape(T, cfg.H, 8, E, k, cf))[0]
+    inputs = moe_synth.make_inputs(cfg, with_ffn=False)
+    r = gpu_route(cfg, to_dev(inputs))
+    _, rep = routing_parity(cfg, inputs, r)
+    if cf is not None:
+        assert rep["dropped"] > 0
+
+
+def test_router_kernels_past_128_tiles_wide_experts():
+    # 133 tiles, E = 128: the cluster router + dispatch kernel path
+    cfg = moe_synth.MoEConfig("wide128", T=17000, H=256, F=0, E=128, k=4, seed=29)
+    assert not moe.moe_forward_plan(moe.make_shape(cfg.T, cfg.H, 8, cfg.E, cfg.k))[0]
+    inputs = moe_synth.make_inputs(cfg, with_ffn=False)
+    r = gpu_route(cfg, to_dev(inputs))
+    routing_parity(cfg, inputs, r)
+
+
 @pytest.mark.parametrize("cf", [None, 0.9])
 def test_router_more_tiles_than_one_wave(cf):
     # 313 tiles of 128 tokens: more router clusters than fit on the GPU at
     # once, and 313 segments for the scan of the per-tile counts
     cfg = moe_synth.MoEConfig("wide", T=40000, H=256, F=0, E=8, k=2, seed=27, capacity_factor=cf)
+    assert not moe.moe_forward_plan(moe.make_shape(cfg.T, cfg.H, 8, cfg.E, cfg.k, cf))[0]
     inputs = moe_synth.make_inputs(cfg, with_ffn=False)
     r = gpu_route(cfg, to_dev(inputs))
     _, rep = routing_parity(cfg, inputs, r)
