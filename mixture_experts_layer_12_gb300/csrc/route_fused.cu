@@ -219,6 +219,8 @@ __global__ void __launch_bounds__(FTHREADS, 1)
   int ok = 1;
   if (lane == 0) ok = fwait_drain(&c.done, 0, a.wait_limit_ns, a.status);
   ok = __shfl_sync(0xffffffffu, ok, 0);
+  // the ring that TMA (async proxy) filled is reused by plain stores below
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   tc_fence_after();
   const bool have = ok && nkb > 0 && c.abort_flag == 0;
 
