@@ -9,11 +9,18 @@ Recipe (the workloads' shapes and distributions):
   W1       ~ N(0, 1/H)        [E, H, F]    (gated experts: [E, H, 2F] = [gate | up])
   W2       ~ N(0, 1/F)        [E, F, H]
   bias     optional fp32 [E] (the skewed workload puts +4.0 on expert 0)
-Each value is drawn as fp32 from torch's CPU generator and rounded to bf16
-(round-to-nearest-even).  Every tensor, and every expert's slice of W1 and
-W2, has its own generator seeded from (seed, tensor id, expert), so one
-expert's weights can be regenerated alone and all slices can be drawn in
-parallel threads; the bits do not depend on the thread count or the device.
+Every tensor, and every expert's slice of W1 and W2, has its own stream:
+numpy's PCG64 bit generator seeded by SeedSequence((seed, tensor id,
+expert)).  Normal values come from the Box-Muller transform in float64 --
+pairs (u1, u2) of uniform doubles give sqrt(-2 ln(1 - u1)) cos(2 pi u2) and
+then the matching sines -- scaled by the std, rounded to fp32 and then to
+bf16 (round-to-nearest-even each time).  The bits are the same on any
+machine: the stream is integer arithmetic, and a one-ulp difference between
+two platforms' float64 log or cos changes a bf16 value with probability
+about 2^-44 per draw (a vectorised fp32 generator, as torch's randn, gives
+different bits on different CPU architectures).  One expert's weights can
+be regenerated alone and the slices are drawn in parallel threads; the bits
+do not depend on the thread count.
 """
 from __future__ import annotations
 
@@ -21,6 +28,7 @@ import math
 from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, replace
 
+import numpy as np
 import torch
 
 _TENSOR_ID = {"x": 1, "w_router": 2, "w1": 3, "w2": 4}
@@ -69,24 +77,52 @@ ALL = {c.name: c for c in [TINY, PREFILL, *ROUTER.values(), SKEWED, SKEWED_CF, D
                            PREFILL_SWIGLU, DECODE_SWIGLU, PREFILL_K1]}
 
 
-def _gen(seed: int, tensor: str, part: int = 0) -> torch.Generator:
-    s = ((seed * 1000003 + _TENSOR_ID[tensor]) * 1000003 + part) % (2**63 - 1)
-    return torch.Generator().manual_seed(s)
+_CHUNK = 1 << 22  # draws per Box-Muller block (bounds the float64 temporaries)
 
 
-def _normal_bf16(shape, std: float, gen: torch.Generator) -> torch.Tensor:
-    a = torch.randn(*shape, generator=gen, dtype=torch.float32)
-    if std != 1.0:
-        a.mul_(std)
-    return a.to(torch.bfloat16)
+def _stream(seed: int, tensor: str, part: int = 0) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence((seed, _TENSOR_ID[tensor],
+                                                                        part))))
+
+
+def _box_muller(rng: np.random.Generator, n: int) -> np.ndarray:
+    """n standard normal float64 values: for m = ceil(n / 2) uniform pairs
+    (u1, u2), r = sqrt(-2 ln(1 - u1)) (1 - u1 in (0, 1]), then r cos(2 pi u2)
+    for the m pairs followed by r sin(2 pi u2), truncated to n."""
+    m = (n + 1) // 2
+    u1 = rng.random(m)
+    u2 = rng.random(m)
+    np.subtract(1.0, u1, out=u1)
+    np.log(u1, out=u1)
+    u1 *= -2.0
+    np.sqrt(u1, out=u1)
+    u2 *= 2.0 * math.pi
+    z = np.empty(2 * m)
+    np.cos(u2, out=z[:m])
+    np.sin(u2, out=z[m:])
+    z[:m] *= u1
+    z[m:] *= u1
+    return z[:n]
+
+
+def _normal_bf16(shape, std: float, rng: np.random.Generator) -> torch.Tensor:
+    n = math.prod(shape)
+    out = np.empty(n, dtype=np.float32)
+    for i in range(0, n, _CHUNK):
+        k = min(_CHUNK, n - i)
+        z = _box_muller(rng, k)
+        if std != 1.0:
+            z *= std
+        out[i:i + k] = z  # float64 -> fp32, round to nearest even
+    return torch.from_numpy(out).reshape(shape).to(torch.bfloat16)
 
 
 def make_x(cfg: MoEConfig) -> torch.Tensor:
-    return _normal_bf16((cfg.T, cfg.H), 1.0, _gen(cfg.seed, "x"))
+    return _normal_bf16((cfg.T, cfg.H), 1.0, _stream(cfg.seed, "x"))
 
 
 def make_w_router(cfg: MoEConfig) -> torch.Tensor:
-    return _normal_bf16((cfg.H, cfg.E), 1.0 / math.sqrt(cfg.H), _gen(cfg.seed, "w_router"))
+    return _normal_bf16((cfg.H, cfg.E), 1.0 / math.sqrt(cfg.H), _stream(cfg.seed, "w_router"))
 
 
 def make_bias(cfg: MoEConfig) -> torch.Tensor | None:
@@ -102,11 +138,11 @@ def w1_cols(cfg: MoEConfig) -> int:
 
 
 def make_w1_expert(cfg: MoEConfig, e: int) -> torch.Tensor:
-    return _normal_bf16((cfg.H, w1_cols(cfg)), 1.0 / math.sqrt(cfg.H), _gen(cfg.seed, "w1", e))
+    return _normal_bf16((cfg.H, w1_cols(cfg)), 1.0 / math.sqrt(cfg.H), _stream(cfg.seed, "w1", e))
 
 
 def make_w2_expert(cfg: MoEConfig, e: int) -> torch.Tensor:
-    return _normal_bf16((cfg.F, cfg.H), 1.0 / math.sqrt(cfg.F), _gen(cfg.seed, "w2", e))
+    return _normal_bf16((cfg.F, cfg.H), 1.0 / math.sqrt(cfg.F), _stream(cfg.seed, "w2", e))
 
 
 def _stack_experts(cfg: MoEConfig, fn, shape, threads: int) -> torch.Tensor:

@@ -487,3 +487,17 @@ def test_stored_routing_stats_match_the_oracle():
         stored = json.load(f)["workloads"]
     for name in ("tiny", "decode"):
         assert mod.stats(moe_synth.ALL[name]) == stored[name]
+
+
+def test_seeded_inputs_are_the_same_bits_on_every_machine():
+    # tests/golden/synth_checksums.json: sha256 of seeded tensors' bf16 bits
+    # (make_synth_checksums.py); the generator is integer streams + float64
+    # Box-Muller, so x86-64 and aarch64 hosts draw identical inputs
+    import importlib.util
+    path = os.path.join(os.path.dirname(__file__), "golden", "make_synth_checksums.py")
+    spec = importlib.util.spec_from_file_location("make_synth_checksums", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    with open(os.path.join(os.path.dirname(__file__), "golden", "synth_checksums.json")) as f:
+        stored = json.load(f)
+    assert {n: mod.digest(fn()) for n, fn in mod.CASES.items()} == stored
