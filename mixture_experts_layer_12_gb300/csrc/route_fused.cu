@@ -53,7 +53,8 @@ struct FCtrl {
   int go;
 };
 
-// Shared memory of the steps after the MMAs (overlays the TMA ring).
+// Shared memory of the steps after the MMAs, behind the staged partial
+// logits [128][npad + 4] fp32 (both overlay the TMA ring).
 struct FPost {
   int ids[FBM * kMaxTopK];          // the group's choices, token-major; -1 past T
   int lrank[FBM * kMaxTopK];        // rank within the expert inside this CTA
@@ -62,7 +63,7 @@ struct FPost {
   int pre[kMaxExperts];             // assignments of the CTAs before this one
   int tot[kMaxExperts];             // all assignments
   int off[kMaxExperts + 1];         // expert offsets (capacity-clipped scan)
-  int red[2][FTHREADS * 16];        // per-thread partial sums of 16 experts
+  int red[2][FWARPS * 256];         // per-warp sums of the experts' counts
 };
 
 template <int NB64>
@@ -74,7 +75,10 @@ struct FCfg {
   static constexpr int STAGES = (196608 / STAGE) < FMAX_STAGES ? (196608 / STAGE) : FMAX_STAGES;
   static constexpr int PIPE = STAGES * STAGE;
   static constexpr size_t SMEM = 1024 + (size_t)PIPE + sizeof(FCtrl);
-  static_assert(sizeof(FPost) <= (size_t)PIPE, "post-MMA state fits in the ring");
+  // staged partial: 128 rows of npad + 4 floats (16-byte rows, banks spread)
+  static constexpr int STG_BYTES = FBM * (NB64 * 64 + 4) * 4;
+  static_assert(STG_BYTES % 16 == 0, "aligned post-MMA state");
+  static_assert(STG_BYTES + sizeof(FPost) <= (size_t)PIPE, "post-MMA state fits in the ring");
 };
 
 __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
@@ -125,7 +129,8 @@ __global__ void __launch_bounds__(FTHREADS, 1)
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + C::STAGES * C::A_BYTES;
-  FPost& P = *reinterpret_cast<FPost*>(smem);  // after the MMAs
+  float* stg = reinterpret_cast<float*>(smem);                // after the MMAs
+  FPost& P = *reinterpret_cast<FPost*>(smem + C::STG_BYTES);  // after the MMAs
   FCtrl& c = *reinterpret_cast<FCtrl*>(smem + C::PIPE);
 
   const int tid = threadIdx.x;
@@ -224,14 +229,17 @@ __global__ void __launch_bounds__(FTHREADS, 1)
   tc_fence_after();
   const bool have = ok && nkb > 0 && c.abort_flag == 0;
 
-  // ---- 2. the partial of all 128 rows to the workspace.  Warps w and w+4
-  // read TMEM lanes 32 (w % 4) .. +31 (their lane quadrant) and take
-  // alternate 16-column chunks, four loads in flight per wait.
+  // ---- 2. the partial of all 128 rows into shared memory (warps w and
+  // w+4 read TMEM lanes 32 (w % 4) .. +31, their lane quadrant, and take
+  // alternate 16-column chunks, four loads in flight per wait), then the
+  // rows the tile's other CTAs own to the workspace, coalesced; this CTA's
+  // own rows never leave the SM
+  const int sp = a.npad + 4;  // staging row pitch (floats)
+  const int v4 = a.npad / 4;  // float4 per row
   {
     const int q = warp & 3;
     const int h = warp >> 2;
     const int row = q * 32 + lane;
-    float* dst = a.part + ((size_t)grp * FBM + row) * a.npad;
     const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16);
     const int nch = a.npad / 16;
     for (int c0 = h; c0 < nch; c0 += 8) {
@@ -243,7 +251,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         if (c0 + 2 * u < nch) {
-          float4* d4 = reinterpret_cast<float4*>(dst + (c0 + 2 * u) * 16);
+          float4* d4 = reinterpret_cast<float4*>(stg + row * sp + (c0 + 2 * u) * 16);
 #pragma unroll
           for (int g4 = 0; g4 < 4; ++g4) {
             float4 f;
@@ -263,13 +271,66 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, (uint32_t)a.tmem_cols);
   }
+  {
+    float* dst = a.part + (size_t)grp * FBM * a.npad;
+    for (int idx = tid; idx < (FBM - R) * v4; idx += FTHREADS) {
+      const int ro = idx / v4;
+      const int row = ro < r0 ? ro : ro + R;  // skip the owned rows
+      const int col = (idx - ro * v4) * 4;
+      *reinterpret_cast<float4*>(dst + (size_t)row * a.npad + col) =
+          *reinterpret_cast<const float4*>(stg + row * sp + col);
+    }
+  }
+  __syncthreads();
   if (tid == 0)
     c.go = arrive_and_wait(a.tile_cnt + tile, (unsigned)S, a.wait_limit_ns, a.status) ? 1 : 0;
   __syncthreads();
   if (!c.go) return;
 
-  // ---- 3. owned tokens: sum the S partials (ranks ascending, then + bias;
-  // NaN -> -inf), TopK and the gate weights; 8 lanes per token
+  // ---- 3a. owned rows: the S partials summed in rank order (all loads of
+  // an element issued before the sums), + bias, NaN -> -inf, columns past E
+  // at -inf; written over the staged row
+  {
+    const float* pt = a.part + (size_t)tile * S * FBM * a.npad;  // rank 0's partial of the tile
+    const size_t rstride = (size_t)FBM * a.npad;
+    for (int idx = tid; idx < R * v4; idx += FTHREADS) {
+      const int li = idx / v4;
+      const int col = (idx - li * v4) * 4;
+      const int row = r0 + li;
+      float4 p[kFusedMaxSplits];
+#pragma unroll
+      for (int r = 0; r < kFusedMaxSplits; ++r)
+        if (r < S && r != s)
+          p[r] = __ldcg(reinterpret_cast<const float4*>(pt + r * rstride + (size_t)row * a.npad + col));
+      float4* mine = reinterpret_cast<float4*>(stg + row * sp + col);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < kFusedMaxSplits; ++r) {
+        if (r < S) {
+          const float4 v = r == s ? *mine : p[r];
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+      }
+      float o[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (col + i < a.E) {
+          float vv = o[i];
+          if (a.bias) vv += __ldg(a.bias + col + i);
+          o[i] = isnan(vv) ? -INFINITY : vv;
+        } else {
+          o[i] = -INFINITY;
+        }
+      }
+      *mine = make_float4(o[0], o[1], o[2], o[3]);
+    }
+  }
+  __syncthreads();
+
+  // ---- 3b. TopK and the gate weights of the owned tokens, 8 lanes per token
   {
     constexpr int GS = kTopkGroup;
     constexpr int NCH = 2 * NB64;  // chunks per lane when E = 64 * NB64
@@ -283,34 +344,21 @@ __global__ void __launch_bounds__(FTHREADS, 1)
         if (g < a.k) P.ids[li * a.k + g] = -1;
         continue;
       }
-      const float* prow = a.part + ((size_t)tile * S * FBM + r0 + li) * a.npad;
-      const size_t rank_stride = (size_t)FBM * a.npad;
+      const float* lrow = stg + (r0 + li) * sp;
       float lv[NCH * 4];
       uint32_t taken = 0;
 #pragma unroll
       for (int cc = 0; cc < NCH; ++cc) {
         const int e0 = (g + cc * GS) * 4;
-        if (e0 < a.E) {
-          float4 acc = __ldcg(reinterpret_cast<const float4*>(prow + e0));
-          for (int r = 1; r < S; ++r) {
-            const float4 p = __ldcg(reinterpret_cast<const float4*>(prow + r * rank_stride + e0));
-            acc.x += p.x;
-            acc.y += p.y;
-            acc.z += p.z;
-            acc.w += p.w;
-          }
-          const float v4[4] = {acc.x, acc.y, acc.z, acc.w};
+        if (e0 < a.npad) {
+          const float4 v = *reinterpret_cast<const float4*>(lrow + e0);
+          lv[cc * 4 + 0] = v.x;
+          lv[cc * 4 + 1] = v.y;
+          lv[cc * 4 + 2] = v.z;
+          lv[cc * 4 + 3] = v.w;
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if (e0 + i < a.E) {
-              float v = v4[i];
-              if (a.bias) v += __ldg(a.bias + e0 + i);
-              lv[cc * 4 + i] = isnan(v) ? -INFINITY : v;
-            } else {  // past E (a zero-padded W_router column): never selected
-              lv[cc * 4 + i] = -INFINITY;
-              taken |= 1u << (cc * 4 + i);
-            }
-          }
+          for (int i = 0; i < 4; ++i)
+            if (e0 + i >= a.E) taken |= 1u << (cc * 4 + i);  // past E: never selected
         } else {
 #pragma unroll
           for (int i = 0; i < 4; ++i) lv[cc * 4 + i] = -INFINITY;
@@ -381,39 +429,64 @@ __global__ void __launch_bounds__(FTHREADS, 1)
   __syncthreads();
   if (!c.go) return;
 
-  // ---- 4c. bases (CTAs before this one) and totals from every CTA's counts:
-  // thread t < NT sums the 16 experts of chunk t % NC over CTAs
-  // t / NC + j * (NT / NC), NT = the largest multiple of NC up to 256
-  const int NT = (FTHREADS / NC) * NC;
+  // ---- 4c. bases (CTAs before this one) and totals from every CTA's counts.
+  // Chunks of 16 experts, NCP = NC rounded up to a power of two (<= 16):
+  // thread t takes chunk t % NCP (idle past NC) of CTAs t / NCP + j (256 /
+  // NCP) -- at most NCP <= 16 loads, all issued before the sums -- then a
+  // butterfly over the lanes of its warp that hold the same chunk, and one
+  // sum over the 8 warps.
   {
-    const int cgi = tid % NC;
+    constexpr int MAXL = 16;
+    int NCP = 1;
+    while (NCP < NC) NCP <<= 1;
+    const int cgi = tid & (NCP - 1);
+    const int gstep = FTHREADS / NCP;
+    uint4 hv[MAXL];
+#pragma unroll
+    for (int j = 0; j < MAXL; ++j) {
+      const int gg = tid / NCP + j * gstep;
+      if (cgi < NC && gg < G)
+        hv[j] = __ldcg(reinterpret_cast<const uint4*>(a.grp_hist + (size_t)gg * EP + cgi * 16));
+    }
     int pre[16], tot[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) pre[i] = tot[i] = 0;
-    for (int gg = tid / NC; tid < NT && gg < G; gg += FTHREADS / NC) {
-      const uint4 v = __ldcg(reinterpret_cast<const uint4*>(a.grp_hist + (size_t)gg * EP + cgi * 16));
-      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int b = (int)((w4[i >> 2] >> (8 * (i & 3))) & 0xffu);
-        tot[i] += b;
-        if (gg < grp) pre[i] += b;
+    for (int j = 0; j < MAXL; ++j) {
+      const int gg = tid / NCP + j * gstep;
+      if (cgi < NC && gg < G) {
+        const uint32_t w4[4] = {hv[j].x, hv[j].y, hv[j].z, hv[j].w};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int b = (int)((w4[i >> 2] >> (8 * (i & 3))) & 0xffu);
+          tot[i] += b;
+          if (gg < grp) pre[i] += b;
+        }
       }
     }
+    // lanes l and l ^ off hold the same chunk for off >= NCP (NCP | 32)
+    for (int off = 16; off >= NCP; off >>= 1) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      P.red[0][tid * 16 + i] = pre[i];
-      P.red[1][tid * 16 + i] = tot[i];
+      for (int i = 0; i < 16; ++i) {
+        pre[i] += __shfl_xor_sync(0xffffffffu, pre[i], off);
+        tot[i] += __shfl_xor_sync(0xffffffffu, tot[i], off);
+      }
+    }
+    if (lane < NCP && lane < NC) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        P.red[0][warp * 256 + lane * 16 + i] = pre[i];
+        P.red[1][warp * 256 + lane * 16 + i] = tot[i];
+      }
     }
   }
   __syncthreads();
   for (int e = tid; e < E; e += FTHREADS) {
-    const int cgi = e >> 4;
-    const int i = e & 15;
     int p = 0, t2 = 0;
-    for (int th = cgi; th < NT; th += NC) {
-      p += P.red[0][th * 16 + i];
-      t2 += P.red[1][th * 16 + i];
+#pragma unroll
+    for (int w = 0; w < FWARPS; ++w) {
+      p += P.red[0][w * 256 + e];
+      t2 += P.red[1][w * 256 + e];
     }
     P.pre[e] = p;
     P.tot[e] = t2;
