@@ -21,8 +21,7 @@
 //     so pairs working at the same time share the expert's weight columns
 //     through L2 (the pages' expert-block / token-block tiling, made ragged:
 //     an expert owns ceil(n_e / 256) row blocks); the tile list is built on
-//     the device from `offsets`, with no host synchronisation, and dealt out
-//     in waves of one tile per pair, cost-balanced within each wave.  An expert's
+//     the device from `offsets`, with no host synchronisation.  An expert's
 //     last row block with at most 128 rows runs as an M = 128 MMA (64 rows
 //     per CTA), a column block with at most 128 valid columns as N = 128,
 //     so short blocks do not pay for padding.
@@ -84,14 +83,6 @@ static_assert(BN_CTA % 64 == 0 && BN <= 256, "UMMA N");
 static_assert(TMEM_COLS <= 512, "TMEM capacity");
 static_assert(EPI_WARPS == 4, "one warp per TMEM lane quadrant (warp % 4), all 256 columns");
 
-// Wave-balanced tile schedule (see balance_schedule): up to kMaxWaves tiles
-// per pair for up to kMaxBalancePairs pairs; otherwise round-robin.
-constexpr int kMaxWaves = 256;
-constexpr int kMaxBalancePairs = 96;
-constexpr int kCostFull = 3;  // relative cost of a 256 x 256 pair tile ...
-constexpr int kCostHalf = 2;  // ... and of an M = 128 or N = 128 one (half the MMAs, the
-                              // full weight tile: more than half the time)
-
 struct Ctrl {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
@@ -101,9 +92,6 @@ struct Ctrl {
   uint32_t tmem_base;
   int abort_flag;
   int n_tiles;
-  int n_mine;                   // this pair's tiles (balanced schedule), -1: round-robin
-  int mine[kMaxWaves];          // this pair's tiles, in order
-  int r2t[kMaxBalancePairs];    // scratch: the wave's tile of each rank (bit 30: cheap)
   int tile_start[kMaxExperts + 1];
   int mblocks[kMaxExperts];
   int row_off[kMaxExperts];
@@ -120,6 +108,8 @@ struct Tile {
   bool nhalf;      // N = 128 tile (256 rows): 64 B columns per CTA
 };
 
+// Tiles of one pair increase monotonically, so the expert cursor only moves
+// forward; experts without rows own no tiles and are skipped.
 // Tiles of one pair increase monotonically, so the expert cursor only moves
 // forward; experts without rows own no tiles and are skipped.  Within an
 // expert the row blocks run fastest, so a weight tile's readers follow one
@@ -146,102 +136,6 @@ __device__ __forceinline__ Tile decode_tile(const Ctrl& c, int tile, int& e, int
   t.row0 = c.row_off[e] + base + rank * per;
   t.rows_valid = min(per, c.rows[e] - base - rank * per);
   return t;
-}
-
-// The pair tiles of the list, in expert-major, row-block-fastest order, are
-// dealt out in waves of n_pairs consecutive tiles -- the tiles that run at
-// the same time, whose pairs share each weight tile through L2 -- and
-// within a wave the costlier tiles go to the pairs with the least work so
-// far (ties: lower pair index), the cheap M = 128 / N = 128 tiles to the
-// pairs furthest ahead.  A greedy list schedule per wave: every CTA
-// replays it in warp 0 (one lane per pair, 3 pairs per lane) and keeps its
-// own pair's tiles.  Plain round-robin (tile = pair + i * n_pairs) gives
-// every pair the same number of tiles but not the same work: on a skewed
-// dispatch the pairs that draw more full tiles set the kernel's time.
-__device__ void balance_schedule(Ctrl& c, int n_tiles, int n_pairs, int pair, int rank,
-                                 bool allow_half, int n_cols) {
-  const int lane = threadIdx.x & 31;
-  const unsigned lt = (1u << lane) - 1u;
-  int load[3] = {0, 0, 0};
-  int ecur[3] = {0, 0, 0};
-  int mine = 0;
-  for (int w0 = 0; w0 < n_tiles; w0 += n_pairs) {
-    const int nw = min(n_pairs, n_tiles - w0);
-    // the wave's tiles: slot j of this lane is tile w0 + lane + 32 j; rank
-    // them full tiles first, each group in tile order
-    bool tv[3], th[3];
-    unsigned fm[3], hm[3];
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      const int li = lane + 32 * j;
-      tv[j] = li < nw;
-      th[j] = false;
-      if (tv[j]) {
-        const Tile t = decode_tile(c, w0 + li, ecur[j], rank, allow_half, n_cols);
-        th[j] = t.half || t.nhalf;
-      }
-      fm[j] = __ballot_sync(0xffffffffu, tv[j] && !th[j]);
-      hm[j] = __ballot_sync(0xffffffffu, th[j]);
-    }
-    const int nfull = __popc(fm[0]) + __popc(fm[1]) + __popc(fm[2]);
-    int fb = 0, hb = 0;
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      if (tv[j]) {
-        const int r = th[j] ? nfull + hb + __popc(hm[j] & lt) : fb + __popc(fm[j] & lt);
-        c.r2t[r] = (w0 + lane + 32 * j) | (th[j] ? (1 << 30) : 0);
-      }
-      fb += __popc(fm[j]);
-      hb += __popc(hm[j]);
-    }
-    __syncwarp();
-    // the pairs ranked by (work so far, pair index): work lies within
-    // [lo, lo + 3] under this schedule (levels past 3 merge: still a total
-    // order); rank r takes the tile of rank r
-    bool pv[3];
-    int lo = 0x7fffffff;
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      pv[j] = lane + 32 * j < n_pairs;
-      if (pv[j]) lo = min(lo, load[j]);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, off));
-    unsigned bm[4][3];
-    int below[4];
-    int run = 0;
-#pragma unroll
-    for (int d = 0; d < 4; ++d) {
-#pragma unroll
-      for (int j = 0; j < 3; ++j) bm[d][j] = __ballot_sync(0xffffffffu, pv[j] && min(load[j] - lo, 3) == d);
-      below[d] = run;
-      run += __popc(bm[d][0]) + __popc(bm[d][1]) + __popc(bm[d][2]);
-    }
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      if (!pv[j]) continue;
-      const int d = min(load[j] - lo, 3);
-      int r = below[d] + __popc(bm[d][j] & lt);
-#pragma unroll
-      for (int jj = 0; jj < j; ++jj) r += __popc(bm[d][jj]);
-      if (r < nw) {
-        const int v = c.r2t[r];
-        load[j] += (v >> 30) ? kCostHalf : kCostFull;
-        if (lane + 32 * j == pair) c.mine[mine++] = v & ((1 << 30) - 1);
-      }
-    }
-    __syncwarp();
-  }
-  mine = __shfl_sync(0xffffffffu, mine, pair & 31);
-  if (lane == 0) c.n_mine = mine;
-}
-
-// Tile i of this pair's sequence.
-__device__ __forceinline__ int pair_tile(const Ctrl& c, int i, int pair, int n_pairs) {
-  return c.n_mine >= 0 ? c.mine[i] : pair + i * n_pairs;
-}
-__device__ __forceinline__ int pair_tile_count(const Ctrl& c, int pair, int n_pairs, int n_tiles) {
-  return c.n_mine >= 0 ? c.n_mine : (pair < n_tiles ? (n_tiles - pair + n_pairs - 1) / n_pairs : 0);
 }
 
 // Wait that ignores the abort flag (used to drain in-flight copies and
@@ -347,12 +241,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       c.tile_start[p.E] = incl;
       c.n_tiles = incl;
     }
-    incl = __shfl_sync(0xffffffffu, incl, 31);
-    __syncwarp();
-    if (n_pairs >= 2 && n_pairs <= kMaxBalancePairs && incl <= kMaxWaves * n_pairs)
-      balance_schedule(c, incl, n_pairs, pair, rank, HALF, p.N);
-    else if (lane == 0)
-      c.n_mine = -1;
   } else if (threadIdx.x == 32) {
     // Only the leader's `full`, `tempty` and `drain` are used.  full: one
     // expect-tx arrival per CTA; tempty: every epilogue warp of both CTAs.
@@ -402,9 +290,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int issued = 0;  // k-blocks issued (all tiles)
       int e = 0;
       bool ok = true;
-      const int my_count = pair_tile_count(c, pair, n_pairs, n_tiles);
-      for (int i = 0; i < my_count && ok; ++i) {
-        const int tile = pair_tile(c, i, pair, n_pairs);
+      for (int tile = pair; tile < n_tiles && ok; tile += n_pairs) {
         const Tile t = decode_tile(c, tile, e, rank, HALF, p.N);
         // B columns of this CTA: its half of the 256-wide tile, or for
         // SwiGLU the gate (rank 0) / up (rank 1) columns of the same 128
@@ -466,9 +352,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       int e = 0;
-      const int my_count = pair_tile_count(c, pair, n_pairs, n_tiles);
-      for (int i = 0; i < my_count && ok; ++i) {
-        const int tile = pair_tile(c, i, pair, n_pairs);
+      for (int tile = pair; tile < n_tiles && ok; tile += n_pairs) {
         const Tile tt = decode_tile(c, tile, e, rank, HALF, p.N);
         const uint32_t idesc = tt.half ? IDESC_HALF : tt.nhalf ? IDESC_NHALF : IDESC;
         if (!mbar_wait(&c.tempty[acc], acc_phase ^ 1u, wc)) break;
@@ -515,9 +399,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int e = 0;
-    const int my_count = pair_tile_count(c, pair, n_pairs, n_tiles);
-    for (int i = 0; i < my_count; ++i) {
-      const int tile = pair_tile(c, i, pair, n_pairs);
+    for (int tile = pair; tile < n_tiles; tile += n_pairs) {
       const Tile t = decode_tile(c, tile, e, rank, HALF, p.N);
       int got = 1;
       if (lane == 0) got = mbar_wait(&c.tfull[acc], acc_phase, wc);
