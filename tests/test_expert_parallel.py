@@ -27,7 +27,8 @@ def test_send_splits_follow_expert_major_dispatch_order():
     assert send_splits(offsets, 4) == [3, 9, 1, 8]
     assert send_splits(offsets, 1) == [21]
     rc = torch.tensor([[2, 0, 5], [1, 4, 0]])  # [sources, local experts]
-    assert segment_offsets(rc) == [0, 2, 2, 7, 8, 12, 12]
+    so = segment_offsets(rc)
+    assert so.dtype == torch.int32 and so.tolist() == [0, 2, 2, 7, 8, 12, 12]
 
 
 class OracleOps:
@@ -52,13 +53,20 @@ class OracleOps:
         xp[:kept] = x[r.perm[:kept].long() // self.k]
         return xp
 
-    def expert_ffn(self, rows, seg_offsets):
+    def max_rows_to_one_rank(self, T):
+        import oracle
+        c = oracle.capacity(T, self.k, self.E, self.cf)
+        return T * self.k if c < 0 else min(T * self.k, self.El * c)
+
+    def expert_ffn(self, rows, seg_offsets, n_segments):
         import oracle
         f = oracle.expert_swiglu if self.act == "swiglu" else oracle.expert_ffn
-        Y = torch.zeros(rows.shape[0], self.H, dtype=torch.float64)
-        for i in range(len(seg_offsets) - 1):
+        so = seg_offsets.tolist()
+        assert len(so) == n_segments + 1
+        Y = torch.full((rows.shape[0], self.H), float("nan"), dtype=torch.float64)
+        for i in range(n_segments):
             e = i % self.El
-            for rr in range(seg_offsets[i], seg_offsets[i + 1]):
+            for rr in range(so[i], so[i + 1]):
                 Y[rr] = torch.from_numpy(f(rows[rr], self.w1[e], self.w2[e]))
         return Y
 
@@ -72,7 +80,7 @@ class OracleOps:
         return y
 
 
-def _worker(rank, world, port, out_dir, cfg_kw):
+def _worker(rank, world, port, out_dir, cfg_kw, padded):
     sys.path.insert(0, ROOT)
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
@@ -87,12 +95,13 @@ def _worker(rank, world, port, out_dir, cfg_kw):
     sl = slice(rank * El, (rank + 1) * El)
     ops = OracleOps(full["w_router"], full["w1"][sl], full["w2"][sl], cfg.k, cfg.E, full["bias"],
                     cfg.capacity_factor, cfg.act)
-    layer = ExpertParallelMoE(ops, rank, world, TorchExchange())
+    layer = ExpertParallelMoE(ops, rank, world, TorchExchange(), padded=padded)
     y = layer.forward(x)
     ref = oracle.moe_forward(x, full["w_router"], full["w1"], full["w2"], cfg.k, bias=full["bias"],
                              capacity_factor=cfg.capacity_factor, act=cfg.act)
     routed = layer.send(x)
-    torch.save(dict(y=y, ref=torch.from_numpy(np.asarray(ref["y"])), sent=routed.send_split,
+    torch.save(dict(y=y, ref=torch.from_numpy(np.asarray(ref["y"])),
+                    sent=routed.send_counts.sum(dim=1).tolist(),
                     dropped=int((routed.slot < 0).sum())),
                os.path.join(out_dir, f"rank{rank}.pt"))
     dist.barrier()
@@ -104,11 +113,14 @@ def _worker(rank, world, port, out_dir, cfg_kw):
     dict(T=40, H=16, F=24, E=8, k=3, seed=71, capacity_factor=0.6, bias0=2.0),  # drops, skew
     dict(T=32, H=16, F=8, E=4, k=1, seed=72, act="swiglu"),
 ], ids=["k2", "k3_drops", "k1_swiglu"])
-def test_two_rank_expert_parallel_matches_whole_layer(tmp_path, cfg_kw):
+@pytest.mark.parametrize("padded", [False, True], ids=["exact", "padded"])
+def test_two_rank_expert_parallel_matches_whole_layer(tmp_path, cfg_kw, padded):
+    # exact: row all-to-alls of exactly the rows (split sizes read once);
+    # padded: equal-split blocks, every index step on the device
     world = 2
-    port = 29600 + (os.getpid() % 1500)
-    mp.start_processes(_worker, args=(world, port, str(tmp_path), cfg_kw), nprocs=world, join=True,
-                       start_method="spawn")
+    port = 29600 + (os.getpid() % 1500) + (7 if padded else 0)
+    mp.start_processes(_worker, args=(world, port, str(tmp_path), cfg_kw, padded), nprocs=world,
+                       join=True, start_method="spawn")
     for r in range(world):
         res = torch.load(tmp_path / f"rank{r}.pt")
         np.testing.assert_allclose(res["y"].numpy(), res["ref"].numpy(), rtol=1e-10, atol=1e-12)

@@ -543,34 +543,46 @@ def test_forward_k1_prefill_sampled():
 
 # ------------------------------------------- expert parallelism (simulated) --
 
-def _exchange_locally(layers, routed):
+def _exchange_locally(layers, routed, padded):
     """The two all-to-alls of an expert-parallel step for G ranks held in
     one process: slices of the senders' rows, concatenated per receiver."""
     G = len(layers)
-    starts = [np.concatenate([[0], np.cumsum(r.send_split)]).tolist() for r in routed]
-    Ys = []
+    backs = [None] * G
+    if padded:
+        cap = routed[0].rows.shape[0] // G
+        outs = []
+        for d in range(G):
+            recv = torch.cat([routed[s].rows[d * cap:(d + 1) * cap] for s in range(G)])
+            counts = torch.stack([routed[s].send_counts[d] for s in range(G)])
+            outs.append(layers[d].compute(recv, counts).clone())
+        for s in range(G):
+            backs[s] = torch.cat([outs[d][s * cap:(s + 1) * cap] for d in range(G)])
+        return backs
+    splits = [r.send_counts.sum(dim=1).tolist() for r in routed]   # splits[s][d]
+    starts = [np.concatenate([[0], np.cumsum(sp)]).tolist() for sp in splits]
+    outs = []
     for d in range(G):
         counts = torch.stack([routed[s].send_counts[d] for s in range(G)])
         rows = torch.cat([routed[s].rows[starts[s][d]:starts[s][d + 1]] for s in range(G)])
-        Ys.append((layers[d].compute(rows, counts), counts.sum(dim=1).tolist()))
-    backs = []
+        outs.append((layers[d].compute(rows, counts).clone(), [splits[s][d] for s in range(G)]))
     for s in range(G):
         parts = []
         for d in range(G):
-            Y, recv = Ys[d]
+            Y, recv = outs[d]
             off = int(sum(recv[:s]))
             parts.append(Y[off:off + recv[s]])
-        backs.append(torch.cat(parts))
+        backs[s] = torch.cat(parts)
     return backs
 
 
+@pytest.mark.parametrize("padded", [False, True], ids=["exact", "padded"])
 @pytest.mark.parametrize("G,T,H,F,E,k,cf,bias,act", [
     (2, 512, 256, 512, 8, 2, None, None, "gelu"),
     (4, 700, 256, 384, 8, 4, 0.8, 2.0, "gelu"),      # drops, skew, ragged
     (2, 300, 128, 256, 16, 2, None, None, "swiglu"),
     (2, 256, 128, 256, 8, 1, 0.7, 1.0, "gelu"),      # k = 1 (the whole layer fuses its combine)
 ])
-def test_expert_parallel_ranks_match_whole_layer(G, T, H, F, E, k, cf, bias, act):
+def test_expert_parallel_ranks_match_whole_layer(G, T, H, F, E, k, cf, bias, act, padded):
     from mixture_experts_layer_12_gb300.expert_parallel import CudaOps, ExpertParallelMoE
     cfg = moe_synth.MoEConfig("ep", T=T, H=H, F=F, E=E, k=k, seed=80, capacity_factor=cf,
                               bias0=bias, act=act)
@@ -580,14 +592,15 @@ def test_expert_parallel_ranks_match_whole_layer(G, T, H, F, E, k, cf, bias, act
     El = E // G
     layers = [ExpertParallelMoE(CudaOps(full["w_router"], full["w1"][r * El:(r + 1) * El],
                                         full["w2"][r * El:(r + 1) * El], k, E, bias=full["bias"],
-                                        capacity_factor=cf, act=act), r, G) for r in range(G)]
+                                        capacity_factor=cf, act=act), r, G, padded=padded)
+              for r in range(G)]
     routed = [layers[r].send(xs[r]) for r in range(G)]
-    backs = _exchange_locally(layers, routed)
+    backs = _exchange_locally(layers, routed, padded)
     whole = moe.MoELayer(full["w_router"], full["w1"], full["w2"], k, bias=full["bias"],
                          capacity_factor=cf, act=act)
     full_cpu = moe_synth.make_inputs(cfg)
     for r in range(G):
-        y = layers[r].finish(routed[r], backs[r])
+        y = layers[r].finish(routed[r], backs[r]).clone()
         # against the oracle: each rank's routing and dispatch over its own
         # tokens, and its y from the oracle's combine on those decisions
         inputs_r = dict(full_cpu, x=xs[r].cpu())
@@ -602,6 +615,43 @@ def test_expert_parallel_ranks_match_whole_layer(G, T, H, F, E, k, cf, bias, act
             assert torch.equal(y, y_ref), f"rank {r}"
         else:  # the whole layer rounds w * acc once; here Y is rounded first
             check_y(y.float().cpu().numpy(), y_ref.double().cpu().numpy())
+
+
+def test_expert_parallel_padded_phases_need_no_host_sync():
+    # the padded mode's local phases -- routing and send blocks, expert FFN of
+    # the received blocks, return to dispatch order and combine -- captured
+    # in CUDA graphs (a device-to-host read would fail the capture) and
+    # replayed: the replay reproduces the eager result
+    from mixture_experts_layer_12_gb300.expert_parallel import CudaOps, ExpertParallelMoE
+    G, cfg = 2, moe_synth.MoEConfig("epg", T=64, H=256, F=512, E=8, k=2, seed=81)
+    full = to_dev(moe_synth.make_inputs(cfg))
+    xs = [to_dev(moe_synth.make_inputs(cfg.with_(seed=95 + r), with_ffn=False))["x"]
+          for r in range(G)]
+    El = cfg.E // G
+    layers = [ExpertParallelMoE(CudaOps(full["w_router"], full["w1"][r * El:(r + 1) * El],
+                                        full["w2"][r * El:(r + 1) * El], cfg.k, cfg.E), r, G,
+                                padded=True) for r in range(G)]
+    routed = [layers[r].send(xs[r]) for r in range(G)]  # eager warm-up allocates the buffers
+    backs = _exchange_locally(layers, routed, True)
+    y_eager = [layers[r].finish(routed[r], backs[r]).clone() for r in range(G)]
+    st = torch.cuda.Stream()
+    gs = [torch.cuda.CUDAGraph() for _ in range(3)]
+    with torch.cuda.graph(gs[0], stream=st):
+        routed = [layers[r].send(xs[r]) for r in range(G)]
+        recv = [torch.cat([routed[s].rows.chunk(G)[d] for s in range(G)]) for d in range(G)]
+        counts = [torch.stack([routed[s].send_counts[d] for s in range(G)]) for d in range(G)]
+    with torch.cuda.graph(gs[1], stream=st):
+        outs = [layers[d].compute(recv[d], counts[d]) for d in range(G)]
+        back = [torch.cat([outs[d].chunk(G)[s] for d in range(G)]) for s in range(G)]
+    with torch.cuda.graph(gs[2], stream=st):
+        ys = [layers[r].finish(routed[r], back[r]) for r in range(G)]
+    for y in ys:
+        y.zero_()
+    for g in gs:
+        g.replay()
+    torch.cuda.synchronize()
+    for r in range(G):
+        assert torch.equal(ys[r], y_eager[r]), f"rank {r}"
 
 
 # ------------------------------------------- the step entry points, one by one --
