@@ -47,10 +47,9 @@ NCU_TRAFFIC = {
     # prefill workload: dram__bytes_read.sum + dram__bytes_write.sum of one launch
     "prefill/expert_gemm1": {"bytes": 1027551744 + 221377280, "src": "ffn_gemm.cu", "src_sha": "9c589b4d85665278"},
     "prefill/expert_gemm2": {"bytes": 1417872640 + 65498880, "src": "ffn_gemm.cu", "src_sha": "9c589b4d85665278"},
-    "prefill/router": {"bytes": 33676032, "src": "router.cu", "src_sha": "d3b06cd2819ee340"},
-    # router sweep, k = 1: router_kernel + dispatch_kernel of one call
-    "router_k1/router+dispatch": {"bytes": 17889024 + 40448, "src": ["router.cu", "dispatch_combine.cu"],
-                                  "src_sha": ["d3b06cd2819ee340", "67a1c639e9ea246b"]},
+    # router sweep, k = 1: the fused route (router + dispatch in one kernel) of one call
+    "router_k1/router+dispatch": {"bytes": 17904896 + 0, "src": ["route_fused.cu", "route_topk.cuh"],
+                                  "src_sha": ["c59dd470e0e349a5", "ee199279a3609b01"]},
     # decode workload: both GEMMs on the small-batch kernel
     "decode/expert_gemm1": {"bytes": 940161024 + 3989760, "src": "ffn_gemm_small.cu", "src_sha": "ff59fa4c79617713"},
     "decode/expert_gemm2": {"bytes": 941419776 + 5054208, "src": "ffn_gemm_small.cu", "src_sha": "ff59fa4c79617713"},
