@@ -714,7 +714,8 @@ def test_step_entry_points_against_oracle(T, H, F, E, k, cf, act):
 
 # ---------------------------------------------- host batches, copies overlapped --
 
-def test_host_pipeline_matches_one_call_at_a_time():
+@pytest.mark.parametrize("graphs", [False, True], ids=["launches", "graphs"])
+def test_host_pipeline_matches_one_call_at_a_time(graphs):
     from mixture_experts_layer_12_gb300.host_pipeline import HostPipeline
     cfg = moe_synth.MoEConfig("pipe", T=256, H=256, F=512, E=8, k=2, seed=28)
     dev_in = to_dev(moe_synth.make_inputs(cfg))
@@ -724,7 +725,7 @@ def test_host_pipeline_matches_one_call_at_a_time():
     refs = [layer(x.to(DEV)).cpu() for x in xs]
     ys = [torch.full((cfg.T, cfg.H), float("nan"), dtype=torch.bfloat16).pin_memory()
           for _ in range(5)]
-    HostPipeline(layer, cfg.T, DEV).run(xs, ys)
+    HostPipeline(layer, cfg.T, DEV, graphs=graphs).run(xs, ys)
     torch.cuda.synchronize()
     assert moe.moe_get_device_status(layer.ws) == 0
     for y, ref in zip(ys, refs):
