@@ -45,8 +45,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # source it was taken on; reported as null once the source changes.
 NCU_TRAFFIC = {
     # prefill workload: dram__bytes_read.sum + dram__bytes_write.sum of one launch
-    "prefill/expert_gemm1": {"bytes": 1027551744 + 221377280, "src": "ffn_gemm.cu", "src_sha": "9c589b4d85665278"},
-    "prefill/expert_gemm2": {"bytes": 1417872640 + 65498880, "src": "ffn_gemm.cu", "src_sha": "9c589b4d85665278"},
+    "prefill/expert_gemm1": {"bytes": 1032561408 + 221230080, "src": "ffn_gemm.cu", "src_sha": "9c589b4d85665278"},
+    "prefill/expert_gemm2": {"bytes": 1429054976 + 60358144, "src": "ffn_gemm.cu", "src_sha": "9c589b4d85665278"},
     # router sweep, k = 1: the fused route (router + dispatch in one kernel) of one call
     "router_k1/router+dispatch": {"bytes": 17904896 + 0, "src": ["route_fused.cu", "route_topk.cuh"],
                                   "src_sha": ["c59dd470e0e349a5", "ee199279a3609b01"]},

@@ -172,7 +172,10 @@ def test_router_sweep_full_size(k):
 
 
 @pytest.mark.parametrize("T,E,k,cf", [(16384, 128, 2, None), (16384, 8, 1, 0.7),
-                                      (3000, 200, 8, 0.3), (9000, 64, 4, None)])
+                                      (3000, 200, 8, 0.3), (9000, 64, 4, None),
+                                      (16384, 256, 8, 1.1),   # widest accumulator, most tiles
+                                      (129, 256, 8, None),    # 2 tiles x 8 K splits, E > 64
+                                      (256, 96, 3, 0.5)])     # 2 tiles, E = 96 (E16 = 96)
 def test_route_in_one_launch_at_scale(T, E, k, cf):
     # the fused route: 128 tiles (the most it takes: one K split each), E that
     # fills an uneven number of count chunks (200 -> 13), drops, many tiles
@@ -183,6 +186,18 @@ def test_route_in_one_launch_at_scale(T, E, k, cf):
     _, rep = routing_parity(cfg, inputs, r)
     if cf is not None:
         assert rep["dropped"] > 0
+
+
+@pytest.mark.parametrize("gating", [moe.MOE_GATE_SOFTMAX_TOPK, moe.MOE_GATE_SOFTMAX_TOPK_RENORM])
+@pytest.mark.parametrize("T,E,k", [(4096, 8, 2), (2048, 128, 8), (700, 13, 4)])
+def test_route_in_one_launch_gating_and_bias(gating, T, E, k):
+    # the fused route with the softmax-over-all-experts gate modes, a bias and
+    # E % 8 != 0 (padded W_router)
+    cfg = moe_synth.MoEConfig("fusedgate", T=T, H=256, F=0, E=E, k=k, seed=33, bias0=1.5)
+    assert moe.moe_forward_plan(moe.make_shape(T, cfg.H, 8, E, k, None, gating))[0]
+    inputs = moe_synth.make_inputs(cfg, with_ffn=False)
+    r = gpu_route(cfg, to_dev(inputs), gating)
+    routing_parity(cfg, inputs, r, gating=gating)
 
 
 def test_router_kernels_past_128_tiles_wide_experts():
