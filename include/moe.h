@@ -159,9 +159,12 @@ MOE_API size_t moe_route_workspace_size(const moe_shape* s);
  * Which kernels moe_forward (and moe_route) launch for this shape; no
  * counterpart on the pages, for callers that count or profile kernels.
  * Host only: depends on the shape alone.
- *   *dispatch_in_router = 1 for small batches (T <= 128 and E <= 64): the
- *     logits are computed on the CUDA cores and the dispatch (step 3) runs
- *     in the same launch; 0: the tensor-core router, then a dispatch kernel.
+ *   *dispatch_in_router = 1 when the dispatch (step 3) runs in the router's
+ *     launch: small batches (T <= 128 and E <= 64, logits on the CUDA
+ *     cores) and batches of up to 128 tiles of 128 tokens (T <= 16384; the
+ *     fused tensor-core route, on a GPU that holds one such CTA per SM for
+ *     at least 128 SMs, as every sm_103 part does); 0: the tensor-core
+ *     cluster router, then a dispatch kernel.
  *   *combine_in_gemm = 1 for k = 1: the combine runs inside the second
  *     expert GEMM; 0: a separate combine kernel.
  * Returns MOE_OK, or MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for a bad
@@ -173,7 +176,11 @@ MOE_API int moe_forward_plan(const moe_shape* s, int32_t* dispatch_in_router,
 /*
  * Steps 1-3 (the router kernel "MoERouterKernel::Process": x × W_router on
  * the tensor cores, per-token TopK, Softmax over the k scores; then the
- * dispatch of GatherTokensByExpert) for all T tokens.
+ * dispatch of GatherTokensByExpert) for all T tokens.  Up to 128 tiles of
+ * 128 tokens this is one launch that splits the logit GEMM along H over
+ * every SM and dispatches in the same kernel; every wait inside it is
+ * bounded (a CTA that could not become resident, e.g. behind another
+ * stream's long kernel, ends the call with MOE_DEV_TIMEOUT, not a hang).
  *   x        [T, H]  bf16        w_router [H, E] bf16 (E contiguous)
  *   b_router [E]     fp32 or NULL (added to the logits)
  * Outputs (device, caller-owned):
@@ -271,12 +278,13 @@ MOE_API int moe_combine(const moe_shape* s, const uint16_t* Y, const float* weig
 /*
  * The whole layer (the op "MoEFusion::Compute(x, w_router, expert_weights,
  * y)" of section "3. 完整调用流程"): moe_route followed by
- * moe_expert_ffn_combine on `stream` with no host synchronisation: a
- * one-warp kernel that clears the status block, then router, dispatch,
- * permute, expert GEMM1, expert GEMM2 and combine -- seven kernels, one
- * fewer when the router also dispatches (moe_forward_plan: small batches)
- * and one fewer when GEMM2 also combines (k = 1).  The routing outputs are
- * written as in moe_route.
+ * moe_expert_ffn_combine on `stream` with no host synchronisation: a small
+ * kernel that clears the status block, then router, dispatch, permute,
+ * expert GEMM1, expert GEMM2 and combine -- seven kernels, one fewer when
+ * the router also dispatches (moe_forward_plan: up to 128 tiles of 128
+ * tokens), one fewer when GEMM2 also combines (k = 1), and one more (a
+ * W_router copy padded to 8-expert rows) when E % 8 != 0.  The routing
+ * outputs are written as in moe_route.
  */
 MOE_API int moe_forward(const moe_shape* s, const uint16_t* x, const uint16_t* w_router,
                 const float* b_router, const uint16_t* w1, const uint16_t* w2, uint16_t* y,

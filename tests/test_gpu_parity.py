@@ -725,6 +725,12 @@ def test_step_entry_points_against_oracle(T, H, F, E, k, cf, act):
     assert moe.moe_get_device_status(ws) == 0
     y_ref = reference_y(inputs, logits, np_(r.ids), np_(r.slot), np.arange(T, dtype=np.int32))
     check_y(y.float().cpu().numpy(), y_ref)
+    # and moe_expert_ffn_combine, the same steps in one call, against the oracle too
+    y2 = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device=DEV)
+    moe.moe_expert_ffn_combine(s, dev_in["x"], dev_in["w1"], dev_in["w2"], r.weights, r.offsets,
+                               r.perm, r.slot, y2, ws)
+    assert moe.moe_get_device_status(ws) == 0
+    check_y(y2.float().cpu().numpy(), y_ref)
 
 
 # ---------------------------------------------- host batches, copies overlapped --
