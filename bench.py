@@ -251,9 +251,11 @@ SUSTAINED_REGION_MS = 1000.0
 def tensor_peak(peaks, region_ms, clocks):
     """(peak TFLOP/s, kind) for a contraction timed over `region_ms` with the
     sampled `clocks`: the burst figure for a short region at full clocks, the
-    sustained one for a region of a second or more or one that hit the
-    power cap."""
-    capped = bool(clocks) and "sw_power_cap" in clocks.get("reasons", [])
+    sustained one for a region of a second or more, or one whose clock the
+    power cap held down (median below 95% of the maximum with sw_power_cap
+    seen; a momentary cap flag at full clock is still a burst)."""
+    capped = (bool(clocks) and "sw_power_cap" in clocks.get("reasons", [])
+              and clocks.get("sm_mhz", 0.0) < 0.95 * (clocks.get("sm_max_mhz") or 0.0))
     if region_ms >= SUSTAINED_REGION_MS or capped:
         return peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]), "sustained"
     return peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]), "burst"

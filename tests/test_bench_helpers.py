@@ -70,11 +70,14 @@ def test_ncu_traffic_only_for_the_sources_it_was_taken_on(monkeypatch):
 
 def test_tensor_peak_follows_the_timed_region_and_clocks():
     peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-    full = {"sm_mhz": 2070.0, "reasons": []}
-    capped = {"sm_mhz": 1650.0, "reasons": ["sw_power_cap"]}
-    # a short region at full clocks is a burst; a long one, or one that hit
-    # the power cap, runs at the sustained rate
+    full = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": []}
+    capped = {"sm_mhz": 1650.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    flagged_full = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]}
+    # a short region at full clocks is a burst (a momentary cap flag included);
+    # a long one, or one whose clock the power cap held down, runs at the
+    # sustained rate
     assert bench.tensor_peak(peaks, 25.0, full) == (1900.0, "burst")
+    assert bench.tensor_peak(peaks, 25.0, flagged_full) == (1900.0, "burst")
     assert bench.tensor_peak(peaks, 25.0, capped) == (1700.0, "sustained")
     assert bench.tensor_peak(peaks, 1400.0, full) == (1700.0, "sustained")
     assert bench.tensor_peak(peaks, 25.0, None) == (1900.0, "burst")
