@@ -189,3 +189,18 @@ def test_forward_plan_is_a_host_only_shape_rule(lib):
     c = ctypes.c_int32(0)
     good = moe.make_shape(64, 128, 256, 8, 2)
     assert lib.moe_forward_plan(ctypes.byref(good), None, ctypes.byref(c)) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_plain_c_caller(lib, tmp_path):
+    # tests/c_abi_check.c: a C program built with gcc against include/moe.h
+    # and linked to libmoe.so, calling the host-answered entry points
+    import subprocess
+    exe = tmp_path / "c_abi_check"
+    libdir = os.path.dirname(moe.LIB_PATH)
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), os.path.join(ROOT, "tests", "c_abi_check.c"),
+                    "-L", libdir, "-l:libmoe.so", f"-Wl,-rpath,{libdir}", "-lm", "-o", str(exe)],
+                   check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == "ok"
