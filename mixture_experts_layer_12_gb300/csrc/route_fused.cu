@@ -448,35 +448,48 @@ __global__ void __launch_bounds__(FTHREADS, 1)
       if (cgi < NC && gg < G)
         hv[j] = __ldcg(reinterpret_cast<const uint4*>(a.grp_hist + (size_t)gg * EP + cgi * 16));
     }
-    int pre[16], tot[16];
+    // packed sums: word q of a chunk holds the counts of experts 4q..4q+3 as
+    // bytes; its even bytes (experts 4q, 4q+2) and odd bytes (4q+1, 4q+3) go
+    // to two words of 16-bit lanes, so one add sums two experts (a lane
+    // reaches at most 256 CTAs x 128 = 32768)
+    uint32_t pre[8], tot[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) pre[i] = tot[i] = 0;
+    for (int i = 0; i < 8; ++i) pre[i] = tot[i] = 0u;
 #pragma unroll
     for (int j = 0; j < MAXL; ++j) {
       const int gg = tid / NCP + j * gstep;
       if (cgi < NC && gg < G) {
         const uint32_t w4[4] = {hv[j].x, hv[j].y, hv[j].z, hv[j].w};
+        const bool before = gg < grp;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int b = (int)((w4[i >> 2] >> (8 * (i & 3))) & 0xffu);
-          tot[i] += b;
-          if (gg < grp) pre[i] += b;
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t ev = w4[q] & 0x00ff00ffu;
+          const uint32_t od = (w4[q] >> 8) & 0x00ff00ffu;
+          tot[2 * q] += ev;
+          tot[2 * q + 1] += od;
+          if (before) {
+            pre[2 * q] += ev;
+            pre[2 * q + 1] += od;
+          }
         }
       }
     }
     // lanes l and l ^ off hold the same chunk for off >= NCP (NCP | 32)
     for (int off = 16; off >= NCP; off >>= 1) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < 8; ++i) {
         pre[i] += __shfl_xor_sync(0xffffffffu, pre[i], off);
         tot[i] += __shfl_xor_sync(0xffffffffu, tot[i], off);
       }
     }
     if (lane < NCP && lane < NC) {
+      // word 2q + h, 16-bit lane l: expert 4q + 2l + h of chunk `lane`
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        P.red[0][warp * 256 + lane * 16 + i] = pre[i];
-        P.red[1][warp * 256 + lane * 16 + i] = tot[i];
+        const int w = 2 * (i >> 2) + (i & 1);
+        const int sh = 16 * ((i >> 1) & 1);
+        P.red[0][warp * 256 + lane * 16 + i] = (int)((pre[w] >> sh) & 0xffffu);
+        P.red[1][warp * 256 + lane * 16 + i] = (int)((tot[w] >> sh) & 0xffffu);
       }
     }
   }
