@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
   for (int e = tid; e < E; e += FTHREADS) P.run[e] = 0;
   const unsigned lt = (1u << lane) - 1u;
   for (int c0 = 0; c0 < n; c0 += FTHREADS) {
-    for (int idx = tid; idx < FWARPS * kMaxExperts; idx += FTHREADS) (&P.wc[0][0])[idx] = 0;
+    for (int idx = tid; idx < FWARPS * E; idx += FTHREADS) P.wc[idx / E][idx % E] = 0;
     __syncthreads();
     const int i = c0 + tid;
     const int e = i < n ? P.ids[i] : -1;
