@@ -142,7 +142,9 @@ MOE_API int64_t moe_expert_capacity(const moe_shape* s);
 /* Workspace bytes needed by moe_forward and moe_expert_ffn_combine (and
  * enough for every other entry point): a 1 KB status block, per-128-token
  * expert counts [ceil(T/128), E] int32, the padded W_router copy when
- * E % 8 != 0 (see moe_route_workspace_size), h [T*k, F] bf16, a [T*k, H] bf16
+ * E % 8 != 0 (see moe_route_workspace_size), the fused route's per-CTA
+ * expert counts (bytes, at most 256 rows of E rounded up to 16) for the
+ * batches it serves, h [T*k, F] bf16, a [T*k, H] bf16
  * region that holds first the token rows in dispatch order, then the
  * expert outputs, and for T*k <= 64 rows fp32 partial expert outputs of up
  * to 4 K splits [4, T*k, H] (the small-batch second GEMM).  Returns 0 for
@@ -150,9 +152,9 @@ MOE_API int64_t moe_expert_capacity(const moe_shape* s);
 MOE_API size_t moe_workspace_size(const moe_shape* s);
 
 /* Workspace bytes needed by moe_route and moe_dispatch (status block,
- * per-128-token expert counts and, when E % 8 != 0, the padded copy of
- * W_router [H, E rounded up to 8]; F is ignored).  Returns 0 for an invalid
- * shape. */
+ * per-128-token expert counts, when E % 8 != 0 the padded copy of W_router
+ * [H, E rounded up to 8], and the fused route's per-CTA counts; F is
+ * ignored).  Returns 0 for an invalid shape. */
 MOE_API size_t moe_route_workspace_size(const moe_shape* s);
 
 /*
@@ -174,11 +176,27 @@ MOE_API int moe_forward_plan(const moe_shape* s, int32_t* dispatch_in_router,
                              int32_t* combine_in_gemm);
 
 /*
+ * The launch shape of the one-launch tensor-core route on the current
+ * device, for callers that profile the route; no counterpart on the pages.
+ *   *tile_tokens = tokens per tile (64 or 128), *splits = K splits per tile
+ *     (the thread-block cluster size: 1, 2, 4 or 8) -- the pair that
+ *     minimises the bytes each CTA streams among those whose clusters all
+ *     fit on the device at once; both 0 when the shape routes otherwise
+ *     (small batch on the CUDA cores, or router + dispatch kernels).
+ * Sets up the current device (as every entry point does).  Returns MOE_OK,
+ * MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for a bad shape or a null
+ * output, MOE_ERR_CUDA if the device cannot be set up.
+ */
+MOE_API int moe_route_plan(const moe_shape* s, int32_t* tile_tokens, int32_t* splits);
+
+/*
  * Steps 1-3 (the router kernel "MoERouterKernel::Process": x × W_router on
  * the tensor cores, per-token TopK, Softmax over the k scores; then the
  * dispatch of GatherTokensByExpert) for all T tokens.  Up to 128 tiles of
- * 128 tokens this is one launch that splits the logit GEMM along H over
- * every SM and dispatches in the same kernel; every wait inside it is
+ * 128 tokens this is one launch that splits the logit GEMM along H across
+ * the CTAs of a thread-block cluster (tiles of 64 or 128 tokens, up to 8
+ * splits, spread over the SMs) and dispatches in the same kernel; every
+ * wait inside it on memory or on other clusters is
  * bounded (a CTA that could not become resident, e.g. behind another
  * stream's long kernel, ends the call with MOE_DEV_TIMEOUT, not a hang).
  *   x        [T, H]  bf16        w_router [H, E] bf16 (E contiguous)

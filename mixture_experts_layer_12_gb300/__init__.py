@@ -39,7 +39,8 @@ EXPORTS = ("moe_version", "moe_last_error_string", "moe_expert_capacity", "moe_w
            "moe_route", "moe_dispatch", "moe_expert_ffn_combine", "moe_forward",
            "moe_get_device_status", "moe_selftest_wait_timeout", "moe_forward_profiled",
            "moe_expert_ffn_combine_noalloc", "moe_route_workspace_size", "moe_dispatch_rows",
-           "moe_expert_ffn", "moe_combine", "moe_forward_plan", "moe_noalloc_device_status")
+           "moe_expert_ffn", "moe_combine", "moe_forward_plan", "moe_noalloc_device_status",
+           "moe_route_plan")
 MOE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -108,6 +109,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
             "moe_combine": ([S, P, P, P, P, P], ctypes.c_int),
             "moe_forward_plan": ([S, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
                                  ctypes.c_int),
+            "moe_route_plan": ([S, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)],
+                               ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -199,6 +202,14 @@ def moe_forward_plan(shape: moe_shape) -> tuple[bool, bool]:
     d, c = ctypes.c_int32(0), ctypes.c_int32(0)
     _check(load_library().moe_forward_plan(ctypes.byref(shape), ctypes.byref(d), ctypes.byref(c)))
     return bool(d.value), bool(c.value)
+
+
+def moe_route_plan(shape: moe_shape) -> tuple[int, int]:
+    """(tokens per tile, K splits) of the one-launch tensor-core route on
+    the current CUDA device, (0, 0) when the shape routes otherwise."""
+    tm, sp = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(load_library().moe_route_plan(ctypes.byref(shape), ctypes.byref(tm), ctypes.byref(sp)))
+    return int(tm.value), int(sp.value)
 
 
 def moe_route_workspace_size(shape: moe_shape) -> int:

@@ -154,17 +154,14 @@ int64_t capacity_of(const moe_shape* s) {
 // --------------------------------------------------------------- workspace --
 
 // Workspace: [status block | per-tile expert counts | padded W_router |
-// fused-route counts | fused-route partial logits | h | Y | fp32 partials].
-// The status block holds the device status word (byte 0), the router's
-// completion ticket (byte 64) and the fused route's grid counter (byte 128)
-// and per-tile counters (bytes 256 .. 767); all are cleared at the start of
+// fused-route counts | h | Y | fp32 partials].  The status block holds the
+// device status word (byte 0), the router's completion ticket (byte 64) and
+// the fused route's grid counter (byte 128); all are cleared at the start of
 // every call.  The padded W_router copy exists only when E % 8 != 0, the
-// fused route's regions only for shapes it serves.
+// fused route's counts only for shapes it serves.
 constexpr size_t kStatusBytes = 1024;
 constexpr size_t kTicketOffset = 64;
 constexpr size_t kGridCntOffset = 128;
-constexpr size_t kTileCntOffset = 256;
-static_assert(kTileCntOffset + 4 * kFusedMaxTiles <= kStatusBytes, "status block layout");
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 size_t hist_bytes(const moe_shape* s) {
@@ -179,30 +176,27 @@ size_t h_bytes(const moe_shape* s) { return align_up((size_t)s->T * s->k * s->F 
 size_t y_bytes(const moe_shape* s) { return align_up((size_t)s->T * s->k * s->H * 2, 1024); }
 
 // The route runs on the CUDA cores in one launch for small batches, as one
-// fused tensor-core launch for up to kFusedMaxTiles tiles (every sm_103 part
-// holds that many of its CTAs at once), else as router + dispatch kernels.
+// fused tensor-core launch for up to kFusedMaxTiles x 128 tokens (when its
+// clusters all fit on the device at once; every sm_103 part holds 128 of its
+// CTAs), else as router + dispatch kernels.
 bool route_small(const moe_shape* s) { return s->T <= kSmallRouteTokens && s->E <= kSmallRouteExperts; }
 int route_tiles(const moe_shape* s) { return (s->T + 127) / 128; }
 bool route_fused_shape(const moe_shape* s) {
   return !route_small(s) && s->T > 0 && route_tiles(s) <= kFusedMaxTiles;
 }
 int route_npad(const moe_shape* s) { return (s->E + 15) / 16 * 16; }
-// upper bound of the fused route's CTAs (tiles x K splits), from the shape alone
+// upper bound of the fused route's CTAs (64-token tiles x K splits), from
+// the shape alone
 int fused_ctas_bound(const moe_shape* s) {
   const int kb = (s->H + 63) / 64;
-  const long long n = (long long)route_tiles(s) * (kb < kFusedMaxSplits ? kb : kFusedMaxSplits);
+  const long long n = (long long)((s->T + 63) / 64) * (kb < kFusedMaxSplits ? kb : kFusedMaxSplits);
   return (int)(n < kFusedMaxCtas ? n : kFusedMaxCtas);
 }
 size_t fused_hist_bytes(const moe_shape* s) {
   return route_fused_shape(s) ? align_up((size_t)fused_ctas_bound(s) * route_npad(s), 1024) : 0;
 }
-size_t fused_part_bytes(const moe_shape* s) {
-  return route_fused_shape(s)
-             ? align_up((size_t)fused_ctas_bound(s) * 128 * route_npad(s) * 4, 1024)
-             : 0;
-}
 size_t route_ws_bytes(const moe_shape* s) {
-  return kStatusBytes + hist_bytes(s) + wpad_bytes(s) + fused_hist_bytes(s) + fused_part_bytes(s);
+  return kStatusBytes + hist_bytes(s) + wpad_bytes(s) + fused_hist_bytes(s);
 }
 // small batches: fp32 partial expert outputs of a K-split second GEMM
 size_t part_bytes(const moe_shape* s) {
@@ -226,10 +220,6 @@ uint16_t* wpad_ptr(void* ws, const moe_shape* s) {
 uint8_t* fused_hist_ptr(void* ws, const moe_shape* s) {
   return reinterpret_cast<uint8_t*>(static_cast<char*>(ws) + kStatusBytes + hist_bytes(s) +
                                     wpad_bytes(s));
-}
-float* fused_part_ptr(void* ws, const moe_shape* s) {
-  return reinterpret_cast<float*>(static_cast<char*>(ws) + kStatusBytes + hist_bytes(s) +
-                                  wpad_bytes(s) + fused_hist_bytes(s));
 }
 uint16_t* h_ptr(void* ws, const moe_shape* s) {
   return reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + route_ws_bytes(s));
@@ -303,49 +293,42 @@ int enqueue_route(const moe_shape* s, int sms, const uint16_t* x, const uint16_t
     return mark(ev, 2, st);  // no separate dispatch kernel
   }
   CUtensorMap tm_x, tm_w;
-  if ((rc = map_2d(&tm_x, x, (uint64_t)s->H, (uint64_t)s->T, 64, 128, "x (router)")) != MOE_OK) return rc;
   if ((rc = map_2d(&tm_w, w_router, (uint64_t)ldw, (uint64_t)s->H, 64, 64, "w_router")) != MOE_OK) return rc;
   const int mtiles = route_tiles(s);
   const int kblocks = (s->H + 63) / 64;
-  if (route_fused_shape(s)) {
-    // one launch: K splits per tile as many as keep every CTA resident
-    long long resident = (long long)route_fused_resident_per_sm(s->E) * sms;
-    if (resident > kFusedMaxCtas) resident = kFusedMaxCtas;
-    int S = (int)(resident / mtiles);
-    if (S > kFusedMaxSplits) S = kFusedMaxSplits;
-    if (S > kblocks) S = kblocks;
-    if (S >= 1) {
-      FusedRouteArgs fa;
-      fa.T = s->T;
-      fa.H = s->H;
-      fa.E = s->E;
-      fa.k = s->k;
-      fa.npad = route_npad(s);
-      fa.ep = route_npad(s);
-      fa.tmem_cols = 32;
-      while (fa.tmem_cols < fa.npad) fa.tmem_cols *= 2;
-      fa.capacity = (int)capacity_of(s);
-      fa.gating = s->gating;
-      fa.bias = b_router;
-      fa.ids = ids;
-      fa.weights = weights;
-      fa.counts = counts;
-      fa.offsets = offsets;
-      fa.perm = perm;
-      fa.slot = slot;
-      fa.part = fused_part_ptr(ws, s);
-      fa.grp_hist = fused_hist_ptr(ws, s);
-      fa.tile_cnt = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kTileCntOffset);
-      fa.grid_cnt = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kGridCntOffset);
-      fa.status = status_ptr(ws);
-      fa.wait_limit_ns = kWaitLimitNs;
-      if ((rc = mark(ev, 0, st)) != MOE_OK) return rc;
-      cudaError_t e = launch_route_fused(tm_x, tm_w, fa, S, st, ev == nullptr);
-      if (e != cudaSuccess) return cuda_fail(e, "route launch");
-      if ((rc = mark(ev, 1, st)) != MOE_OK) return rc;
-      return mark(ev, 2, st);  // the dispatch ran in the same launch
-    }
+  FusedRoutePlan plan;
+  if (route_fused_shape(s) && route_fused_pick(s->T, s->H, s->E, &plan)) {
+    if ((rc = map_2d(&tm_x, x, (uint64_t)s->H, (uint64_t)s->T, 64, (uint32_t)plan.tm, "x (route)")) != MOE_OK)
+      return rc;
+    FusedRouteArgs fa;
+    fa.T = s->T;
+    fa.H = s->H;
+    fa.E = s->E;
+    fa.k = s->k;
+    fa.npad = route_npad(s);
+    fa.ep = route_npad(s);
+    fa.tmem_cols = 32;
+    while (fa.tmem_cols < fa.npad) fa.tmem_cols *= 2;
+    fa.capacity = (int)capacity_of(s);
+    fa.gating = s->gating;
+    fa.bias = b_router;
+    fa.ids = ids;
+    fa.weights = weights;
+    fa.counts = counts;
+    fa.offsets = offsets;
+    fa.perm = perm;
+    fa.slot = slot;
+    fa.grp_hist = fused_hist_ptr(ws, s);
+    fa.grid_cnt = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + kGridCntOffset);
+    fa.status = status_ptr(ws);
+    fa.wait_limit_ns = kWaitLimitNs;
+    if ((rc = mark(ev, 0, st)) != MOE_OK) return rc;
+    cudaError_t e = launch_route_fused(tm_x, tm_w, fa, plan, st, ev == nullptr);
+    if (e != cudaSuccess) return cuda_fail(e, "route launch");
+    if ((rc = mark(ev, 1, st)) != MOE_OK) return rc;
+    return mark(ev, 2, st);  // the dispatch ran in the same launch
   }
+  if ((rc = map_2d(&tm_x, x, (uint64_t)s->H, (uint64_t)s->T, 64, 128, "x (router)")) != MOE_OK) return rc;
   RouterArgs ra;
   ra.T = s->T;
   ra.H = s->H;
@@ -641,6 +624,22 @@ int moe_forward_plan(const moe_shape* s, int32_t* dispatch_in_router, int32_t* c
     return fail(MOE_ERR_INVALID_ARG, "dispatch_in_router / combine_in_gemm is null");
   *dispatch_in_router = route_small(s) || route_fused_shape(s) ? 1 : 0;
   *combine_in_gemm = s->k == 1 ? 1 : 0;
+  return MOE_OK;
+}
+
+int moe_route_plan(const moe_shape* s, int32_t* tile_tokens, int32_t* splits) {
+  int rc = check_shape(s, false);
+  if (rc != MOE_OK) return rc;
+  if (!tile_tokens || !splits) return fail(MOE_ERR_INVALID_ARG, "tile_tokens / splits is null");
+  *tile_tokens = 0;
+  *splits = 0;
+  int sms = 0;
+  if ((rc = device_setup(&sms)) != MOE_OK) return rc;
+  FusedRoutePlan plan;
+  if (route_fused_shape(s) && route_fused_pick(s->T, s->H, s->E, &plan)) {
+    *tile_tokens = plan.tm;
+    *splits = plan.splits;
+  }
   return MOE_OK;
 }
 

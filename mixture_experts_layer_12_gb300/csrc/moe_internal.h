@@ -50,11 +50,11 @@ cudaError_t launch_router(const CUtensorMap& tm_x, const CUtensorMap& tm_w, cons
 size_t router_smem_bytes(int E);
 
 // ---- the whole route (router + dispatch) in one launch for batches of up
-// to kFusedMaxTiles tiles of 128 tokens (route_fused.cu): tiles x splits
-// CTAs, all resident at once, K split across the CTAs of a tile with the
-// fp32 partials exchanged through the workspace.
+// to kFusedMaxTiles x 128 tokens (route_fused.cu): tiles of 64 or 128 tokens
+// x S K splits, all resident at once; the S CTAs of a tile are one cluster
+// and exchange their fp32 partial logits through distributed shared memory.
 constexpr int kFusedMaxTiles = 128;   // T <= 16384 tokens
-constexpr int kFusedMaxSplits = 12;   // K splits per tile
+constexpr int kFusedMaxSplits = 8;    // K splits per tile (the cluster size)
 constexpr int kFusedMaxCtas = 256;    // tiles x splits
 struct FusedRouteArgs {
   int T, H, E, k;
@@ -70,19 +70,26 @@ struct FusedRouteArgs {
   int32_t* offsets;   // [E+1]
   int32_t* perm;      // [T*k]
   int32_t* slot;      // [T, k]
-  float* part;        // workspace: [tiles * splits][128][npad] fp32 partial logits
   uint8_t* grp_hist;  // workspace: [tiles * splits][ep] assignments per expert
-  unsigned* tile_cnt; // [tiles] zero before the launch
   unsigned* grid_cnt; // zero before the launch
   int* status;
   uint64_t wait_limit_ns;
 };
-// tm_x / tm_w as for launch_router; grid (splits, ceil(T/128)).
+struct FusedRoutePlan {
+  int tm;      // tokens per tile: 64 or 128
+  int splits;  // K splits per tile = cluster size: 1, 2, 4 or 8
+  int tiles;   // ceil(T / tm)
+};
+// The tile height and split that minimise the bytes each CTA streams, among
+// those whose clusters all fit on the current device at once and with at
+// most kFusedMaxCtas CTAs; false if none does (or before
+// route_fused_set_attributes ran on the device).
+bool route_fused_pick(int T, int H, int E, FusedRoutePlan* plan);
+// tm_x: x [T, H] bf16, box {64, plan.tm}, 128B swizzle; tm_w as for
+// launch_router.  Grid (splits, tiles), clusters of `splits`.
 cudaError_t launch_route_fused(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                               const FusedRouteArgs& a, int splits, cudaStream_t st, bool pdl);
-// CTAs of the fused route kernel (for E experts) resident per SM on the
-// current device (0 before route_fused_set_attributes ran on it).
-int route_fused_resident_per_sm(int E);
+                               const FusedRouteArgs& a, const FusedRoutePlan& plan,
+                               cudaStream_t st, bool pdl);
 
 // ---- small-batch route (router + dispatch in one launch, CUDA cores):
 // for T <= kSmallRouteTokens and E <= kSmallRouteExperts.

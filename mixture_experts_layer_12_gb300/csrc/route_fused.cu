@@ -1,7 +1,7 @@
 // route_fused.cu -- the whole route in one launch that fills the GPU:
 // router logits on the tensor cores, per-token TopK and gate weights, and
 // the dispatch (histogram, scan, stable counting sort with the capacity
-// clip), for batches of up to kFusedMaxTiles tiles of 128 tokens.
+// clip), for batches of up to kFusedMaxTiles x 128 tokens.
 //
 // Follows "用Ascend C写一个MoE融合算子": section "1. Routing + Gating 合并"
 // (x × W_router, TopK per sample, Softmax over the top-k scores only) and
@@ -10,18 +10,21 @@
 // token dropping past the capacity from "CANN ops-transformer：MoE 路由算子的
 // 负载均衡策略", section "负载不均衡的根源".
 //
-// Design (sm_103a).  A batch of `tiles` tiles of 128 tokens runs as
-// tiles x S CTAs, one per SM, all resident at once (S = K splits per tile,
-// as many as fit):
+// Design (sm_103a).  A batch of `tiles` tiles of TM tokens (TM = 64 or 128)
+// runs as tiles x S CTAs, one per SM, all resident at once; the S CTAs of a
+// tile form one thread-block cluster (S = 1, 2, 4 or 8 K splits, chosen on
+// the host so that every cluster fits in one wave):
 //   1. each CTA streams its K slice of the tile's x rows and of W_router by
-//      TMA (128-byte swizzle, a ring of up to 8 stages) into one tcgen05.mma
-//      accumulator, 128 tokens x E experts in TMEM;
-//   2. it writes that fp32 partial to the workspace (L2) and arrives on the
-//      tile's counter; rank s of the tile owns rows [128 s / S, 128 (s+1) / S)
-//      and, once all S partials are in, sums each owned row's S partials in
-//      rank order (deterministic) -- with S up to 12 each SM takes in about
-//      a twelfth of the tile's bytes, and no thread-block cluster is needed
-//      (clusters of 8 do not all fit on the GPU at once);
+//      TMA (128-byte swizzle, a ring of up to 12 stages that fills shared
+//      memory) into one tcgen05.mma accumulator, 128 rows x E experts in
+//      TMEM (a 64-token tile loads 64 rows per A stage; the accumulator
+//      rows past them are never read);
+//   2. it stages that fp32 partial in its own shared memory (the ring, idle
+//      after the MMAs); after one cluster barrier, rank s -- the owner of
+//      rows [TM s / S, TM (s+1) / S) of the tile -- reads those rows of the
+//      other ranks' partials through distributed shared memory and sums
+//      the S partials of each row in rank order (deterministic); the
+//      partials never reach L2;
 //   3. TopK and the gate weights of the owned tokens by groups of 8 lanes
 //      (route_topk.cuh); the logits never reach HBM;
 //   4. the dispatch: each CTA ranks its own assignments within each expert
@@ -31,18 +34,22 @@
 //      CTAs before it (its base, in token order) and the totals (capacity
 //      clip, exclusive scan = offsets), and writes slot / perm of its own
 //      assignments -- the serial scan's order, with no second kernel.
-// Every wait (TMA ring, MMA completion, the two counters) is bounded; on
-// expiry MOE_DEV_TIMEOUT is recorded and the CTA returns.
+// Every wait on the CTA's own pipeline (TMA ring, MMA completion) and on the
+// grid counter is bounded; on expiry MOE_DEV_TIMEOUT is recorded.  A CTA
+// whose pipeline wait expired still stages (zeros) and reaches the cluster
+// barrier, which every CTA of the cluster therefore passes; no CTA exits
+// before the other ranks of its tile are done reading its shared memory.
 #include "route_topk.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int FBM = 128;
+constexpr int FBM = 128;  // MMA rows (M); a tile holds TM = 64 or 128 tokens of them
 constexpr int FBK = 64;
 constexpr int FTHREADS = 256;
 constexpr int FWARPS = FTHREADS / 32;
-constexpr int FMAX_STAGES = 8;
+constexpr int FMAX_STAGES = 12;
+constexpr int FSMEM_LIMIT = 232448;  // dynamic shared memory of one CTA (227 KB)
 
 struct FCtrl {
   uint64_t full[FMAX_STAGES];
@@ -54,7 +61,7 @@ struct FCtrl {
 };
 
 // Shared memory of the steps after the MMAs, behind the staged partial
-// logits [128][npad + 4] fp32 (both overlay the TMA ring).
+// logits [TM][npad + 4] fp32 (both overlay the TMA ring).
 struct FPost {
   int ids[FBM * kMaxTopK];          // the group's choices, token-major; -1 past T
   int lrank[FBM * kMaxTopK];        // rank within the expert inside this CTA
@@ -66,17 +73,25 @@ struct FPost {
   int red[2][FWARPS * 256];         // per-warp sums of the experts' counts
 };
 
-template <int NB64>
+template <int NB64, int TM>
 struct FCfg {
-  static constexpr int A_BYTES = FBM * FBK * 2;  // 16 KB
-  static constexpr int B_CHUNK = FBK * 64 * 2;   // 8 KB
+  static_assert(TM == 64 || TM == 128, "tile height");
+  // A slot: the tile's TM rows of a 64-wide K block.  The MMA always reads
+  // 128 rows (M = 128): with TM = 64 its rows 64..127 come from whatever
+  // follows the slot in shared memory (the next slot, or the first B
+  // buffer), and the accumulator rows they feed are never read.
+  static constexpr int A_BYTES = TM * FBK * 2;
+  static constexpr int B_CHUNK = FBK * 64 * 2;  // 8 KB
   static constexpr int B_BYTES = NB64 * B_CHUNK;
   static constexpr int STAGE = A_BYTES + B_BYTES;
-  static constexpr int STAGES = (196608 / STAGE) < FMAX_STAGES ? (196608 / STAGE) : FMAX_STAGES;
+  static constexpr int FIT = (int)((FSMEM_LIMIT - 1024 - sizeof(FCtrl)) / STAGE);
+  static constexpr int STAGES = FIT < FMAX_STAGES ? FIT : FMAX_STAGES;
   static constexpr int PIPE = STAGES * STAGE;
   static constexpr size_t SMEM = 1024 + (size_t)PIPE + sizeof(FCtrl);
-  // staged partial: 128 rows of npad + 4 floats (16-byte rows, banks spread)
-  static constexpr int STG_BYTES = FBM * (NB64 * 64 + 4) * 4;
+  static_assert(SMEM <= (size_t)FSMEM_LIMIT, "shared memory");
+  static_assert(STAGES * A_BYTES + (FBM - TM) * FBK * 2 <= PIPE, "128-row A reads stay in the ring");
+  // staged partial: TM rows of npad + 4 floats (16-byte rows, banks spread)
+  static constexpr int STG_BYTES = TM * (NB64 * 64 + 4) * 4;
   static_assert(STG_BYTES % 16 == 0, "aligned post-MMA state");
   static_assert(STG_BYTES + sizeof(FPost) <= (size_t)PIPE, "post-MMA state fits in the ring");
 };
@@ -119,11 +134,11 @@ __device__ bool fwait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns, i
   return true;
 }
 
-template <int NB64>
+template <int NB64, int TM>
 __global__ void __launch_bounds__(FTHREADS, 1)
     route_fused_kernel(const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_w, const FusedRouteArgs a) {
-  using C = FCfg<NB64>;
+  using C = FCfg<NB64, TM>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -136,18 +151,18 @@ __global__ void __launch_bounds__(FTHREADS, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int S = (int)gridDim.x;
-  const int s = (int)blockIdx.x;
+  const int S = (int)gridDim.x;  // = the cluster size
+  const int s = (int)blockIdx.x;  // = the rank in the cluster
   const int tile = (int)blockIdx.y;
   const int G = S * (int)gridDim.y;
   const int grp = tile * S + s;  // this CTA's group of tokens, in token order
-  const int m0 = tile * FBM;
+  const int m0 = tile * TM;
   const int KB = (a.H + FBK - 1) / FBK;
   const int kb0 = (int)(((long long)KB * s) / S);
   const int kb1 = (int)(((long long)KB * (s + 1)) / S);
   const int nkb = kb1 - kb0;
-  const int r0 = FBM * s / S;  // owned rows of the tile
-  const int R = FBM * (s + 1) / S - r0;
+  const int R = TM / S;  // owned rows of the tile (S divides TM)
+  const int r0 = R * s;
   pdl_launch_dependents();
 
   if (tid == 0) {
@@ -172,7 +187,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
   const uint32_t tmem = c.tmem_base;
   const WaitCtl wc{&c.abort_flag, a.status, a.wait_limit_ns};
 
-  // ---- 1. partial logits [128 x npad] over this CTA's K slice
+  // ---- 1. partial logits [TM x npad] over this CTA's K slice
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_w);
@@ -229,37 +244,38 @@ __global__ void __launch_bounds__(FTHREADS, 1)
   tc_fence_after();
   const bool have = ok && nkb > 0 && c.abort_flag == 0;
 
-  // ---- 2. the partial of all 128 rows into shared memory (warps w and
-  // w+4 read TMEM lanes 32 (w % 4) .. +31, their lane quadrant, and take
-  // alternate 16-column chunks, four loads in flight per wait), then the
-  // rows the tile's other CTAs own to the workspace, coalesced; this CTA's
-  // own rows never leave the SM
+  // ---- 2. the partial of the tile's TM rows into this CTA's shared memory
+  // (warps w and w+4 read TMEM lanes 32 (w % 4) .. +31, their lane quadrant,
+  // rows past TM skipped, and take alternate 16-column chunks, four loads in
+  // flight per wait)
   const int sp = a.npad + 4;  // staging row pitch (floats)
   const int v4 = a.npad / 4;  // float4 per row
   {
     const int q = warp & 3;
-    const int h = warp >> 2;
-    const int row = q * 32 + lane;
-    const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16);
-    const int nch = a.npad / 16;
-    for (int c0 = h; c0 < nch; c0 += 8) {
-      uint32_t v[4][16];
+    if (q * 32 < TM) {
+      const int h = warp >> 2;
+      const int row = q * 32 + lane;
+      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16);
+      const int nch = a.npad / 16;
+      for (int c0 = h; c0 < nch; c0 += 8) {
+        uint32_t v[4][16];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (c0 + 2 * u < nch) tmem_ld_x16(tb + (uint32_t)((c0 + 2 * u) * 16), v[u]);
-      tmem_ld_wait();
+        for (int u = 0; u < 4; ++u)
+          if (c0 + 2 * u < nch) tmem_ld_x16(tb + (uint32_t)((c0 + 2 * u) * 16), v[u]);
+        tmem_ld_wait();
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (c0 + 2 * u < nch) {
-          float4* d4 = reinterpret_cast<float4*>(stg + row * sp + (c0 + 2 * u) * 16);
+        for (int u = 0; u < 4; ++u) {
+          if (c0 + 2 * u < nch) {
+            float4* d4 = reinterpret_cast<float4*>(stg + row * sp + (c0 + 2 * u) * 16);
 #pragma unroll
-          for (int g4 = 0; g4 < 4; ++g4) {
-            float4 f;
-            f.x = have ? __uint_as_float(v[u][4 * g4 + 0]) : 0.f;
-            f.y = have ? __uint_as_float(v[u][4 * g4 + 1]) : 0.f;
-            f.z = have ? __uint_as_float(v[u][4 * g4 + 2]) : 0.f;
-            f.w = have ? __uint_as_float(v[u][4 * g4 + 3]) : 0.f;
-            d4[g4] = f;
+            for (int g4 = 0; g4 < 4; ++g4) {
+              float4 f;
+              f.x = have ? __uint_as_float(v[u][4 * g4 + 0]) : 0.f;
+              f.y = have ? __uint_as_float(v[u][4 * g4 + 1]) : 0.f;
+              f.z = have ? __uint_as_float(v[u][4 * g4 + 2]) : 0.f;
+              f.w = have ? __uint_as_float(v[u][4 * g4 + 3]) : 0.f;
+              d4[g4] = f;
+            }
           }
         }
       }
@@ -271,63 +287,50 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, (uint32_t)a.tmem_cols);
   }
-  {
-    float* dst = a.part + (size_t)grp * FBM * a.npad;
-    for (int idx = tid; idx < (FBM - R) * v4; idx += FTHREADS) {
-      const int ro = idx / v4;
-      const int row = ro < r0 ? ro : ro + R;  // skip the owned rows
-      const int col = (idx - ro * v4) * 4;
-      *reinterpret_cast<float4*>(dst + (size_t)row * a.npad + col) =
-          *reinterpret_cast<const float4*>(stg + row * sp + col);
-    }
-  }
-  __syncthreads();
-  if (tid == 0)
-    c.go = arrive_and_wait(a.tile_cnt + tile, (unsigned)S, a.wait_limit_ns, a.status) ? 1 : 0;
-  __syncthreads();
-  if (!c.go) return;
+  cluster_sync_all();  // every rank of the tile has staged its partial
 
-  // ---- 3a. owned rows: the S partials summed in rank order (all loads of
-  // an element issued before the sums), + bias, NaN -> -inf, columns past E
-  // at -inf; written over the staged row
-  {
-    const float* pt = a.part + (size_t)tile * S * FBM * a.npad;  // rank 0's partial of the tile
-    const size_t rstride = (size_t)FBM * a.npad;
-    for (int idx = tid; idx < R * v4; idx += FTHREADS) {
-      const int li = idx / v4;
-      const int col = (idx - li * v4) * 4;
-      const int row = r0 + li;
-      float4 p[kFusedMaxSplits];
+  // ---- 3a. owned rows: the S partials in rank order (the other ranks'
+  // read from their shared memory through DSMEM, a warp reading whole rows;
+  // all loads of an element issued before the sums), + bias, NaN -> -inf,
+  // columns past E at -inf; written over the staged row (rows no other rank
+  // reads)
+  for (int idx = tid; idx < R * v4; idx += FTHREADS) {
+    const int li = idx / v4;
+    const int col = (idx - li * v4) * 4;
+    const int row = r0 + li;
+    float4* mine = reinterpret_cast<float4*>(stg + row * sp + col);
+    const uint32_t la = smem_u32(mine);
+    float4 p[kFusedMaxSplits];
 #pragma unroll
-      for (int r = 0; r < kFusedMaxSplits; ++r)
-        if (r < S && r != s)
-          p[r] = __ldcg(reinterpret_cast<const float4*>(pt + r * rstride + (size_t)row * a.npad + col));
-      float4* mine = reinterpret_cast<float4*>(stg + row * sp + col);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < kFusedMaxSplits; ++r)
+      if (r < S && r != s) p[r] = dsmem_ld_v4(dsmem_map(la, (uint32_t)r));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int r = 0; r < kFusedMaxSplits; ++r) {
-        if (r < S) {
-          const float4 v = r == s ? *mine : p[r];
-          acc.x += v.x;
-          acc.y += v.y;
-          acc.z += v.z;
-          acc.w += v.w;
-        }
+    for (int r = 0; r < kFusedMaxSplits; ++r) {
+      if (r < S) {
+        const float4 v = r == s ? *mine : p[r];
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
       }
-      float o[4] = {acc.x, acc.y, acc.z, acc.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (col + i < a.E) {
-          float vv = o[i];
-          if (a.bias) vv += __ldg(a.bias + col + i);
-          o[i] = isnan(vv) ? -INFINITY : vv;
-        } else {
-          o[i] = -INFINITY;
-        }
-      }
-      *mine = make_float4(o[0], o[1], o[2], o[3]);
     }
+    float o[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (col + i < a.E) {
+        float vv = o[i];
+        if (a.bias) vv += __ldg(a.bias + col + i);
+        o[i] = isnan(vv) ? -INFINITY : vv;
+      } else {
+        o[i] = -INFINITY;
+      }
+    }
+    *mine = make_float4(o[0], o[1], o[2], o[3]);
   }
+  // done reading the other ranks' shared memory; every exit below waits
+  // until all ranks of the tile are done with this CTA's
+  cluster_arrive();
   __syncthreads();
 
   // ---- 3b. TopK and the gate weights of the owned tokens, 8 lanes per token
@@ -427,7 +430,10 @@ __global__ void __launch_bounds__(FTHREADS, 1)
   __syncthreads();
   if (tid == 0) c.go = arrive_and_wait(a.grid_cnt, (unsigned)G, a.wait_limit_ns, a.status) ? 1 : 0;
   __syncthreads();
-  if (!c.go) return;
+  if (!c.go) {
+    cluster_wait();
+    return;
+  }
 
   // ---- 4c. bases (CTAs before this one) and totals from every CTA's counts.
   // Chunks of 16 experts, NCP = NC rounded up to a power of two (<= 16):
@@ -569,37 +575,61 @@ __global__ void __launch_bounds__(FTHREADS, 1)
   const int lo = Nk + grp * per;
   const int hi = min(Tk, lo + per);
   for (int i = lo + tid; i < hi; i += FTHREADS) a.perm[i] = -1;
+  cluster_wait();
 }
 
-template <int NB64>
+template <int NB64, int TM>
+void fused_config(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr, int splits, int tiles,
+                  cudaStream_t st, bool pdl) {
+  cfg = {};
+  cfg.gridDim = dim3((unsigned)splits, (unsigned)tiles, 1);
+  cfg.blockDim = dim3(FTHREADS, 1, 1);
+  cfg.dynamicSmemBytes = FCfg<NB64, TM>::SMEM;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  if (pdl) set_pdl_attr(attr[1]);
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+}
+
+template <int NB64, int TM>
 cudaError_t launch_fused_nb(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
                             const FusedRouteArgs& a, int splits, cudaStream_t st, bool pdl) {
-  using C = FCfg<NB64>;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)splits, (unsigned)((a.T + FBM - 1) / FBM), 1);
-  cfg.blockDim = dim3(FTHREADS, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  if (pdl) {
-    set_pdl_attr(attr[0]);
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
-  return cudaLaunchKernelEx(&cfg, route_fused_kernel<NB64>, tm_x, tm_w, a);
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  fused_config<NB64, TM>(cfg, attr, splits, (a.T + TM - 1) / TM, st, pdl);
+  return cudaLaunchKernelEx(&cfg, route_fused_kernel<NB64, TM>, tm_x, tm_w, a);
 }
 
-template <int NB64>
-cudaError_t fused_setup_nb(int* per_sm) {
-  cudaError_t e = cudaFuncSetAttribute(route_fused_kernel<NB64>,
+// cluster sizes 1, 2, 4, 8 (the portable limit)
+constexpr int kSplitSizes[4] = {1, 2, 4, 8};
+
+template <int NB64, int TM>
+cudaError_t fused_setup_nb(int* clusters) {
+  cudaError_t e = cudaFuncSetAttribute(route_fused_kernel<NB64, TM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)FCfg<NB64>::SMEM);
+                                       (int)FCfg<NB64, TM>::SMEM);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, route_fused_kernel<NB64>, FTHREADS,
-                                                       FCfg<NB64>::SMEM);
+  for (int i = 0; i < 4; ++i) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    fused_config<NB64, TM>(cfg, attr, kSplitSizes[i], 1, nullptr, false);
+    clusters[i] = 0;
+    // a size the device refuses is simply never planned
+    if (cudaOccupancyMaxActiveClusters(&clusters[i], route_fused_kernel<NB64, TM>, &cfg) !=
+        cudaSuccess) {
+      clusters[i] = 0;
+      (void)cudaGetLastError();
+    }
+  }
+  return cudaSuccess;
 }
 
-int g_fused_per_sm[64][4];
+// [device][E bucket][tile height 64, 128][cluster size 1, 2, 4, 8]
+int g_fused_clusters[64][4][2][4];
 
 }  // namespace
 
@@ -607,29 +637,67 @@ cudaError_t route_fused_set_attributes() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int n[4] = {0, 0, 0, 0};
-  if ((e = fused_setup_nb<1>(&n[0])) != cudaSuccess) return e;
-  if ((e = fused_setup_nb<2>(&n[1])) != cudaSuccess) return e;
-  if ((e = fused_setup_nb<3>(&n[2])) != cudaSuccess) return e;
-  if ((e = fused_setup_nb<4>(&n[3])) != cudaSuccess) return e;
+  int n[4][2][4] = {};
+  if ((e = fused_setup_nb<1, 64>(n[0][0])) != cudaSuccess) return e;
+  if ((e = fused_setup_nb<1, 128>(n[0][1])) != cudaSuccess) return e;
+  if ((e = fused_setup_nb<2, 64>(n[1][0])) != cudaSuccess) return e;
+  if ((e = fused_setup_nb<2, 128>(n[1][1])) != cudaSuccess) return e;
+  if ((e = fused_setup_nb<3, 64>(n[2][0])) != cudaSuccess) return e;
+  if ((e = fused_setup_nb<3, 128>(n[2][1])) != cudaSuccess) return e;
+  if ((e = fused_setup_nb<4, 64>(n[3][0])) != cudaSuccess) return e;
+  if ((e = fused_setup_nb<4, 128>(n[3][1])) != cudaSuccess) return e;
   if (dev >= 0 && dev < 64)
-    for (int i = 0; i < 4; ++i) g_fused_per_sm[dev][i] = n[i];
+    for (int i = 0; i < 4; ++i)
+      for (int j = 0; j < 2; ++j)
+        for (int q = 0; q < 4; ++q) g_fused_clusters[dev][i][j][q] = n[i][j][q];
   return cudaSuccess;
 }
 
-int route_fused_resident_per_sm(int E) {
+bool route_fused_pick(int T, int H, int E, FusedRoutePlan* plan) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  return g_fused_per_sm[dev][(E + 63) / 64 - 1];
+  if (T <= 0 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  const int nb = (E + 63) / 64 - 1;
+  const long long npad = (E + 15) / 16 * 16;
+  const int KB = (H + FBK - 1) / FBK;
+  long long best = -1;
+  for (int j = 1; j >= 0; --j) {  // 128-token tiles first: ties keep them
+    const int tm = j ? 128 : 64;
+    const long long tiles = (T + tm - 1) / tm;
+    for (int i = 0; i < 4; ++i) {
+      const int S = kSplitSizes[i];
+      if (S > KB || tiles * S > kFusedMaxCtas) continue;
+      if (tiles > g_fused_clusters[dev][nb][j][i]) continue;  // not all in one wave
+      // bytes each CTA takes in (its K blocks of x rows and of W_router)
+      const long long cost = (long long)((KB + S - 1) / S) * (tm + npad);
+      if (best < 0 || cost < best) {
+        best = cost;
+        plan->tm = tm;
+        plan->splits = S;
+        plan->tiles = (int)tiles;
+      }
+    }
+  }
+  return best >= 0;
 }
 
 cudaError_t launch_route_fused(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                               const FusedRouteArgs& a, int splits, cudaStream_t st, bool pdl) {
-  switch ((a.E + 63) / 64) {
-    case 1: return launch_fused_nb<1>(tm_x, tm_w, a, splits, st, pdl);
-    case 2: return launch_fused_nb<2>(tm_x, tm_w, a, splits, st, pdl);
-    case 3: return launch_fused_nb<3>(tm_x, tm_w, a, splits, st, pdl);
-    default: return launch_fused_nb<4>(tm_x, tm_w, a, splits, st, pdl);
+                               const FusedRouteArgs& a, const FusedRoutePlan& plan,
+                               cudaStream_t st, bool pdl) {
+  const int nb = (a.E + 63) / 64;
+  const int S = plan.splits;
+  if (plan.tm == 64) {
+    switch (nb) {
+      case 1: return launch_fused_nb<1, 64>(tm_x, tm_w, a, S, st, pdl);
+      case 2: return launch_fused_nb<2, 64>(tm_x, tm_w, a, S, st, pdl);
+      case 3: return launch_fused_nb<3, 64>(tm_x, tm_w, a, S, st, pdl);
+      default: return launch_fused_nb<4, 64>(tm_x, tm_w, a, S, st, pdl);
+    }
+  }
+  switch (nb) {
+    case 1: return launch_fused_nb<1, 128>(tm_x, tm_w, a, S, st, pdl);
+    case 2: return launch_fused_nb<2, 128>(tm_x, tm_w, a, S, st, pdl);
+    case 3: return launch_fused_nb<3, 128>(tm_x, tm_w, a, S, st, pdl);
+    default: return launch_fused_nb<4, 128>(tm_x, tm_w, a, S, st, pdl);
   }
 }
 

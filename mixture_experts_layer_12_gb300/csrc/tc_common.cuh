@@ -251,6 +251,25 @@ __device__ __forceinline__ uint32_t dsmem_map(uint32_t local_saddr, uint32_t ran
   return r;
 }
 
+// Load 16 bytes from (possibly another CTA's) shared memory of the cluster.
+__device__ __forceinline__ float4 dsmem_ld_v4(uint32_t cluster_saddr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(cluster_saddr)
+               : "memory");
+  return v;
+}
+
+// Split cluster barrier: arrive (release: this thread's prior memory
+// operations, DSMEM loads included, are ordered before it) and wait.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Store 16 bytes into (possibly another CTA's) shared memory of the cluster.
 __device__ __forceinline__ void dsmem_st_v4(uint32_t cluster_saddr, float a, float b, float c,
                                             float d) {

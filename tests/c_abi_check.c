@@ -80,6 +80,7 @@ int main(void) {
                                        NULL) == MOE_ERR_UNSUPPORTED);
   CHECK(strstr(moe_last_error_string(), "scratch") != NULL);
   CHECK(moe_noalloc_device_status(NULL, NULL) == MOE_ERR_INVALID_ARG);
+  CHECK(moe_route_plan(&d, NULL, NULL) == MOE_ERR_INVALID_ARG);
 
   if (failures) return 1;
   printf("ok\n");

@@ -34,7 +34,7 @@ def exported_symbols(path):
 
 def test_exports_match_header(lib):
     decl = declared_symbols()
-    assert len(decl) == 18
+    assert len(decl) == 19
     assert decl == set(moe.EXPORTS)
     exported = {s for s in exported_symbols(moe.LIB_PATH) if s.startswith("moe_")}
     assert exported == decl
@@ -51,15 +51,15 @@ def _al(v, a=1024):
 
 
 def fused_route_bytes(T, H, E):
-    """The fused route's workspace regions (T > 128 or E > 64, at most 128
-    tiles of 128 tokens): per-CTA counts [ctas, E16] bytes and fp32 partial
-    logits [ctas, 128, E16], ctas <= min(tiles * min(12, H / 64), 256)."""
-    tiles = -(-T // 128)
-    if (T <= 128 and E <= 64) or tiles > 128:
+    """The fused route's workspace region (T > 128 or E > 64, at most 128
+    tiles of 128 tokens): per-CTA counts [ctas, E16] bytes, ctas <=
+    min(ceil(T / 64) * min(8, H / 64), 256) (64-token tiles, clusters of up
+    to 8 K splits)."""
+    if (T <= 128 and E <= 64) or -(-T // 128) > 128:
         return 0
-    ctas = min(tiles * min(12, -(-H // 64)), 256)
+    ctas = min(-(-T // 64) * min(8, -(-H // 64)), 256)
     e16 = -(-E // 16) * 16
-    return _al(ctas * e16) + _al(ctas * 128 * e16 * 4)
+    return _al(ctas * e16)
 
 
 def test_workspace_size_and_capacity_host_only(lib):
@@ -67,11 +67,11 @@ def test_workspace_size_and_capacity_host_only(lib):
     # status block + per-128-token expert counts + the fused route's regions
     # + h [T*k, F] + Y [T*k, H], bf16
     route = 1024 + 1024 + fused_route_bytes(4096, 4096, 8)
-    assert fused_route_bytes(4096, 4096, 8) == 4096 + 256 * 128 * 16 * 4
+    assert fused_route_bytes(4096, 4096, 8) == 4096
     assert moe.moe_workspace_size(s) == route + 8192 * 14336 * 2 + 8192 * 4096 * 2
     assert moe.moe_route_workspace_size(s) == route  # 32 tiles x 8 experts x 4 B of counts
     s3 = moe.make_shape(2048, 4096, 0, 128, 8)
-    assert moe.moe_route_workspace_size(s3) == 1024 + 16 * 128 * 4 + 192 * 128 + 192 * 128 * 128 * 4
+    assert moe.moe_route_workspace_size(s3) == 1024 + 16 * 128 * 4 + 256 * 128
     # past 128 tiles the route is router + dispatch kernels: no fused regions
     s4 = moe.make_shape(40000, 256, 0, 8, 2)
     assert moe.moe_route_workspace_size(s4) == 1024 + _al(313 * 8 * 4)

@@ -168,7 +168,7 @@ def test_router_sweep_full_size(k):
     inputs = moe_synth.make_inputs(cfg, with_ffn=False)
     r = gpu_route(cfg, to_dev(inputs))
     _, rep = routing_parity(cfg, inputs, r)
-    print(cfg.name, rep)
+    print(cfg.name, moe.moe_route_plan(moe.make_shape(cfg.T, cfg.H, 8, cfg.E, cfg.k)), rep)
 
 
 @pytest.mark.parametrize("T,E,k,cf", [(16384, 128, 2, None), (16384, 8, 1, 0.7),
@@ -198,6 +198,36 @@ def test_route_in_one_launch_gating_and_bias(gating, T, E, k):
     inputs = moe_synth.make_inputs(cfg, with_ffn=False)
     r = gpu_route(cfg, to_dev(inputs), gating)
     routing_parity(cfg, inputs, r, gating=gating)
+
+
+def test_route_plans_cover_tile_heights_and_splits():
+    # the one-launch route picks 64- or 128-token tiles and clusters of 1, 2,
+    # 4 or 8 K splits by shape; every pair these shapes select is checked
+    # against the oracle, and together they take both heights and all splits
+    shapes = [(300, 4096, 16, 2),    # few tiles, long K: 64-token tiles x 8
+              (2048, 1024, 8, 2),    # 16 tiles
+              (4096, 1024, 8, 2),    # 32 tiles
+              (8192, 1024, 64, 4),   # 64 tiles
+              (12000, 512, 8, 1),    # 94 tiles: one CTA each
+              (129, 64, 8, 2)]       # one K block: 64-token tiles, no split
+    seen = set()
+    for i, (T, H, E, k) in enumerate(shapes):
+        cfg = moe_synth.MoEConfig("plans", T=T, H=H, F=0, E=E, k=k, seed=40 + i)
+        plan = moe.moe_route_plan(moe.make_shape(T, H, 8, E, k))
+        assert plan[0] in (64, 128) and plan[1] in (1, 2, 4, 8), plan
+        seen.add(plan)
+        inputs = moe_synth.make_inputs(cfg, with_ffn=False)
+        r = gpu_route(cfg, to_dev(inputs))
+        _, rep = routing_parity(cfg, inputs, r)
+        print(T, H, E, k, plan, rep)
+    assert {tm for tm, _ in seen} == {64, 128}, seen
+    assert {sp for _, sp in seen} == {1, 2, 4, 8}, seen
+
+
+def test_route_plan_outside_the_fused_route():
+    # small batches and batches past 128 tiles of 128 tokens route otherwise
+    assert moe.moe_route_plan(moe.make_shape(32, 4096, 8, 8, 2)) == (0, 0)
+    assert moe.moe_route_plan(moe.make_shape(17000, 256, 8, 128, 4)) == (0, 0)
 
 
 def test_router_kernels_past_128_tiles_wide_experts():
