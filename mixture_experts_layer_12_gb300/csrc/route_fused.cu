@@ -16,9 +16,8 @@
 // the host so that every cluster fits in one wave):
 //   1. each CTA streams its K slice of the tile's x rows and of W_router by
 //      TMA (128-byte swizzle, a ring of up to 12 stages that fills shared
-//      memory) into one tcgen05.mma accumulator, 128 rows x E experts in
-//      TMEM (a 64-token tile loads 64 rows per A stage; the accumulator
-//      rows past them are never read);
+//      memory) into one tcgen05.mma accumulator of TM tokens x E experts in
+//      TMEM (M = TM: a 64-token tile runs the M = 64 form);
 //   2. it stages that fp32 partial in its own shared memory (the ring, idle
 //      after the MMAs); after one cluster barrier, rank s -- the owner of
 //      rows [TM s / S, TM (s+1) / S) of the tile -- reads those rows of the
@@ -44,7 +43,7 @@
 namespace moe {
 namespace {
 
-constexpr int FBM = 128;  // MMA rows (M); a tile holds TM = 64 or 128 tokens of them
+constexpr int FBM = 128;  // the largest tile (tokens); the MMA's M is the tile height
 constexpr int FBK = 64;
 constexpr int FTHREADS = 256;
 constexpr int FWARPS = FTHREADS / 32;
@@ -76,10 +75,7 @@ struct FPost {
 template <int NB64, int TM>
 struct FCfg {
   static_assert(TM == 64 || TM == 128, "tile height");
-  // A slot: the tile's TM rows of a 64-wide K block.  The MMA always reads
-  // 128 rows (M = 128): with TM = 64 its rows 64..127 come from whatever
-  // follows the slot in shared memory (the next slot, or the first B
-  // buffer), and the accumulator rows they feed are never read.
+  // A slot: the tile's TM rows of a 64-wide K block (the MMA's M = TM)
   static constexpr int A_BYTES = TM * FBK * 2;
   static constexpr int B_CHUNK = FBK * 64 * 2;  // 8 KB
   static constexpr int B_BYTES = NB64 * B_CHUNK;
@@ -89,7 +85,6 @@ struct FCfg {
   static constexpr int PIPE = STAGES * STAGE;
   static constexpr size_t SMEM = 1024 + (size_t)PIPE + sizeof(FCtrl);
   static_assert(SMEM <= (size_t)FSMEM_LIMIT, "shared memory");
-  static_assert(STAGES * A_BYTES + (FBM - TM) * FBK * 2 <= PIPE, "128-row A reads stay in the ring");
   // staged partial: TM rows of npad + 4 floats (16-byte rows, banks spread)
   static constexpr int STG_BYTES = TM * (NB64 * 64 + 4) * 4;
   static_assert(STG_BYTES % 16 == 0, "aligned post-MMA state");
@@ -213,7 +208,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
       fwait_drain(&c.full[m % C::STAGES], (uint32_t)((m / C::STAGES) & 1), a.wait_limit_ns,
                   a.status);
   } else if (warp == 1 && lane == 0) {
-    const uint32_t idesc = idesc_bf16_f32(FBM, a.npad, false, true);
+    const uint32_t idesc = idesc_bf16_f32(TM, a.npad, false, true);
     int stage = 0;
     uint32_t phase = 0;
     for (int i = 0; i < nkb; ++i) {
@@ -244,25 +239,27 @@ __global__ void __launch_bounds__(FTHREADS, 1)
   tc_fence_after();
   const bool have = ok && nkb > 0 && c.abort_flag == 0;
 
-  // ---- 2. the partial of the tile's TM rows into this CTA's shared memory
-  // (warps w and w+4 read TMEM lanes 32 (w % 4) .. +31, their lane quadrant,
-  // rows past TM skipped, and take alternate 16-column chunks, four loads in
-  // flight per wait)
+  // ---- 2. the partial of the tile's TM rows into this CTA's shared memory.
+  // Warps w and w+4 read TMEM lanes 32 (w % 4) .. +31 (their lane quadrant)
+  // and take alternate 16-column chunks, four loads in flight per wait.  The
+  // accumulator of an M = 128 MMA holds row r in lane r; that of M = 64 holds
+  // row r in lane 32 (r / 16) + r % 16 (lanes 16..31 of a quadrant unused).
   const int sp = a.npad + 4;  // staging row pitch (floats)
   const int v4 = a.npad / 4;  // float4 per row
   {
     const int q = warp & 3;
-    if (q * 32 < TM) {
-      const int h = warp >> 2;
-      const int row = q * 32 + lane;
-      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16);
-      const int nch = a.npad / 16;
-      for (int c0 = h; c0 < nch; c0 += 8) {
-        uint32_t v[4][16];
+    const int h = warp >> 2;
+    const int row = TM == 128 ? q * 32 + lane : q * 16 + lane;
+    const bool holds = TM == 128 || lane < 16;
+    const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16);
+    const int nch = a.npad / 16;
+    for (int c0 = h; c0 < nch; c0 += 8) {
+      uint32_t v[4][16];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (c0 + 2 * u < nch) tmem_ld_x16(tb + (uint32_t)((c0 + 2 * u) * 16), v[u]);
-        tmem_ld_wait();
+      for (int u = 0; u < 4; ++u)
+        if (c0 + 2 * u < nch) tmem_ld_x16(tb + (uint32_t)((c0 + 2 * u) * 16), v[u]);
+      tmem_ld_wait();
+      if (holds) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           if (c0 + 2 * u < nch) {
