@@ -48,8 +48,8 @@ NCU_TRAFFIC = {
     "prefill/expert_gemm1": {"bytes": 1032561408 + 221230080, "src": "ffn_gemm.cu", "src_sha": "9c589b4d85665278"},
     "prefill/expert_gemm2": {"bytes": 1429054976 + 60358144, "src": "ffn_gemm.cu", "src_sha": "9c589b4d85665278"},
     # router sweep, k = 1: the fused route (router + dispatch in one kernel) of one call
-    "router_k1/router+dispatch": {"bytes": 17904896 + 0, "src": ["route_fused.cu", "route_topk.cuh"],
-                                  "src_sha": ["c59dd470e0e349a5", "ee199279a3609b01"]},
+    "router_k1/router+dispatch": {"bytes": 17898496 + 0, "src": ["route_fused.cu", "route_topk.cuh"],
+                                  "src_sha": ["a7321e97027ef3df", "ee199279a3609b01"]},
     # decode workload: both GEMMs on the small-batch kernel
     "decode/expert_gemm1": {"bytes": 940161024 + 3989760, "src": "ffn_gemm_small.cu", "src_sha": "ff59fa4c79617713"},
     "decode/expert_gemm2": {"bytes": 941419776 + 5054208, "src": "ffn_gemm_small.cu", "src_sha": "ff59fa4c79617713"},
