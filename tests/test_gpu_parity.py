@@ -224,6 +224,21 @@ def test_route_plans_cover_tile_heights_and_splits():
     assert {sp for _, sp in seen} == {1, 2, 4, 8}, seen
 
 
+@pytest.mark.parametrize("T,H,E,k", [(1, 1000, 128, 8), (63, 1000, 96, 2), (65, 1000, 96, 3),
+                                     (191, 1000, 200, 4), (320, 1000, 72, 2), (2100, 1000, 128, 1)])
+def test_route_ragged_tokens_and_k_blocks(T, H, E, k):
+    # the one-launch route at token counts off the 64- and 128-token tiles and
+    # with H = 1000 (a last K block of 40 columns, zero-filled by TMA), so the
+    # K splits of a cluster hold different numbers of K blocks
+    cfg = moe_synth.MoEConfig("ragged", T=T, H=H, F=0, E=E, k=k, seed=50)
+    plan = moe.moe_route_plan(moe.make_shape(T, H, 8, E, k))
+    assert plan != (0, 0), plan
+    inputs = moe_synth.make_inputs(cfg, with_ffn=False)
+    r = gpu_route(cfg, to_dev(inputs))
+    _, rep = routing_parity(cfg, inputs, r)
+    print(T, H, E, k, plan, rep)
+
+
 def test_route_plan_outside_the_fused_route():
     # small batches and batches past 128 tiles of 128 tokens route otherwise
     assert moe.moe_route_plan(moe.make_shape(32, 4096, 8, 8, 2)) == (0, 0)
