@@ -413,7 +413,9 @@ def measure_route(args, cfg, device, with_cpu=True):
     torch.cuda.synchronize(device)
     graph.replay()
     torch.cuda.synchronize(device)
-    reps = max(1, args.steps // copies)
+    # at least three replays back to back, so that one replay's launch
+    # latency does not sit in the per-route time of a short run
+    reps = max(3, args.steps // copies)
     K = reps * copies
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     clocks = ClockSampler(gpu_id_for(device))
