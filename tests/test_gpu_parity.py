@@ -372,6 +372,8 @@ def test_forward_skewed_sampled(cfg):
     (129, 256, 264, 4, 3, None, 1.0),       # four experts, tensor-core router
     (300, 136, 200, 6, 4, 0.8, None),       # six experts, drops
     (500, 256, 256, 13, 2, None, None),     # thirteen experts
+    (190, 1000, 264, 96, 2, None, None),    # one-launch route, 64-token tiles x 8 K splits, ragged K
+    (2100, 1024, 256, 128, 1, 1.1, None),   # 64-token tiles x 4 splits, k = 1 combine in GEMM2, drops
 ])
 def test_forward_edge_shapes(T, H, F, E, k, cf, bias):
     cfg = moe_synth.MoEConfig("edge", T=T, H=H, F=F, E=E, k=k, seed=21, capacity_factor=cf,
