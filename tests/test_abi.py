@@ -191,6 +191,20 @@ def test_forward_plan_is_a_host_only_shape_rule(lib):
     assert lib.moe_forward_plan(ctypes.byref(good), None, ctypes.byref(c)) == moe.MOE_ERR_INVALID_ARG
 
 
+def test_route_plan_validates_before_the_device(lib):
+    # bad shapes and null outputs are refused on the host; a good shape needs
+    # a device (without one the call reports a CUDA error, never a crash)
+    tm, sp = ctypes.c_int32(-1), ctypes.c_int32(-1)
+    bad = moe.make_shape(64, 100, 256, 8, 2)  # H not a multiple of 8
+    assert lib.moe_route_plan(ctypes.byref(bad), ctypes.byref(tm), ctypes.byref(sp)) == moe.MOE_ERR_UNSUPPORTED
+    good = moe.make_shape(2048, 4096, 0, 128, 1)
+    assert lib.moe_route_plan(ctypes.byref(good), None, ctypes.byref(sp)) == moe.MOE_ERR_INVALID_ARG
+    import torch
+    if not torch.cuda.is_available():
+        rc = lib.moe_route_plan(ctypes.byref(good), ctypes.byref(tm), ctypes.byref(sp))
+        assert rc == moe.MOE_ERR_CUDA and (tm.value, sp.value) == (0, 0)
+
+
 def test_plain_c_caller(lib, tmp_path):
     # tests/c_abi_check.c: a C program built with gcc against include/moe.h
     # and linked to libmoe.so, calling the host-answered entry points
